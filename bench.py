@@ -1,0 +1,377 @@
+"""Benchmark of the fused MoE expert block on GB300.
+
+One step = one forward of the whole block (dispatch, quant, GEMM1 + SwiGLU,
+requant, GEMM2, combine, shared expert) on one batch of the decode workload
+(bs 8 = 4 requests x 2 rows, h 4096, 256 experts, top-8, I 2048, shared
+expert), with weights and inputs already resident in HBM.  Prints one JSON
+line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU (torchrun): each rank runs an independent replica on its own batch
+(no collective on the data path; weak scaling); the timed region is bracketed
+by a barrier and the max over ranks is reported.
+
+`--impl reference` times the CPU oracle on the host cores on a bounded sample
+of the same workload (the only other reference available for this block).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE block tokens/s and µs/forward at 1 GB300; % of HBM / INT8 roofline"
+PROFILES = os.path.join(ROOT, "profiles")
+GEMM_SRC = os.path.join(ROOT, "moe_expert_ffn_dispatch_gb300", "csrc", "grouped_gemm.cu")
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_sha() -> str:
+    with open(GEMM_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per GEMM1 launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(PROFILES, "gemm1_swiglu_%s.md" % workload)
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m1 = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    m2 = re.search(r"kernel_sha:\s*([0-9a-f]+)", txt)
+    if not m1 or not m2 or m2.group(1) != kernel_sha():
+        return None
+    return int(m1.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active"
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], 0
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                reasons |= int(parts[3], 16)
+            except (ValueError, IndexError):
+                continue
+        names = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+                 0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+                 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+        rs = [n for b, n in names.items() if reasons & b]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": rs, "samples": len(sm)}
+
+
+def algorithmic_bytes(wl, counts_per_expert, n_active):
+    """Bytes each kernel must move at least once (the roofline numerator).
+
+    Per touched expert (routed experts with >= 1 row, plus the shared expert
+    when it has rows): GEMM1 reads its W1 (2I*h int8) and scales (2I fp32);
+    GEMM2 reads W2 (h*I int8) and scales (h fp32).  Activations: x (bf16), ids
+    and scales, outputs; token-row traffic of the GEMMs is counted per row.
+    Scratch that a fused kernel could keep on chip is not counted."""
+    h, I, K, bs = wl.hidden, wl.inter, wl.topk, wl.bs
+    touched = sum(1 for c in counts_per_expert if c > 0) + (1 if (wl.has_shared and n_active > 0) else 0)
+    R = sum(counts_per_expert)
+    rows = R + (n_active if wl.has_shared else 0)
+    gemm1 = touched * (2 * I * h + 4 * 2 * I) + rows * h + rows * I * 4
+    gemm2 = touched * (h * I + 4 * h) + rows * I + rows * 4 + R * h * 2 + (n_active * h * 2 if wl.has_shared else 0)
+    step = touched * (2 * I * h + h * I + 4 * (2 * I + h)) + bs * h * 2 + bs * K * 8 + \
+        bs * h * 2 * (2 if wl.has_shared else 1) + wl.num_experts * 4
+    int_ops = 2 * rows * (2 * I * h + h * I)
+    return {"gemm1": gemm1, "gemm2": gemm2, "step": step, "int_ops": int_ops, "touched_experts": touched,
+            "rows": rows}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, wl, ws, rank, local):
+    import moe_expert_ffn_dispatch_gb300 as m
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        torch.distributed.init_process_group("nccl")
+    # each rank runs its own batch (seed + rank) through the same replicated weights
+    wl_r = synth.Workload(**{**wl.__dict__, "seed": wl.seed + 7919 * rank})
+    inp = synth.make_inputs(wl_r, with_weights=False)
+    base = synth.make_inputs(wl, with_weights=False)
+    weights = {"w1": synth.draw_all_w1(wl, dev), "w1_scale": base.w1_scale.to(dev),
+               "w2": synth.draw_all_w2(wl, dev), "w2_scale": base.w2_scale.to(dev)}
+    if wl.has_shared:
+        weights.update(share_w1=synth.draw_w1(wl, wl.num_experts, dev), share_w1_scale=base.share_w1_scale.to(dev),
+                       share_w2=synth.draw_w2(wl, wl.num_experts, dev), share_w2_scale=base.share_w2_scale.to(dev))
+    if base.smooth is not None:
+        weights["smooth"] = base.smooth.to(dev)
+    if base.share_smooth is not None:
+        weights["share_smooth"] = base.share_smooth.to(dev)
+    di = {"x": inp.x.to(dev), "expert_ids": inp.expert_ids.to(dev), "expert_scales": inp.expert_scales.to(dev)}
+    if inp.mask is not None:
+        di["mask"] = inp.mask.to(dev)
+
+    blk = m.MoeFused(wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter, wl.has_shared, dev)
+    stream = torch.cuda.current_stream(dev)
+    out, sout, nums = blk.forward_inputs(di, weights)
+    torch.cuda.synchronize()
+    st = blk.status()
+    if st["rc"] != 0:
+        raise RuntimeError("forward status %s" % st)
+    counts = nums.cpu().tolist()
+    n_active = int(inp.mask.sum()) if inp.mask is not None else wl.bs
+    alg = algorithmic_bytes(wl, counts, n_active)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    # ---- device-resident timing (value), with per-kernel events on the launch stream
+    for _ in range(args.warmup):
+        blk.forward_inputs(di, weights, out=out, share_out=sout, token_nums=nums)
+    torch.cuda.synchronize()
+    blk.set_timing(True)
+    blk.get_timing()  # clear
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            blk.forward_inputs(di, weights, out=out, share_out=sout, token_nums=nums)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    ktimes = blk.get_timing()
+    blk.set_timing(False)
+    if blk.status()["rc"] != 0:
+        raise RuntimeError("device status after the timed loop: %s" % blk.status())
+    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_total = float(t.item())
+    launches = sum(n for _, n in ktimes.values())
+
+    # ---- end to end through the public API: host inputs in, host results out
+    pin = {k: v.cpu().pin_memory() for k, v in di.items()}
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    h_sout = torch.empty_like(sout, device="cpu").pin_memory() if sout is not None else None
+    h_nums = torch.empty_like(nums, device="cpu").pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = h_out.numel() * 2 + (h_sout.numel() * 2 if h_sout is not None else 0) + h_nums.numel() * 4
+
+    def e2e_step():
+        for k, v in pin.items():
+            di[k].copy_(v, non_blocking=True)
+        blk.forward_inputs(di, weights, out=out, share_out=sout, token_nums=nums)
+        h_out.copy_(out, non_blocking=True)
+        if h_sout is not None:
+            h_sout.copy_(sout, non_blocking=True)
+        h_nums.copy_(nums, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 200))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    t1 = time.perf_counter()
+    barrier()
+    te = torch.tensor([t1 - t0], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_s = float(te.item())
+
+    peaks, peak_kind = measured_peaks()
+    g1_ms, g1_n = ktimes["gemm1_swiglu"]
+    g1_avg_s = g1_ms / max(g1_n, 1) / 1e3
+    achieved = alg["gemm1"] / g1_avg_s / 1e9
+    traffic = recorded_traffic(wl.name)
+    step_s = ms_total / args.steps / 1e3
+    tokens = wl.bs * ws
+    res = {
+        "metric": METRIC,
+        "value": tokens * args.steps / (ms_total / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_total / args.steps,
+        "us_per_forward": ms_total / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8",
+        "data": "synthetic (seeded counter-hash inputs, random-init int8 weights)",
+        "config": {"workload": wl.name, "bs": wl.bs, "hidden": wl.hidden, "experts": wl.num_experts,
+                   "topk": wl.topk, "inter": wl.inter, "shared_expert": wl.has_shared,
+                   "touched_experts": alg["touched_experts"], "rows": alg["rows"],
+                   "l2": "inputs larger than L2 (%.2f GB of touched weights per step vs 0.13 GB L2)" % (alg["step"] / 1e9),
+                   "parallelism": "replicas x%d (independent batches, no collective)" % ws},
+        "roofline": {"bound": "hbm", "kernel": "gemm1_swiglu", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "alg_bytes_per_launch": alg["gemm1"], "avg_launch_us": g1_avg_s * 1e6},
+        "roofline_step": {"bound": "hbm", "alg_bytes": alg["step"], "achieved": alg["step"] / step_s / 1e9,
+                          "frac": alg["step"] / step_s / 1e9 / peaks["hbm_gbs"], "unit": "GB/s"},
+        "kernels_us": {k: (v[0] / max(v[1], 1) * 1e3) for k, v in ktimes.items()},
+        "gpu_launches": launches,
+        "e2e": {"value": tokens * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return res if rank == 0 else None
+
+
+# ---------------------------------------------------------------- oracle arms
+def _oracle_setup(wl):
+    import oracle
+    inp = synth.make_inputs(wl, with_weights=False)
+    cache = {}
+    need = synth.touched_experts(inp.expert_ids, wl.num_experts, inp.mask)
+    for e in need + ([wl.num_experts] if wl.has_shared else []):
+        cache[e] = (synth.draw_w1(wl, e), synth.draw_w2(wl, e))
+    return oracle, inp, cache
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    """The oracle as it stands, on the host cores, on a bounded sample: whole
+    forwards of the workload repeated until about `budget_s` of CPU time."""
+    oracle, inp, cache = _oracle_setup(wl)
+    threads = os.cpu_count() or 1
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.forward(inp, threads=threads, expert_weights=lambda e: cache[e])
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": wl.bs * n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "%d full forwards of %s (bs %d), weights pre-drawn on the host" % (n, wl.name, wl.bs)}
+
+
+def run_reference(args, wl, ws, rank):
+    if rank != 0:
+        return None
+    oracle, inp, cache = _oracle_setup(wl)
+    threads = os.cpu_count() or 1
+    bs = wl.bs
+    # each step: one token of the batch (cycling), so K + W steps stay within minutes
+    samples = []
+    for i in range(bs):
+        s = torch.zeros(bs, dtype=torch.bool)
+        s[i] = True
+        samples.append(s)
+
+    def step(i):
+        oracle.forward(inp, threads=threads, token_sample=samples[i % bs], expert_weights=lambda e: cache[e])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    v = args.steps / dt
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic", "config": {"workload": wl.name, "bs": wl.bs},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": "one token of %s per step (its %d routed rows + shared row)" % (wl.name, wl.topk)},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="decode8", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = dist_env()
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        res = run_reference(args, wl, ws, rank)
+    else:
+        res = run_ours(args, wl, ws, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/* moe_fused.h -- C ABI of the GB300 fused MoE expert block.
+ *
+ * The block (FusedDeepMoE analysis, §1.2 operator signature and §9.1 the
+ * DeepSeek-style MoE it implements) computes, on one GPU, for a batch of bs
+ * tokens already routed by an external router:
+ *
+ *   dispatch   counting sort of the active (token, k) pairs by expert
+ *              (§4.1 local token counting and the prefix-sum expand index);
+ *   quant      per-token dynamic INT8 quantisation of x (§4.1, §7.3);
+ *   GEMM1      grouped INT8 x INT8 -> INT32, dequantised by per-output-channel
+ *              x per-token FP32 scales, SwiGLU (§3.3, §6.1);
+ *   requant    per-row dynamic INT8 quantisation of the SwiGLU output (§7.2);
+ *   GEMM2      grouped INT8 GEMM, dequantised to bf16 (§3.4, §6.2);
+ *   combine    output[t] = sum_k expert_scales[t,k] * row(t,k), in fp32,
+ *              k ascending, rounded once to bf16 (§4.2 LocalWindowCopy);
+ *   shared     an optional shared expert on every active token, written to
+ *              share_output.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise; all are
+ *     owned by the caller.  The library allocates no device memory and never
+ *     copies weights; it owns only the host-side handle.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is enqueued asynchronously; only argument checks are synchronous.
+ *   - Return 0 on success or a negative MOE_ERR_* code.  A call that returns an
+ *     error before launching leaves every output untouched.
+ *   - Tensors are dense, row-major, with the innermost dimension contiguous.
+ *     Every pointer must be 16-byte aligned.
+ */
+#ifndef MOE_FUSED_H
+#define MOE_FUSED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)          /* NULL where a tensor is required, bad count, bad handle  */
+#define MOE_ERR_UNSUPPORTED_SHAPE (-2)    /* shape outside the limits below                           */
+#define MOE_ERR_WORKSPACE_TOO_SMALL (-3)  /* workspace_bytes below what create() reported             */
+#define MOE_ERR_CUDA (-4)                 /* a CUDA runtime call failed (launch, attribute, memcpy)  */
+#define MOE_ERR_DEVICE_TIMEOUT (-5)       /* a bounded in-kernel wait gave up (see get_status)        */
+#define MOE_ERR_UNIMPLEMENTED (-6)
+#define MOE_ERR_ALIGNMENT (-7)            /* a pointer is not 16-byte aligned                          */
+
+/* Static shape of one block.  Limits: 1 <= hidden, inter <= 16384 and both
+ * multiples of 64; 1 <= num_experts <= 1024; 1 <= topk <= min(num_experts, 16);
+ * 0 <= bs_max <= 65536.  GEMM1 has N = 2*inter outputs (gate rows 0..inter-1,
+ * up rows inter..2*inter-1); GEMM2 maps inter -> hidden.  `flags` is reserved
+ * and must be 0.  The pages' supported ranges (§9.4) are not enforced. */
+typedef struct {
+  int32_t bs_max;
+  int32_t hidden;
+  int32_t num_experts;
+  int32_t topk;
+  int32_t inter;
+  int32_t has_shared;
+  int32_t flags;
+} moe_fused_config_t;
+
+/* Per-call tensors, following the operator signature (§1.2):
+ *   x                  [bs, hidden] bf16
+ *   expert_ids         [bs, topk] int32; a pair whose id is outside
+ *                      [0, num_experts) is skipped (not counted, adds nothing)
+ *   expert_scales      [bs, topk] fp32 routing weights
+ *   gmm1_weight        [num_experts, 2*inter, hidden] int8, K (hidden) contiguous
+ *   gmm1_weight_scale  [num_experts, 2*inter] fp32 per output channel
+ *   gmm2_weight        [num_experts, hidden, inter] int8, K (inter) contiguous
+ *   gmm2_weight_scale  [num_experts, hidden] fp32
+ *   share_gmm1_weight / _scale   [2*inter, hidden] / [2*inter]  (has_shared)
+ *   share_gmm2_weight / _scale   [hidden, inter] / [hidden]     (has_shared)
+ *   expert_smooth_scales  [hidden] fp32 or NULL: multiplies x per channel
+ *                      before the routed experts' quant
+ *   share_smooth_scales   [hidden] fp32 or NULL: same for the shared expert
+ *   x_active_mask      [bs] bool (one byte, 0 = inactive) or NULL (all active);
+ *                      inactive tokens are not dispatched and get zero rows in
+ *                      output and share_output
+ * Outputs:
+ *   output             [bs, hidden] bf16
+ *   share_output       [bs, hidden] bf16, required iff has_shared, else NULL
+ *   expert_token_nums  [num_experts] int32: rows each expert received (counts,
+ *                      not a prefix sum)
+ * bs: 0 <= bs <= bs_max.  bs == 0 zeroes expert_token_nums and leaves the other
+ * outputs untouched. */
+typedef struct {
+  const void* x;
+  const int32_t* expert_ids;
+  const float* expert_scales;
+  const int8_t* gmm1_weight;
+  const float* gmm1_weight_scale;
+  const int8_t* gmm2_weight;
+  const float* gmm2_weight_scale;
+  const int8_t* share_gmm1_weight;
+  const float* share_gmm1_weight_scale;
+  const int8_t* share_gmm2_weight;
+  const float* share_gmm2_weight_scale;
+  const float* expert_smooth_scales;
+  const float* share_smooth_scales;
+  const uint8_t* x_active_mask;
+  void* output;
+  void* share_output;
+  int32_t* expert_token_nums;
+  int32_t bs;
+} moe_fused_args_t;
+
+/* Device-side status of the last forward that used a workspace. */
+typedef struct {
+  int32_t skipped_pairs;   /* active pairs whose expert id was outside [0, E) */
+  int32_t error_flags;     /* bit 0: an in-kernel wait gave up                 */
+  int32_t error_site;      /* which wait gave up (kernel id * 16 + site)       */
+  int32_t dispatched_rows; /* R: routed rows dispatched                        */
+  int32_t shared_rows;     /* S: rows run through the shared expert            */
+  int32_t active_slots;    /* experts with at least one row (+1 for shared)    */
+  int32_t reserved[2];
+} moe_fused_status_t;
+
+typedef struct moe_fused_handle moe_fused_handle_t;
+
+/* Validate `cfg`, allocate the host handle and report the workspace size in
+ * bytes (device memory the caller allocates, 256-byte aligned, and passes to
+ * every forward).  The device current at this call is the device the handle
+ * launches on.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, CUDA. */
+int moe_fused_create(const moe_fused_config_t* cfg, moe_fused_handle_t** out_handle,
+                     size_t* workspace_bytes);
+
+/* Workspace bytes for `cfg` without creating a handle. */
+int moe_fused_workspace_size(const moe_fused_config_t* cfg, size_t* workspace_bytes);
+
+/* Enqueue one forward of the block on `stream`.  `workspace` must hold at least
+ * the reported bytes; its contents need no initialisation and are overwritten.
+ * Two forwards that share a workspace must be ordered on the GPU.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE (bs > bs_max), WORKSPACE_TOO_SMALL,
+ * ALIGNMENT, CUDA (launch failure). */
+int moe_fused_forward(moe_fused_handle_t* handle, const moe_fused_args_t* args, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream` and read the status words of the last forward that used
+ * `workspace` into *out (host memory).  Returns DEVICE_TIMEOUT if a wait gave
+ * up, otherwise 0 (or CUDA). */
+int moe_fused_get_status(moe_fused_handle_t* handle, const void* workspace, void* stream,
+                         moe_fused_status_t* out);
+
+/* Free the handle (no device memory is owned).  NULL is accepted. */
+int moe_fused_destroy(moe_fused_handle_t* handle);
+
+/* Static string for an error code. */
+const char* moe_fused_strerror(int code);
+
+/* ---- per-kernel timing (used by the benchmark) ---------------------------
+ * With timing enabled, forward brackets each kernel launch with CUDA events on
+ * `stream`.  get_timing synchronises the recorded events, writes for each
+ * kernel id k < max_kernels the summed milliseconds ms[k] and launch count
+ * launches[k] (host arrays), returns the number of kernel ids, and clears the
+ * record.  Kernel ids: 0 dispatch, 1 quant, 2 gemm1, 3 requant, 4 gemm2,
+ * 5 combine. */
+int moe_fused_set_timing(moe_fused_handle_t* handle, int enable);
+int moe_fused_get_timing(moe_fused_handle_t* handle, float* ms, int32_t* launches, int max_kernels);
+const char* moe_fused_kernel_name(int kernel_id);
+
+/* ---- test-only entry points (prefix moe_fused_debug_) -------------------
+ * Workspace regions, so a test can read the intermediates of the last forward
+ * or plant inputs for a single stage.  Region ids:
+ *   0 status  1 counts [E]  2 offsets [E+1]  3 row_of [bs*topk]
+ *   4 tk_of_row [bs*topk]  5 active tokens [bs]  6 x_q [bs_max,h] int8
+ *   7 x_scale [bs_max] f32  8 xs_q [bs_max,h] int8  9 xs_scale [bs_max]
+ *   10 h [rows,inter] f32  11 x2 [rows,inter] int8  12 s2 [rows] f32
+ *   13 y2 [bs_max*topk,h] bf16 (aliases region 10)  14 slot table
+ * `rows` = bs*topk + bs: routed row r at index r (r < R), the shared expert's
+ * i-th active token at index bs*topk + i.  Writes *offset and *bytes. */
+int moe_fused_debug_region(moe_fused_handle_t* handle, int region, size_t* offset, size_t* bytes);
+
+/* Phase-stop forward: enqueue kernels 0..last_kernel of the forward (kernel
+ * ids as for get_timing) and stop, so that a test can read the intermediates
+ * of that stage before a later stage reuses their space (h is overwritten by
+ * y2 in GEMM2).  Same arguments, checks and errors as moe_fused_forward. */
+int moe_fused_debug_forward_until(moe_fused_handle_t* handle, const moe_fused_args_t* args, void* workspace,
+                                  size_t workspace_bytes, int last_kernel, void* stream);
+
+/* Run one grouped GEMM with a raw INT32 epilogue on the dispatch state and
+ * operands currently in `workspace` (left by a forward with the same args):
+ * which = 1: acc1[r, n] = sum_c xq(r)[c] * W1[e(r)][n][c] for every row
+ *            r of the routed and shared groups, n < 2*inter;
+ * which = 2: acc2[r, j] = sum_i x2[r][i] * W2[e(r)][j][i], j < hidden.
+ * `acc` is a device int32 buffer [rows, N] (rows as for region 10); rows not
+ * dispatched are left untouched. */
+int moe_fused_debug_gemm_acc(moe_fused_handle_t* handle, const moe_fused_args_t* args, void* workspace,
+                             size_t workspace_bytes, int which, int32_t* acc, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FUSED_H */

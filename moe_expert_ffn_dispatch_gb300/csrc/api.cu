@@ -1,0 +1,343 @@
+// C ABI of the fused MoE expert block: argument checks, workspace planning,
+// launch sequence, per-kernel timing and the test-only entry points.
+//
+// Launch sequence of one forward (the pages' Process(): dispatch, GMM1 with
+// SwiGLU + quant, GMM2, combine -- FusedDeepMoE analysis §3.2):
+//   dispatch (1 CTA) -> quant (1 CTA per token) -> GEMM1 + SwiGLU (persistent)
+//   -> requant (persistent) -> GEMM2 + bf16 dequant (persistent) -> combine.
+// Kernel boundaries carry the dependencies; no kernel waits on another.
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "moe_fused.h"
+#include "moe_internal.h"
+
+struct TimingRecord {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+
+struct moe_fused_handle {
+  moe_fused_config_t cfg;
+  int device;
+  int num_sms;
+  moe::WsLayout L;
+  bool timing;
+  std::vector<TimingRecord> records;
+  std::vector<cudaEvent_t> pool;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+int check_config(const moe_fused_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->flags != 0) return MOE_ERR_INVALID_ARG;
+  if (c->hidden < 64 || c->hidden > 16384 || c->hidden % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->inter < 64 || c->inter > 16384 || c->inter % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->num_experts < 1 || c->num_experts > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->topk < 1 || c->topk > 16 || c->topk > c->num_experts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->bs_max < 0 || c->bs_max > 65536) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->has_shared != 0 && c->has_shared != 1) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe::WsLayout plan(const moe_fused_config_t& c) {
+  moe::WsLayout L{};
+  const size_t bs = static_cast<size_t>(c.bs_max), E = static_cast<size_t>(c.num_experts);
+  const size_t h = static_cast<size_t>(c.hidden), I = static_cast<size_t>(c.inter), K = static_cast<size_t>(c.topk);
+  const size_t routed = bs * K;
+  const size_t rows = routed + (c.has_shared ? bs : 0);
+  size_t off = 0;
+  auto take = [&](size_t& field, size_t bytes, int id) {
+    field = off;
+    L.sizes[id] = bytes;
+    off = align_up(off + (bytes ? bytes : 1));
+  };
+  take(L.status, 64 * sizeof(int32_t), 0);
+  take(L.counts, E * 4, 1);
+  take(L.offsets, (E + 1) * 4, 2);
+  take(L.row_of, routed * 4, 3);
+  take(L.tk_of_row, routed * 4, 4);
+  take(L.active, bs * 4, 5);
+  take(L.x_q, bs * h, 6);
+  take(L.x_scale, bs * 4, 7);
+  take(L.xs_q, c.has_shared ? bs * h : 0, 8);
+  take(L.xs_scale, c.has_shared ? bs * 4 : 0, 9);
+  const size_t hbytes = rows * I * 4, ybytes = routed * h * 2;
+  take(L.hbuf, hbytes > ybytes ? hbytes : ybytes, 10);
+  take(L.x2, rows * I, 11);
+  take(L.s2, rows * 4, 12);
+  L.y2 = L.hbuf;
+  L.sizes[13] = ybytes;
+  take(L.slots, static_cast<size_t>(moe::SlotTable::words(c.num_experts)) * 4, 14);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int build_params(moe_fused_handle* hd, const moe_fused_args_t* a, void* ws, size_t ws_bytes, moe::FwdParams* p) {
+  if (!hd || !a) return MOE_ERR_INVALID_ARG;
+  const moe_fused_config_t& c = hd->cfg;
+  if (a->bs < 0 || a->bs > c.bs_max) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < hd->L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_ALIGNMENT;
+  if (!a->expert_token_nums) return MOE_ERR_INVALID_ARG;
+  if (a->bs > 0) {
+    if (!a->x || !a->expert_ids || !a->expert_scales || !a->gmm1_weight || !a->gmm1_weight_scale ||
+        !a->gmm2_weight || !a->gmm2_weight_scale || !a->output)
+      return MOE_ERR_INVALID_ARG;
+    if (c.has_shared) {
+      if (!a->share_gmm1_weight || !a->share_gmm1_weight_scale || !a->share_gmm2_weight ||
+          !a->share_gmm2_weight_scale || !a->share_output)
+        return MOE_ERR_INVALID_ARG;
+    } else if (a->share_output) {
+      return MOE_ERR_INVALID_ARG;
+    }
+    const void* ptrs[] = {a->x, a->expert_ids, a->expert_scales, a->gmm1_weight, a->gmm1_weight_scale,
+                          a->gmm2_weight, a->gmm2_weight_scale, a->share_gmm1_weight, a->share_gmm1_weight_scale,
+                          a->share_gmm2_weight, a->share_gmm2_weight_scale, a->expert_smooth_scales,
+                          a->share_smooth_scales, a->x_active_mask, a->output, a->share_output,
+                          a->expert_token_nums};
+    for (const void* q : ptrs)
+      if (q && !aligned16(q)) return MOE_ERR_ALIGNMENT;
+  }
+  std::memset(p, 0, sizeof(*p));
+  p->bs = a->bs;
+  p->h = c.hidden;
+  p->E = c.num_experts;
+  p->topk = c.topk;
+  p->I = c.inter;
+  p->has_shared = c.has_shared;
+  p->share_uses_xq = c.has_shared && (a->expert_smooth_scales == a->share_smooth_scales);
+  p->x = static_cast<const uint16_t*>(a->x);
+  p->ids = a->expert_ids;
+  p->scales = a->expert_scales;
+  p->w1 = a->gmm1_weight;
+  p->w1s = a->gmm1_weight_scale;
+  p->w2 = a->gmm2_weight;
+  p->w2s = a->gmm2_weight_scale;
+  p->sw1 = a->share_gmm1_weight;
+  p->sw1s = a->share_gmm1_weight_scale;
+  p->sw2 = a->share_gmm2_weight;
+  p->sw2s = a->share_gmm2_weight_scale;
+  p->smooth = a->expert_smooth_scales;
+  p->ssmooth = a->share_smooth_scales;
+  p->mask = a->x_active_mask;
+  p->out = static_cast<uint16_t*>(a->output);
+  p->sout = static_cast<uint16_t*>(a->share_output);
+  p->token_nums = a->expert_token_nums;
+  p->ws = static_cast<char*>(ws);
+  p->L = hd->L;
+  return MOE_OK;
+}
+
+cudaEvent_t take_event(moe_fused_handle* hd) {
+  if (!hd->pool.empty()) {
+    cudaEvent_t e = hd->pool.back();
+    hd->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Launch `fn` bracketed by timing events when enabled.
+template <typename F>
+cudaError_t timed(moe_fused_handle* hd, int kernel, cudaStream_t s, F fn) {
+  if (!hd->timing) return fn();
+  TimingRecord r{kernel, take_event(hd), take_event(hd)};
+  if (!r.start || !r.stop) return cudaErrorMemoryAllocation;
+  cudaError_t e = cudaEventRecord(r.start, s);
+  if (e != cudaSuccess) return e;
+  e = fn();
+  if (e != cudaSuccess) return e;
+  e = cudaEventRecord(r.stop, s);
+  if (e != cudaSuccess) return e;
+  hd->records.push_back(r);
+  return cudaSuccess;
+}
+
+int cuda_fail(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  std::fprintf(stderr, "moe_fused: CUDA error %s\n", cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_fused_workspace_size(const moe_fused_config_t* cfg, size_t* workspace_bytes) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!workspace_bytes) return MOE_ERR_INVALID_ARG;
+  *workspace_bytes = plan(*cfg).total;
+  return MOE_OK;
+}
+
+int moe_fused_create(const moe_fused_config_t* cfg, moe_fused_handle_t** out_handle, size_t* workspace_bytes) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!out_handle) return MOE_ERR_INVALID_ARG;
+  *out_handle = nullptr;
+  moe_fused_handle* hd = new (std::nothrow) moe_fused_handle();
+  if (!hd) return MOE_ERR_INVALID_ARG;
+  hd->cfg = *cfg;
+  hd->timing = false;
+  cudaError_t e = cudaGetDevice(&hd->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&hd->num_sms, cudaDevAttrMultiProcessorCount, hd->device);
+  if (e == cudaSuccess) e = moe::gemm_prepare_attributes();
+  if (e == cudaSuccess) e = moe::dispatch_prepare_attributes(1024);
+  if (e != cudaSuccess) {
+    delete hd;
+    return cuda_fail(e);
+  }
+  hd->L = plan(*cfg);
+  if (workspace_bytes) *workspace_bytes = hd->L.total;
+  *out_handle = hd;
+  return MOE_OK;
+}
+
+int moe_fused_forward(moe_fused_handle_t* hd, const moe_fused_args_t* args, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  return moe_fused_debug_forward_until(hd, args, workspace, workspace_bytes, moe::kNumKernels - 1, stream);
+}
+
+int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t* args, void* workspace,
+                                  size_t workspace_bytes, int last_kernel, void* stream) {
+  moe::FwdParams p;
+  int rc = build_params(hd, args, workspace, workspace_bytes, &p);
+  if (rc) return rc;
+  if (last_kernel < 0 || last_kernel >= moe::kNumKernels) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (p.bs == 0) {
+    e = cudaMemsetAsync(args->expert_token_nums, 0, sizeof(int32_t) * hd->cfg.num_experts, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p.ws + p.L.status, 0, 64 * sizeof(int32_t), s);
+    return cuda_fail(e);
+  }
+  const int sms = hd->num_sms;
+  auto run = [&](int k) -> cudaError_t {
+    switch (k) {
+      case moe::kKDispatch: return moe::launch_dispatch(p, s);
+      case moe::kKQuant: return moe::launch_quant(p, s);
+      case moe::kKGemm1: return moe::launch_gemm(p, moe::kGemm1SwiGLU, nullptr, sms, s);
+      case moe::kKRequant: return moe::launch_requant(p, sms * 8, s);
+      case moe::kKGemm2: return moe::launch_gemm(p, moe::kGemm2Bf16, nullptr, sms, s);
+      default: return moe::launch_combine(p, s);
+    }
+  };
+  e = cudaSuccess;
+  for (int k = 0; k <= last_kernel && e == cudaSuccess; ++k) e = timed(hd, k, s, [&] { return run(k); });
+  return cuda_fail(e);
+}
+
+int moe_fused_get_status(moe_fused_handle_t* hd, const void* workspace, void* stream, moe_fused_status_t* out) {
+  if (!hd || !workspace || !out) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t w[8];
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(w, static_cast<const char*>(workspace) + hd->L.status, sizeof(w), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  out->skipped_pairs = w[moe::kStSkipped];
+  out->error_flags = w[moe::kStErrorFlags];
+  out->error_site = w[moe::kStErrorSite];
+  out->dispatched_rows = w[moe::kStRows];
+  out->shared_rows = w[moe::kStSharedRows];
+  out->active_slots = w[moe::kStSlots];
+  out->reserved[0] = out->reserved[1] = 0;
+  return (out->error_flags & moe::kErrWaitTimeout) ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+int moe_fused_destroy(moe_fused_handle_t* hd) {
+  if (!hd) return MOE_OK;
+  for (auto& r : hd->records) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  for (auto e : hd->pool) cudaEventDestroy(e);
+  delete hd;
+  return MOE_OK;
+}
+
+const char* moe_fused_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_UNIMPLEMENTED: return "not implemented";
+    case MOE_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    default: return "unknown error";
+  }
+}
+
+int moe_fused_set_timing(moe_fused_handle_t* hd, int enable) {
+  if (!hd) return MOE_ERR_INVALID_ARG;
+  hd->timing = enable != 0;
+  return MOE_OK;
+}
+
+int moe_fused_get_timing(moe_fused_handle_t* hd, float* ms, int32_t* launches, int max_kernels) {
+  if (!hd || max_kernels < 0 || (max_kernels > 0 && (!ms || !launches))) return MOE_ERR_INVALID_ARG;
+  for (int k = 0; k < max_kernels; ++k) {
+    ms[k] = 0.0f;
+    launches[k] = 0;
+  }
+  cudaError_t err = cudaSuccess;
+  for (auto& r : hd->records) {
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    float t = 0.0f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.start, r.stop);
+    if (e != cudaSuccess) err = e;
+    if (r.kernel < max_kernels) {
+      ms[r.kernel] += t;
+      launches[r.kernel] += 1;
+    }
+    hd->pool.push_back(r.start);
+    hd->pool.push_back(r.stop);
+  }
+  hd->records.clear();
+  if (err != cudaSuccess) return cuda_fail(err);
+  return moe::kNumKernels;
+}
+
+const char* moe_fused_kernel_name(int k) {
+  static const char* names[] = {"dispatch", "quant", "gemm1_swiglu", "requant", "gemm2_bf16", "combine"};
+  return (k >= 0 && k < moe::kNumKernels) ? names[k] : "unknown";
+}
+
+int moe_fused_debug_region(moe_fused_handle_t* hd, int region, size_t* offset, size_t* bytes) {
+  if (!hd || !offset || !bytes) return MOE_ERR_INVALID_ARG;
+  const moe::WsLayout& L = hd->L;
+  const size_t offs[15] = {L.status, L.counts, L.offsets, L.row_of, L.tk_of_row, L.active, L.x_q, L.x_scale,
+                           L.xs_q, L.xs_scale, L.hbuf, L.x2, L.s2, L.y2, L.slots};
+  if (region < 0 || region > 14) return MOE_ERR_INVALID_ARG;
+  *offset = offs[region];
+  *bytes = L.sizes[region];
+  return MOE_OK;
+}
+
+int moe_fused_debug_gemm_acc(moe_fused_handle_t* hd, const moe_fused_args_t* args, void* workspace,
+                             size_t workspace_bytes, int which, int32_t* acc, void* stream) {
+  moe::FwdParams p;
+  int rc = build_params(hd, args, workspace, workspace_bytes, &p);
+  if (rc) return rc;
+  if ((which != 1 && which != 2) || !acc) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_fail(moe::launch_gemm(p, which == 1 ? moe::kGemm1Raw : moe::kGemm2Raw, acc, hd->num_sms, s));
+}
+
+}  // extern "C"

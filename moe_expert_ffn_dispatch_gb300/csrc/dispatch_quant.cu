@@ -1,0 +1,269 @@
+// Dispatch (counting sort by expert) and per-token dynamic INT8 quantisation.
+//
+// Dispatch follows the FusedDeepMoE analysis §4.1 (local token counting into
+// expert_token_nums; for small batches a (bs+1) x E table whose prefix sums
+// give the expand index, §8.4).  On the GPU the table becomes a per-warp
+// count table built with __match_any_sync: one CTA walks the (t, k) pairs in
+// flat order, 1024 at a time, so every row's position inside its expert group
+// is its rank by flat index t*topk + k -- the same stable order a sequential
+// counting sort produces, with no atomics deciding the order.
+//
+// Quant follows §4.1 / §7.3 and the W8A8 contract of the DeepSeek-V4 decode
+// case study: xs = x * smooth, amax = max(max|xs|, 1e-4), m = 127 / amax,
+// q = RNE(xs * m) clamped to +-127, scale = 1 / m.  Every fp32 operation is an
+// explicit round-to-nearest intrinsic so no contraction can change a code.
+#include "device_prims.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kDispatchThreads = 1024;
+constexpr int kQuantThreads = 256;
+constexpr float kAmaxEps = 1e-4f;
+
+// Exclusive scan of one int per thread over a 1024-thread block.
+__device__ int block_exclusive_scan(int v, int* total, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    s_warp[lane] = wi;  // inclusive over warps
+  }
+  __syncthreads();
+  int excl = incl - v + (warp > 0 ? s_warp[warp - 1] : 0);
+  *total = s_warp[31];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(FwdParams p) {
+  extern __shared__ int32_t dsm[];
+  __shared__ int s_warp[32];
+  __shared__ int s_skipped;
+  const int E = p.E, K = p.topk, bs = p.bs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t* running = dsm;    // [E]: rows per expert so far, later the offsets
+  int32_t* wcnt = dsm + E;   // [32][E]: rows per (warp, expert) in this chunk
+  int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
+  int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
+  int32_t* counts = ws_ptr<int32_t>(p, p.L.counts);
+  int32_t* offsets = ws_ptr<int32_t>(p, p.L.offsets);
+  int32_t* active = ws_ptr<int32_t>(p, p.L.active);
+  int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
+  int32_t* status = ws_ptr<int32_t>(p, p.L.status);
+
+  for (int e = tid; e < E; e += kDispatchThreads) running[e] = 0;
+  if (tid == 0) s_skipped = 0;
+  __syncthreads();
+
+  // 1. rank of every active, valid pair inside its expert group (flat order)
+  const int nf = bs * K;
+  for (int base = 0; base < nf; base += kDispatchThreads) {
+    const int f = base + tid;
+    int e = -1;
+    if (f < nf) {
+      const int t = f / K;
+      const bool act = (p.mask == nullptr) || (p.mask[t] != 0);
+      const int id = p.ids[f];
+      if (act) {
+        if (id >= 0 && id < E) e = id;
+        else atomicAdd(&s_skipped, 1);
+      }
+      row_of[f] = -1;
+    }
+    for (int i = tid; i < 32 * E; i += kDispatchThreads) wcnt[i] = 0;
+    __syncthreads();
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank_w = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank_w == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int pos = running[e] + rank_w;
+      for (int w = 0; w < warp; ++w) pos += wcnt[w * E + e];
+      row_of[f] = pos;  // rank inside the expert group; the offset is added below
+    }
+    __syncthreads();
+    for (int e2 = tid; e2 < E; e2 += kDispatchThreads) {
+      int s = 0;
+      for (int w = 0; w < 32; ++w) s += wcnt[w * E + e2];
+      running[e2] += s;
+    }
+    __syncthreads();
+  }
+
+  // 2. counts -> exclusive offsets (E <= 1024: one expert per thread)
+  const int c = tid < E ? running[tid] : 0;
+  int R = 0;
+  const int off = block_exclusive_scan(c, &R, s_warp);
+  if (tid < E) {
+    counts[tid] = c;
+    offsets[tid] = off;
+    p.token_nums[tid] = c;
+    running[tid] = off;
+  }
+  if (tid == 0) offsets[E] = R;
+  __syncthreads();
+
+  // 3. final row index and its inverse
+  for (int f = tid; f < nf; f += kDispatchThreads) {
+    const int rank = row_of[f];
+    if (rank >= 0) {
+      const int r = running[p.ids[f]] + rank;
+      row_of[f] = r;
+      tk_of_row[r] = f;
+    }
+  }
+
+  // 4. active tokens in ascending order (rows of the shared expert)
+  int S = 0;
+  for (int base = 0; base < bs; base += kDispatchThreads) {
+    const int t = base + tid;
+    const int a = (t < bs) && ((p.mask == nullptr) || (p.mask[t] != 0));
+    int chunk_total = 0;
+    const int pos = block_exclusive_scan(a, &chunk_total, s_warp);
+    if (a) active[S + pos] = t;
+    S += chunk_total;
+  }
+
+  // 5. slot table: experts with rows in ascending id, then the shared expert
+  const int st = SlotTable::stride(E);
+  int32_t* s_exp = slots + SlotTable::kHeader;
+  int32_t* s_row0 = s_exp + st;
+  int32_t* s_rows = s_row0 + st;
+  int32_t* s_blk = s_rows + st;
+  const int has = (tid < E) && (c > 0);
+  const int nblk = has ? (c + kTokenBlock - 1) / kTokenBlock : 0;
+  int n_routed = 0, routed_blk = 0;
+  const int si = block_exclusive_scan(has, &n_routed, s_warp);
+  const int bi = block_exclusive_scan(nblk, &routed_blk, s_warp);
+  if (has) {
+    s_exp[si] = tid;
+    s_row0[si] = off;
+    s_rows[si] = c;
+    s_blk[si] = bi;
+  }
+  if (tid == 0) {
+    int n_slots = n_routed, total_blk = routed_blk;
+    if (p.has_shared && S > 0) {
+      s_exp[n_slots] = -1;
+      s_row0[n_slots] = bs * K;
+      s_rows[n_slots] = S;
+      s_blk[n_slots] = total_blk;
+      total_blk += (S + kTokenBlock - 1) / kTokenBlock;
+      n_slots += 1;
+    }
+    s_blk[n_slots] = total_blk;
+    slots[0] = n_slots;
+    slots[1] = total_blk;
+    slots[2] = R;
+    slots[3] = (p.has_shared ? S : 0);
+    status[kStSkipped] = s_skipped;
+    status[kStErrorFlags] = 0;
+    status[kStErrorSite] = 0;
+    status[kStRows] = R;
+    status[kStSharedRows] = (p.has_shared ? S : 0);
+    status[kStSlots] = n_slots;
+  }
+}
+
+__device__ __forceinline__ float block_max(float v, float* s_red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  float r = (lane < (int)(blockDim.x >> 5)) ? s_red[lane] : 0.0f;
+  if (warp == 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, o));
+    if (lane == 0) s_red[32] = r;
+  }
+  __syncthreads();
+  r = s_red[32];
+  __syncthreads();
+  return r;
+}
+
+// Quantise one bf16 row (h multiple of 64) with optional smooth scales.
+__device__ void quant_row(const uint16_t* __restrict__ x, const float* __restrict__ smooth, int h,
+                          int8_t* __restrict__ q, float* __restrict__ scale_out, float* s_red) {
+  const int n8 = h >> 3;
+  float amax = 0.0f;
+  for (int i = threadIdx.x; i < n8; i += kQuantThreads) {
+    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float f = bf16_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
+      if (smooth) f = __fmul_rn(f, smooth[i * 8 + j]);
+      amax = fmaxf(amax, fabsf(f));
+    }
+  }
+  amax = block_max(amax, s_red);
+  if (amax < kAmaxEps) amax = kAmaxEps;
+  const float m = __fdiv_rn(127.0f, amax);
+  for (int i = threadIdx.x; i < n8; i += kQuantThreads) {
+    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float f = bf16_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
+      if (smooth) f = __fmul_rn(f, smooth[i * 8 + j]);
+      const uint32_t b = static_cast<uint8_t>(f32_to_q(__fmul_rn(f, m)));
+      packed[j >> 2] |= b << ((j & 3) * 8);
+    }
+    reinterpret_cast<uint2*>(q)[i] = make_uint2(packed[0], packed[1]);
+  }
+  if (threadIdx.x == 0) *scale_out = __fdiv_rn(1.0f, m);
+}
+
+__global__ void __launch_bounds__(kQuantThreads) quant_kernel(FwdParams p) {
+  __shared__ float s_red[33];
+  const int t = blockIdx.x;
+  if (p.mask && p.mask[t] == 0) return;
+  const uint16_t* xr = p.x + static_cast<size_t>(t) * p.h;
+  quant_row(xr, p.smooth, p.h, ws_ptr<int8_t>(p, p.L.x_q) + static_cast<size_t>(t) * p.h,
+            ws_ptr<float>(p, p.L.x_scale) + t, s_red);
+  if (p.has_shared && !p.share_uses_xq) {
+    quant_row(xr, p.ssmooth, p.h, ws_ptr<int8_t>(p, p.L.xs_q) + static_cast<size_t>(t) * p.h,
+              ws_ptr<float>(p, p.L.xs_scale) + t, s_red);
+  }
+}
+
+}  // namespace
+
+size_t dispatch_smem_bytes(int E) { return sizeof(int32_t) * static_cast<size_t>(33 * E); }
+
+cudaError_t launch_dispatch(const FwdParams& p, cudaStream_t s) {
+  dispatch_kernel<<<1, kDispatchThreads, dispatch_smem_bytes(p.E), s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant(const FwdParams& p, cudaStream_t s) {
+  if (p.bs == 0) return cudaSuccess;
+  quant_kernel<<<p.bs, kQuantThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t dispatch_prepare_attributes(int E) {
+  return cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(dispatch_smem_bytes(E)));
+}
+
+}  // namespace moe

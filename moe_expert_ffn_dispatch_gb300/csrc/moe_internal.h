@@ -1,0 +1,105 @@
+// Internal host/device declarations shared by the kernels and the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// status word indices (int32) at the start of the workspace
+enum StatusWord : int {
+  kStSkipped = 0,
+  kStErrorFlags = 1,
+  kStErrorSite = 2,
+  kStRows = 3,
+  kStSharedRows = 4,
+  kStSlots = 5,
+};
+constexpr int kErrWaitTimeout = 1;
+
+// ---------------------------------------------------------------- layout
+// Workspace regions (byte offsets, 256-byte aligned).  `rows` = bs_max*topk
+// routed rows + bs_max shared rows.  h (fp32 SwiGLU output) and y2 (bf16
+// GEMM2 output) share one region: h is dead once requant has run, the same
+// reuse the pages' ENABLE_REUSE_MEMORY applies to its swap / SwiGLU space.
+struct WsLayout {
+  size_t status;     // 64 int32 status words
+  size_t counts;     // [E] int32
+  size_t offsets;    // [E+1] int32
+  size_t row_of;     // [bs_max*topk] int32
+  size_t tk_of_row;  // [bs_max*topk] int32
+  size_t active;     // [bs_max] int32: i-th active token
+  size_t slots;      // slot table (int32), see SlotTable
+  size_t x_q;        // [bs_max, h] int8
+  size_t x_scale;    // [bs_max] f32
+  size_t xs_q;       // [bs_max, h] int8 (shared-expert quant)
+  size_t xs_scale;   // [bs_max] f32
+  size_t hbuf;       // [rows, I] f32  (aliased by y2)
+  size_t x2;         // [rows, I] int8
+  size_t s2;         // [rows] f32
+  size_t y2;         // [bs_max*topk, h] bf16 (== hbuf)
+  size_t total;
+  size_t sizes[16];  // bytes per region id (debug_region)
+};
+
+// Slot table: one slot per expert with rows (ascending id), then the shared
+// expert.  Stored as int32 words at layout.slots:
+//   [0] n_slots  [1] total token blocks  [2] R  [3] S
+//   then four arrays of (E + 2) words: expert id (-1 = shared), first row,
+//   row count, exclusive prefix of token blocks.
+struct SlotTable {
+  static constexpr int kHeader = 4;
+  static __host__ __device__ int stride(int E) { return E + 2; }
+  static __host__ __device__ int words(int E) { return kHeader + 4 * stride(E); }
+};
+
+constexpr int kTokenBlock = 64;  // token rows per GEMM work item
+
+// ---------------------------------------------------------------- params
+struct FwdParams {
+  int32_t bs, h, E, topk, I, has_shared;
+  int32_t share_uses_xq;  // shared quant identical to routed quant (same smooth vector)
+  const uint16_t* x;
+  const int32_t* ids;
+  const float* scales;
+  const int8_t* w1;
+  const float* w1s;
+  const int8_t* w2;
+  const float* w2s;
+  const int8_t* sw1;
+  const float* sw1s;
+  const int8_t* sw2;
+  const float* sw2s;
+  const float* smooth;
+  const float* ssmooth;
+  const uint8_t* mask;
+  uint16_t* out;
+  uint16_t* sout;
+  int32_t* token_nums;
+  char* ws;
+  WsLayout L;
+};
+
+template <typename T>
+__host__ __device__ inline T* ws_ptr(const FwdParams& p, size_t off) {
+  return reinterpret_cast<T*>(p.ws + off);
+}
+
+// kernel ids (timing / status sites)
+enum KernelId : int { kKDispatch = 0, kKQuant = 1, kKGemm1 = 2, kKRequant = 3, kKGemm2 = 4, kKCombine = 5, kNumKernels = 6 };
+
+// GEMM modes
+enum GemmMode : int { kGemm1SwiGLU = 0, kGemm2Bf16 = 1, kGemm1Raw = 2, kGemm2Raw = 3 };
+
+// ---------------------------------------------------------------- launches
+size_t dispatch_smem_bytes(int E);
+cudaError_t launch_dispatch(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_quant(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_gemm(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);
+cudaError_t launch_requant(const FwdParams& p, int num_ctas, cudaStream_t s);
+cudaError_t launch_combine(const FwdParams& p, cudaStream_t s);
+cudaError_t gemm_prepare_attributes();
+cudaError_t dispatch_prepare_attributes(int E);
+
+}  // namespace moe

@@ -222,14 +222,20 @@ def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tenso
     keep = []
     w1p = (ctypes.c_void_p * E)()
     w2p = (ctypes.c_void_p * E)()
-    for e in sorted(need):
+    def host_weights(e):
+        """Host copy of expert e's weights (e == E: the shared expert), never
+        read back from a device: redrawn from the seeded generator instead."""
         if expert_weights is not None:
-            a, b = expert_weights(e)
-        elif inp.w1 is not None:
-            a, b = inp.w1[e], inp.w2[e]
-        else:
-            a, b = inp.expert_w1(e), inp.expert_w2(e)
-        a = a.to("cpu").contiguous(); b = b.to("cpu").contiguous()
+            return expert_weights(e)
+        if e < E and inp.w1 is not None and inp.w1.device.type == "cpu":
+            return inp.w1[e], inp.w2[e]
+        if e == E and inp.share_w1 is not None and inp.share_w1.device.type == "cpu":
+            return inp.share_w1, inp.share_w2
+        return inp.expert_w1(e), inp.expert_w2(e)
+
+    for e in sorted(need):
+        a, b = host_weights(e)
+        a = a.contiguous(); b = b.contiguous()
         keep += [a, b]
         w1p[e] = a.data_ptr(); w2p[e] = b.data_ptr()
 
@@ -237,8 +243,8 @@ def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tenso
     w2s = inp.w2_scale.to(torch.float32).contiguous()
     sw1 = sw2 = sw1s = sw2s = None
     if shared:
-        sw1 = (inp.share_w1 if inp.share_w1 is not None else inp.expert_w1(E)).to("cpu").contiguous()
-        sw2 = (inp.share_w2 if inp.share_w2 is not None else inp.expert_w2(E)).to("cpu").contiguous()
+        sw1, sw2 = host_weights(E)
+        sw1 = sw1.contiguous(); sw2 = sw2.contiguous()
         sw1s = inp.share_w1_scale.to(torch.float32).contiguous()
         sw2s = inp.share_w2_scale.to(torch.float32).contiguous()
     smooth = None if inp.smooth is None else inp.smooth.to(torch.float32).contiguous()

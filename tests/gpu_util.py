@@ -1,0 +1,199 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI on
+seeded synthetic inputs and compare with the CPU oracle.
+
+Tolerances (the block's accuracy contract):
+  * integer and index work (dispatch arrays, expert_token_nums, x_q codes,
+    int32 accumulators): bit-exact;
+  * fp32 x_scale: bit-exact (only IEEE mul/div/max are involved);
+  * SwiGLU output h: within 2e-6 relative -- the only difference between the
+    two sides is the exp() implementation (CUDA expf vs the C library's expf,
+    each within a few ulp);
+  * requantised x2: at most 1 LSB apart on at most 0.1 % of the elements
+    (an exp ulp can move a value across a rounding boundary), s2 within 2e-6;
+  * bf16 y2 / output / share_output: per row, max |gpu - oracle| <= 2e-2 *
+    max |oracle row|; masked rows exactly zero.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import moe_expert_ffn_dispatch_gb300 as m
+import oracle
+import synth
+
+H_REL = 2e-6
+OUT_REL = 2e-2
+X2_FRAC = 1e-3
+
+
+def device_inputs(inp, dev):
+    d = {"x": inp.x.to(dev), "expert_ids": inp.expert_ids.to(dev), "expert_scales": inp.expert_scales.to(dev)}
+    if inp.mask is not None:
+        d["mask"] = inp.mask.to(dev)
+    return d
+
+
+def device_weights(inp, dev):
+    w = {"w1": inp.w1.to(dev), "w1_scale": inp.w1_scale.to(dev), "w2": inp.w2.to(dev),
+         "w2_scale": inp.w2_scale.to(dev)}
+    if inp.wl.has_shared:
+        w.update(share_w1=inp.share_w1.to(dev), share_w1_scale=inp.share_w1_scale.to(dev),
+                 share_w2=inp.share_w2.to(dev), share_w2_scale=inp.share_w2_scale.to(dev))
+    if inp.smooth is not None:
+        w["smooth"] = inp.smooth.to(dev)
+    if inp.share_smooth is not None:
+        w["share_smooth"] = inp.share_smooth.to(dev)
+    return w
+
+
+def make_block(wl, dev, bs_max=None):
+    return m.MoeFused(bs_max if bs_max is not None else wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter,
+                      wl.has_shared, dev)
+
+
+def region(blk, name, dtype, shape=None):
+    t = blk.region(name).view(dtype)
+    if shape is not None:
+        n = int(np.prod(shape))
+        t = t[:n].view(*shape)
+    return t.cpu()
+
+
+def assert_rows_close(got: torch.Tensor, ref: torch.Tensor, rel: float = OUT_REL, what: str = ""):
+    g = got.float().cpu().double()
+    r = ref.float().cpu().double()
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    if g.numel() == 0:
+        return
+    tol = rel * r.abs().amax(dim=1, keepdim=True)
+    bad = (g - r).abs() > tol
+    zero_rows = r.abs().amax(dim=1) == 0
+    assert torch.all(g[zero_rows] == 0), "%s: rows that must be zero are not" % what
+    if bad.any():
+        i = int(bad.any(dim=1).nonzero()[0])
+        raise AssertionError("%s: row %d max err %.3e > tol %.3e" % (what, i, float((g[i] - r[i]).abs().max()),
+                                                                     float(tol[i])))
+
+
+def assert_codes_close(got: torch.Tensor, ref: torch.Tensor, what: str):
+    d = (got.to(torch.int32) - ref.to(torch.int32)).abs()
+    if d.numel() == 0:
+        return
+    assert int(d.max()) <= 1, "%s: code differs by %d" % (what, int(d.max()))
+    frac = float((d > 0).sum()) / d.numel()
+    assert frac <= X2_FRAC, "%s: %.4f%% of codes differ" % (what, 100 * frac)
+
+
+def assert_rel(got: torch.Tensor, ref: torch.Tensor, rel: float, what: str):
+    g = got.double().cpu()
+    r = ref.double().cpu()
+    err = (g - r).abs()
+    tol = rel * r.abs() + 1e-35
+    if not torch.all(err <= tol):
+        i = int((err - tol).argmax())
+        raise AssertionError("%s: element %d got %r want %r" % (what, i, float(g.view(-1)[i]), float(r.view(-1)[i])))
+
+
+def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
+    """Run one forward on the GPU and check every stage against the oracle.
+    Returns (block, oracle result)."""
+    wl = inp.wl
+    bs, h, E, K, I = wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter
+    if blk is None:
+        blk = make_block(wl, dev, bs_max)
+    di = device_inputs(inp, dev)
+    dw = device_weights(inp, dev)
+    if staged and bs > 0:
+        # stop after requant: h is reused by y2 once GEMM2 runs
+        blk.forward_inputs(di, dw, until=3)
+        torch.cuda.synchronize()
+        staged_h = blk.region("h").clone().cpu()
+    out, sout, nums = blk.forward_inputs(di, dw)
+    torch.cuda.synchronize()
+    st = blk.status()
+    assert st["rc"] == 0 and st["error_flags"] == 0, st
+    ref = oracle.forward(inp, intermediates=staged, threads=8)
+    R = ref["R"]
+    assert st["dispatched_rows"] == R
+    assert st["skipped_pairs"] == ref["skipped"]
+    assert torch.equal(nums.cpu(), ref["expert_token_nums"])
+    mask = torch.ones(bs, dtype=torch.bool) if inp.mask is None else inp.mask
+    act = mask.nonzero().view(-1)
+    S = int(act.numel()) if wl.has_shared else 0
+    assert st["shared_rows"] == S
+    if staged and bs > 0:
+        # dispatch (bit-exact)
+        assert torch.equal(region(blk, "counts", torch.int32, (E,)), ref["expert_token_nums"])
+        assert torch.equal(region(blk, "offsets", torch.int32, (E + 1,)), ref["offsets"])
+        assert torch.equal(region(blk, "row_of", torch.int32, (bs, K)), ref["row_of"])
+        assert torch.equal(region(blk, "tk_of_row", torch.int32, (R,)), ref["tk_of_row"])
+        if wl.has_shared:
+            assert torch.equal(region(blk, "active", torch.int32, (S,)), act.to(torch.int32))
+        # quant (bit-exact on active tokens)
+        xq = region(blk, "x_q", torch.int8, (bs, h))
+        xs = region(blk, "x_scale", torch.float32, (bs,))
+        assert torch.equal(xq[act], ref["x_q"][act]), "x_q differs"
+        assert torch.equal(xs[act], ref["x_scale"][act]), "x_scale differs"
+        if wl.has_shared and (inp.smooth is not None or inp.share_smooth is not None):
+            assert torch.equal(region(blk, "xs_q", torch.int8, (bs, h))[act], ref["xs_q"][act])
+            assert torch.equal(region(blk, "xs_scale", torch.float32, (bs,))[act], ref["xs_scale"][act])
+        rows = bs * K + (bs if wl.has_shared else 0)
+        # SwiGLU output h (fp32, exp ulps)
+        hb = staged_h.view(torch.float32)[:rows * I].view(rows, I)
+        assert_rel(hb[:R], ref["h"], H_REL, "h routed")
+        if S:
+            assert_rel(hb[bs * K:bs * K + S], ref["share_h"][act], H_REL, "h shared")
+        # requant
+        x2 = region(blk, "x2", torch.int8, (rows, I))
+        s2 = region(blk, "s2", torch.float32, (rows,))
+        assert_codes_close(x2[:R], ref["x2"], "x2 routed")
+        assert_rel(s2[:R], ref["s2"], H_REL, "s2 routed")
+        if S:
+            assert_codes_close(x2[bs * K:bs * K + S], ref["share_x2"][act], "x2 shared")
+            assert_rel(s2[bs * K:bs * K + S], ref["share_s2"][act], H_REL, "s2 shared")
+        # y2 (bf16) of routed rows
+        y2 = region(blk, "y2", torch.int16, (max(R, 1), h))[:R].view(torch.bfloat16)
+        assert_rows_close(y2, ref["y2"], OUT_REL, "y2")
+    if bs > 0:
+        assert_rows_close(out, ref["output"], OUT_REL, "output")
+        if wl.has_shared:
+            assert_rows_close(sout, ref["share_output"], OUT_REL, "share_output")
+        assert torch.all(out.cpu()[~mask].float() == 0)
+    return blk, ref, (di, dw)
+
+
+def check_raw_accumulators(blk, inp, ref, di, dw, dev):
+    """int32 accumulators of both GEMMs, bit-exact.  GEMM1 runs on the x_q the
+    forward left in the workspace (already checked bit-exact); for GEMM2 the
+    oracle's x2 is planted into the workspace first, so both sides contract the
+    same codes."""
+    wl = inp.wl
+    bs, h, K, I = wl.bs, wl.hidden, wl.topk, wl.inter
+    R = ref["R"]
+    mask = torch.ones(bs, dtype=torch.bool) if inp.mask is None else inp.mask
+    act = mask.nonzero().view(-1)
+    S = int(act.numel()) if wl.has_shared else 0
+    rows = bs * K + (bs if wl.has_shared else 0)
+    fargs = (di["x"], di["expert_ids"], di["expert_scales"], dw["w1"], dw["w1_scale"], dw["w2"], dw["w2_scale"],
+             dw.get("share_w1"), dw.get("share_w1_scale"), dw.get("share_w2"), dw.get("share_w2_scale"),
+             dw.get("smooth"), dw.get("share_smooth"), di.get("mask"))
+    acc1 = torch.zeros(rows, 2 * I, dtype=torch.int32, device=dev)
+    blk.debug_gemm_acc(1, acc1, *fargs)
+    torch.cuda.synchronize()
+    a1 = acc1.cpu()
+    assert torch.equal(a1[:R], ref["acc1"]), "acc1 routed differs"
+    if S:
+        assert torch.equal(a1[bs * K:bs * K + S], ref["share_acc1"][act]), "acc1 shared differs"
+    # plant the oracle's x2 and contract it
+    x2v = blk.region("x2").view(torch.int8)[:rows * I].view(rows, I)
+    x2v[:R] = ref["x2"].to(dev)
+    if S:
+        x2v[bs * K:bs * K + S] = ref["share_x2"][act].to(dev)
+    acc2 = torch.zeros(rows, h, dtype=torch.int32, device=dev)
+    blk.debug_gemm_acc(2, acc2, *fargs)
+    torch.cuda.synchronize()
+    a2 = acc2.cpu()
+    assert torch.equal(a2[:R], ref["acc2"]), "acc2 routed differs"
+    if S:
+        assert torch.equal(a2[bs * K:bs * K + S], ref["share_acc2"][act]), "acc2 shared differs"

@@ -1,0 +1,62 @@
+"""Host-side argument checks of the C ABI on a GPU machine: each bad call returns
+its error code before any launch and leaves the outputs untouched."""
+import pytest
+import torch
+
+import moe_expert_ffn_dispatch_gb300 as m
+import synth
+from gpu_util import device_inputs, device_weights, make_block
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+def _setup():
+    wl = synth.custom("errs", bs=8, hidden=128, num_experts=4, topk=2, inter=64, has_shared=True, seed=41)
+    inp = synth.make_inputs(wl)
+    blk = make_block(wl, DEV)
+    di, dw = device_inputs(inp, DEV), device_weights(inp, DEV)
+    out = torch.full((8, 128), 3.0, dtype=torch.bfloat16, device=DEV)
+    a, keep, _ = blk.make_args(di["x"], di["expert_ids"], di["expert_scales"], dw["w1"], dw["w1_scale"], dw["w2"],
+                               dw["w2_scale"], dw["share_w1"], dw["share_w1_scale"], dw["share_w2"],
+                               dw["share_w2_scale"], out=out)
+    return blk, a, keep, out
+
+
+def _fwd(blk, a, ws=None, nbytes=None):
+    w = blk.workspace() if ws is None else ws
+    return m.moe_fused_forward(blk.handle, a, w.data_ptr(), w.numel() if nbytes is None else nbytes,
+                               torch.cuda.current_stream().cuda_stream)
+
+
+def test_error_codes_leave_outputs_untouched():
+    blk, a, keep, out = _setup()
+    assert _fwd(blk, a, nbytes=blk.workspace_bytes - 1) == m.MOE_ERR_WORKSPACE_TOO_SMALL
+    a.bs = 9
+    assert _fwd(blk, a) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    a.bs = 8
+    x = a.x
+    a.x = x + 2
+    assert _fwd(blk, a) == m.MOE_ERR_ALIGNMENT
+    a.x = 0
+    assert _fwd(blk, a) == m.MOE_ERR_INVALID_ARG
+    a.x = x
+    sw = a.share_gmm1_weight
+    a.share_gmm1_weight = 0
+    assert _fwd(blk, a) == m.MOE_ERR_INVALID_ARG
+    a.share_gmm1_weight = sw
+    ws = blk.workspace()
+    assert _fwd(blk, a, ws=ws[16:], nbytes=blk.workspace_bytes) == m.MOE_ERR_ALIGNMENT
+    torch.cuda.synchronize()
+    assert torch.all(out.float().cpu() == 3.0)
+    assert _fwd(blk, a) == m.MOE_OK
+    torch.cuda.synchronize()
+    assert not torch.all(out.float().cpu() == 3.0)
+
+
+def test_create_rejects_bad_config():
+    bad = [m.Config(8, 100, 4, 2, 64, 0, 0), m.Config(8, 128, 4, 5, 64, 0, 0), m.Config(8, 128, 0, 1, 64, 0, 0),
+           m.Config(8, 128, 4, 2, 64, 0, 1), m.Config(-1, 128, 4, 2, 64, 0, 0)]
+    for cfg in bad:
+        rc, h, _ = m.moe_fused_create(cfg)
+        assert rc < 0 and h == 0
