@@ -149,6 +149,37 @@ int moe_fused_destroy(moe_fused_handle_t* handle);
 /* Static string for an error code. */
 const char* moe_fused_strerror(int code);
 
+/* ---- dispatch for callers that cannot allocate device memory ------------
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that may not allocate device memory at all -- a plugin or custom op inside
+ * a host framework that owns every device allocation, or a process running
+ * on a fixed, pre-reserved device-memory budget -- and therefore cannot
+ * provide the workspace that moe_fused_forward needs.
+ *
+ * It runs only the dispatch step (the counting sort of the active (t, k)
+ * pairs by expert, stable by flat index t*topk+k) and writes
+ *   expert_token_nums  [num_experts] int32 (device): rows per expert, exactly
+ *                      as moe_fused_forward writes it;
+ *   expand_row         [bs, topk] int32 (device) or NULL: the row of each pair
+ *                      in expert-sorted order, -1 for pairs not dispatched
+ *                      (masked token or id outside [0, num_experts)).
+ * Inputs: expert_ids [bs, topk] int32 and x_active_mask [bs] (or NULL), device.
+ *
+ * Its scratch lives in one library-owned static device array of 1 MiB, which
+ * every GPU that loads the library keeps until the process exits.  Limits:
+ * bs * topk <= 65536, num_experts <= 1024, 1 <= topk <= min(16, num_experts);
+ * larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before any launch.  It calls
+ * no allocating routine.  The first call on each device looks up the array's
+ * device address (and sets the kernel's shared-memory attribute) with that
+ * device current; make that first call before any stream capture.  Every call
+ * on a device shares the one array: calls that may overlap on the GPU (on
+ * different streams without ordering) race and must not be issued.  Nothing
+ * in the array needs clearing between calls: the kernel initialises all it
+ * reads.  Errors: INVALID_ARG (NULL expert_token_nums, or NULL expert_ids with
+ * bs > 0), UNSUPPORTED_SHAPE, CUDA. */
+int moe_fused_dispatch_noalloc(const int32_t* expert_ids, const uint8_t* x_active_mask, int32_t bs, int32_t topk,
+                               int32_t num_experts, int32_t* expert_token_nums, int32_t* expand_row, void* stream);
+
 /* ---- per-kernel timing (used by the benchmark) ---------------------------
  * With timing enabled, forward brackets each kernel launch with CUDA events on
  * `stream`.  get_timing synchronises the recorded events, writes for each

@@ -36,8 +36,8 @@ REGIONS = {"status": 0, "counts": 1, "offsets": 2, "row_of": 3, "tk_of_row": 4, 
 
 EXPORTS = ["moe_fused_create", "moe_fused_workspace_size", "moe_fused_forward", "moe_fused_get_status",
            "moe_fused_destroy", "moe_fused_strerror", "moe_fused_set_timing", "moe_fused_get_timing",
-           "moe_fused_kernel_name", "moe_fused_debug_region", "moe_fused_debug_forward_until",
-           "moe_fused_debug_gemm_acc"]
+           "moe_fused_kernel_name", "moe_fused_dispatch_noalloc", "moe_fused_debug_region",
+           "moe_fused_debug_forward_until", "moe_fused_debug_gemm_acc"]
 
 P = ctypes.c_void_p
 I32 = ctypes.c_int32
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
                                              ctypes.POINTER(ctypes.c_size_t)]
         L.moe_fused_debug_gemm_acc.argtypes = [P, ctypes.POINTER(Args), P, ctypes.c_size_t, ctypes.c_int, P, P]
         L.moe_fused_debug_forward_until.argtypes = [P, ctypes.POINTER(Args), P, ctypes.c_size_t, ctypes.c_int, P]
+        L.moe_fused_dispatch_noalloc.argtypes = [P, P, I32, I32, I32, P, P, P]
         for name in EXPORTS:
             if name not in ("moe_fused_strerror", "moe_fused_kernel_name"):
                 getattr(L, name).restype = ctypes.c_int
@@ -151,6 +152,13 @@ def moe_fused_get_timing(handle: int, max_kernels: int = 6):
 
 def moe_fused_kernel_name(k: int) -> str:
     return lib().moe_fused_kernel_name(k).decode()
+
+
+def moe_fused_dispatch_noalloc(expert_ids: int, x_active_mask: int, bs: int, topk: int, num_experts: int,
+                               expert_token_nums: int, expand_row: int, stream: int) -> int:
+    """Dispatch only, with library-owned static scratch (no workspace; see the header)."""
+    return lib().moe_fused_dispatch_noalloc(expert_ids, x_active_mask, bs, topk, num_experts,
+                                            expert_token_nums, expand_row, stream)
 
 
 def moe_fused_debug_region(handle: int, region: int) -> Tuple[int, int, int]:

@@ -319,6 +319,12 @@ const char* moe_fused_kernel_name(int k) {
   return (k >= 0 && k < moe::kNumKernels) ? names[k] : "unknown";
 }
 
+int moe_fused_dispatch_noalloc(const int32_t* expert_ids, const uint8_t* x_active_mask, int32_t bs, int32_t topk,
+                               int32_t num_experts, int32_t* expert_token_nums, int32_t* expand_row, void* stream) {
+  return moe::dispatch_noalloc(expert_ids, x_active_mask, bs, topk, num_experts, expert_token_nums, expand_row,
+                               static_cast<cudaStream_t>(stream));
+}
+
 int moe_fused_debug_region(moe_fused_handle_t* hd, int region, size_t* offset, size_t* bytes) {
   if (!hd || !offset || !bytes) return MOE_ERR_INVALID_ARG;
   const moe::WsLayout& L = hd->L;

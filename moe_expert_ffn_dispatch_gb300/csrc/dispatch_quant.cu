@@ -12,7 +12,10 @@
 // case study: xs = x * smooth, amax = max(max|xs|, 1e-4), m = 127 / amax,
 // q = RNE(xs * m) clamped to +-127, scale = 1 / m.  Every fp32 operation is an
 // explicit round-to-nearest intrinsic so no contraction can change a code.
+#include <cstring>
+
 #include "device_prims.cuh"
+#include "moe_fused.h"
 #include "moe_internal.h"
 
 namespace moe {
@@ -264,6 +267,100 @@ cudaError_t launch_quant(const FwdParams& p, cudaStream_t s) {
 cudaError_t dispatch_prepare_attributes(int E) {
   return cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(dispatch_smem_bytes(E)));
+}
+
+}  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Dispatch without caller-provided scratch (moe_fused_dispatch_noalloc).
+//
+// Some callers cannot allocate device memory at all: plugins and custom ops
+// inside a host framework that owns every device allocation, or processes
+// that run on a fixed, pre-reserved device-memory budget.  For them the
+// dispatch kernel above can run with its scratch (offsets, inverse index,
+// active-token list, slot table, status words) in the file-scope array
+// below, which every GPU that loads this library holds until the process
+// exits.  Host code must not pass the array's name to a kernel: on the host
+// that name is only a stand-in, so its device address is looked up once per
+// device with cudaGetSymbolAddress.
+namespace moe {
+
+constexpr size_t kNoallocScratchBytes = size_t(1) << 20;  // 1 MiB
+constexpr int kNoallocMaxPairs = 65536;                   // bs * topk
+constexpr int kNoallocMaxExperts = 1024;
+
+}  // namespace moe
+
+static __device__ __align__(256) char g_noalloc_dispatch_scratch[moe::kNoallocScratchBytes];
+
+namespace moe {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+char* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Scratch layout inside the static array for (bs, topk, E).
+WsLayout noalloc_layout(int bs, int topk, int E) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t& field, size_t bytes) {
+    field = off;
+    off = (off + (bytes ? bytes : 1) + 255) / 256 * 256;
+  };
+  const size_t pairs = static_cast<size_t>(bs) * topk;
+  take(L.status, 64 * sizeof(int32_t));
+  take(L.counts, static_cast<size_t>(E) * 4);
+  take(L.offsets, static_cast<size_t>(E + 1) * 4);
+  take(L.row_of, pairs * 4);
+  take(L.tk_of_row, pairs * 4);
+  take(L.active, static_cast<size_t>(bs) * 4);
+  take(L.slots, static_cast<size_t>(SlotTable::words(E)) * 4);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+// Returns 0, or a negative MOE_ERR_* value (see moe_fused.h).
+int dispatch_noalloc(const int32_t* expert_ids, const uint8_t* mask, int bs, int topk, int E,
+                     int32_t* expert_token_nums, int32_t* expand_row, cudaStream_t s) {
+  if (bs < 0 || topk < 1 || topk > 16 || E < 1 || E > kNoallocMaxExperts || topk > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(bs) * topk > kNoallocMaxPairs) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!expert_token_nums || (bs > 0 && !expert_ids)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = noalloc_layout(bs, topk, E);
+  if (L.total > kNoallocScratchBytes) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  if (!g_noalloc_ptr[dev]) {
+    // once per device, with that device current
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_dispatch_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
+    if (dispatch_prepare_attributes(kNoallocMaxExperts) != cudaSuccess) return MOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<char*>(ptr);
+  }
+  if (bs == 0) {
+    return cudaMemsetAsync(expert_token_nums, 0, sizeof(int32_t) * E, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.bs = bs;
+  p.E = E;
+  p.topk = topk;
+  p.has_shared = 0;
+  p.ids = expert_ids;
+  p.mask = mask;
+  p.token_nums = expert_token_nums;
+  p.ws = g_noalloc_ptr[dev];
+  p.L = L;
+  dispatch_kernel<<<1, kDispatchThreads, dispatch_smem_bytes(E), s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (expand_row) {
+    if (cudaMemcpyAsync(expand_row, p.ws + L.row_of, sizeof(int32_t) * static_cast<size_t>(bs) * topk,
+                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 }  // namespace moe

@@ -101,5 +101,7 @@ cudaError_t launch_requant(const FwdParams& p, int num_ctas, cudaStream_t s);
 cudaError_t launch_combine(const FwdParams& p, cudaStream_t s);
 cudaError_t gemm_prepare_attributes();
 cudaError_t dispatch_prepare_attributes(int E);
+int dispatch_noalloc(const int32_t* expert_ids, const uint8_t* mask, int bs, int topk, int E,
+                     int32_t* expert_token_nums, int32_t* expand_row, cudaStream_t s);
 
 }  // namespace moe
