@@ -165,7 +165,7 @@ const char* moe_fused_strerror(int code);
  *                      (masked token or id outside [0, num_experts)).
  * Inputs: expert_ids [bs, topk] int32 and x_active_mask [bs] (or NULL), device.
  *
- * Its scratch lives in one library-owned static device array of 1 MiB, which
+ * Its scratch lives in one library-owned static device array of 2 MiB, which
  * every GPU that loads the library keeps until the process exits.  Limits:
  * bs * topk <= 65536, num_experts <= 1024, 1 <= topk <= min(16, num_experts);
  * larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before any launch.  It calls
@@ -185,8 +185,9 @@ int moe_fused_dispatch_noalloc(const int32_t* expert_ids, const uint8_t* x_activ
  * `stream`.  get_timing synchronises the recorded events, writes for each
  * kernel id k < max_kernels the summed milliseconds ms[k] and launch count
  * launches[k] (host arrays), returns the number of kernel ids, and clears the
- * record.  Kernel ids: 0 dispatch, 1 quant, 2 gemm1, 3 requant, 4 gemm2,
- * 5 combine. */
+ * record.  Kernel ids: 0 dispatch, 1 quant, 2 gemm1 for experts with at most
+ * 8 rows (weight streaming), 3 gemm1 for the others (tensor cores), 4 requant,
+ * 5 gemm2 (at most 8 rows), 6 gemm2 (others), 7 combine. */
 int moe_fused_set_timing(moe_fused_handle_t* handle, int enable);
 int moe_fused_get_timing(moe_fused_handle_t* handle, float* ms, int32_t* launches, int max_kernels);
 const char* moe_fused_kernel_name(int kernel_id);

@@ -76,6 +76,9 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
   L.y2 = L.hbuf;
   L.sizes[13] = ybytes;
   take(L.slots, static_cast<size_t>(moe::SlotTable::words(c.num_experts)) * 4, 14);
+  take(L.row_token, rows * 4, 15);
+  take(L.row_scale, rows * 4, 16);
+  take(L.shared_row, bs * 4, 17);
   L.total = off;
   return L;
 }
@@ -196,6 +199,7 @@ int moe_fused_create(const moe_fused_config_t* cfg, moe_fused_handle_t** out_han
   cudaError_t e = cudaGetDevice(&hd->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&hd->num_sms, cudaDevAttrMultiProcessorCount, hd->device);
   if (e == cudaSuccess) e = moe::gemm_prepare_attributes();
+  if (e == cudaSuccess) e = moe::gemv_prepare_attributes();
   if (e == cudaSuccess) e = moe::dispatch_prepare_attributes(1024);
   if (e != cudaSuccess) {
     delete hd;
@@ -230,8 +234,10 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
     switch (k) {
       case moe::kKDispatch: return moe::launch_dispatch(p, s);
       case moe::kKQuant: return moe::launch_quant(p, s);
+      case moe::kKGemm1Small: return moe::launch_gemv(p, moe::kGemm1SwiGLU, nullptr, sms, s);
       case moe::kKGemm1: return moe::launch_gemm(p, moe::kGemm1SwiGLU, nullptr, sms, s);
       case moe::kKRequant: return moe::launch_requant(p, sms * 8, s);
+      case moe::kKGemm2Small: return moe::launch_gemv(p, moe::kGemm2Bf16, nullptr, sms, s);
       case moe::kKGemm2: return moe::launch_gemm(p, moe::kGemm2Bf16, nullptr, sms, s);
       default: return moe::launch_combine(p, s);
     }
@@ -315,7 +321,8 @@ int moe_fused_get_timing(moe_fused_handle_t* hd, float* ms, int32_t* launches, i
 }
 
 const char* moe_fused_kernel_name(int k) {
-  static const char* names[] = {"dispatch", "quant", "gemm1_swiglu", "requant", "gemm2_bf16", "combine"};
+  static const char* names[] = {"dispatch", "quant", "gemm1_small", "gemm1_swiglu", "requant",
+                                "gemm2_small", "gemm2_bf16", "combine"};
   return (k >= 0 && k < moe::kNumKernels) ? names[k] : "unknown";
 }
 
@@ -328,9 +335,10 @@ int moe_fused_dispatch_noalloc(const int32_t* expert_ids, const uint8_t* x_activ
 int moe_fused_debug_region(moe_fused_handle_t* hd, int region, size_t* offset, size_t* bytes) {
   if (!hd || !offset || !bytes) return MOE_ERR_INVALID_ARG;
   const moe::WsLayout& L = hd->L;
-  const size_t offs[15] = {L.status, L.counts, L.offsets, L.row_of, L.tk_of_row, L.active, L.x_q, L.x_scale,
-                           L.xs_q, L.xs_scale, L.hbuf, L.x2, L.s2, L.y2, L.slots};
-  if (region < 0 || region > 14) return MOE_ERR_INVALID_ARG;
+  const size_t offs[18] = {L.status, L.counts, L.offsets, L.row_of, L.tk_of_row, L.active, L.x_q, L.x_scale,
+                           L.xs_q, L.xs_scale, L.hbuf, L.x2, L.s2, L.y2, L.slots, L.row_token, L.row_scale,
+                           L.shared_row};
+  if (region < 0 || region > 17) return MOE_ERR_INVALID_ARG;
   *offset = offs[region];
   *bytes = L.sizes[region];
   return MOE_OK;
@@ -343,7 +351,10 @@ int moe_fused_debug_gemm_acc(moe_fused_handle_t* hd, const moe_fused_args_t* arg
   if (rc) return rc;
   if ((which != 1 && which != 2) || !acc) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return cuda_fail(moe::launch_gemm(p, which == 1 ? moe::kGemm1Raw : moe::kGemm2Raw, acc, hd->num_sms, s));
+  const int mode = which == 1 ? moe::kGemm1Raw : moe::kGemm2Raw;
+  cudaError_t e = moe::launch_gemv(p, mode, acc, hd->num_sms, s);
+  if (e == cudaSuccess) e = moe::launch_gemm(p, mode, acc, hd->num_sms, s);
+  return cuda_fail(e);
 }
 
 }  // extern "C"

@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(FwdParams
   int32_t* active = ws_ptr<int32_t>(p, p.L.active);
   int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
   int32_t* status = ws_ptr<int32_t>(p, p.L.status);
+  int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
+  int32_t* shared_row = ws_ptr<int32_t>(p, p.L.shared_row);
 
   for (int e = tid; e < E; e += kDispatchThreads) running[e] = 0;
   if (tid == 0) s_skipped = 0;
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(FwdParams
       const int r = running[p.ids[f]] + rank;
       row_of[f] = r;
       tk_of_row[r] = f;
+      row_token[r] = f / K;
     }
   }
 
@@ -139,48 +142,69 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(FwdParams
     const int a = (t < bs) && ((p.mask == nullptr) || (p.mask[t] != 0));
     int chunk_total = 0;
     const int pos = block_exclusive_scan(a, &chunk_total, s_warp);
-    if (a) active[S + pos] = t;
+    if (a) {
+      active[S + pos] = t;
+      if (p.has_shared) row_token[bs * K + S + pos] = t;
+    }
+    if (t < bs && p.has_shared) shared_row[t] = a ? bs * K + S + pos : -1;
     S += chunk_total;
   }
 
-  // 5. slot table: experts with rows in ascending id, then the shared expert
+  // 5. slot tables: experts with rows in ascending id, split by row count,
+  //    then the shared expert in the list its row count selects
   const int st = SlotTable::stride(E);
-  int32_t* s_exp = slots + SlotTable::kHeader;
+  int32_t* b_exp = slots + SlotTable::kHeader;
+  int32_t* b_row0 = b_exp + st;
+  int32_t* b_rows = b_row0 + st;
+  int32_t* b_blk = b_rows + st;
+  int32_t* s_exp = b_blk + st;
   int32_t* s_row0 = s_exp + st;
   int32_t* s_rows = s_row0 + st;
-  int32_t* s_blk = s_rows + st;
-  const int has = (tid < E) && (c > 0);
-  const int nblk = has ? (c + kTokenBlock - 1) / kTokenBlock : 0;
-  int n_routed = 0, routed_blk = 0;
-  const int si = block_exclusive_scan(has, &n_routed, s_warp);
-  const int bi = block_exclusive_scan(nblk, &routed_blk, s_warp);
-  if (has) {
+  const int is_small = (tid < E) && (c > 0) && (c <= kSmallRows);
+  const int is_big = (tid < E) && (c > kSmallRows);
+  const int nblk = is_big ? (c + kTokenBlock - 1) / kTokenBlock : 0;
+  int n_small = 0, n_big = 0, big_blk = 0;
+  const int si = block_exclusive_scan(is_small, &n_small, s_warp);
+  const int bi = block_exclusive_scan(is_big, &n_big, s_warp);
+  const int ki = block_exclusive_scan(nblk, &big_blk, s_warp);
+  if (is_small) {
     s_exp[si] = tid;
     s_row0[si] = off;
     s_rows[si] = c;
-    s_blk[si] = bi;
+  }
+  if (is_big) {
+    b_exp[bi] = tid;
+    b_row0[bi] = off;
+    b_rows[bi] = c;
+    b_blk[bi] = ki;
   }
   if (tid == 0) {
-    int n_slots = n_routed, total_blk = routed_blk;
-    if (p.has_shared && S > 0) {
-      s_exp[n_slots] = -1;
-      s_row0[n_slots] = bs * K;
-      s_rows[n_slots] = S;
-      s_blk[n_slots] = total_blk;
-      total_blk += (S + kTokenBlock - 1) / kTokenBlock;
-      n_slots += 1;
+    const int shared_rows = p.has_shared ? S : 0;
+    if (shared_rows > 0 && shared_rows <= kSmallRows) {
+      s_exp[n_small] = -1;
+      s_row0[n_small] = bs * K;
+      s_rows[n_small] = shared_rows;
+      n_small += 1;
+    } else if (shared_rows > kSmallRows) {
+      b_exp[n_big] = -1;
+      b_row0[n_big] = bs * K;
+      b_rows[n_big] = shared_rows;
+      b_blk[n_big] = big_blk;
+      big_blk += (shared_rows + kTokenBlock - 1) / kTokenBlock;
+      n_big += 1;
     }
-    s_blk[n_slots] = total_blk;
-    slots[0] = n_slots;
-    slots[1] = total_blk;
-    slots[2] = R;
-    slots[3] = (p.has_shared ? S : 0);
+    b_blk[n_big] = big_blk;
+    slots[SlotTable::kNumBig] = n_big;
+    slots[SlotTable::kBigBlocks] = big_blk;
+    slots[SlotTable::kRows] = R;
+    slots[SlotTable::kSharedRows] = shared_rows;
+    slots[SlotTable::kNumSmall] = n_small;
     status[kStSkipped] = s_skipped;
     status[kStErrorFlags] = 0;
     status[kStErrorSite] = 0;
     status[kStRows] = R;
-    status[kStSharedRows] = (p.has_shared ? S : 0);
-    status[kStSlots] = n_slots;
+    status[kStSharedRows] = shared_rows;
+    status[kStSlots] = n_small + n_big;
   }
 }
 
@@ -236,16 +260,31 @@ __device__ void quant_row(const uint16_t* __restrict__ x, const float* __restric
   if (threadIdx.x == 0) *scale_out = __fdiv_rn(1.0f, m);
 }
 
+// One CTA per token.  Besides x_q / x_scale it writes the scale of every
+// GEMM1 row that reads this token (row_scale[row]), so the GEMM kernels need
+// no token lookup to dequantise.
 __global__ void __launch_bounds__(kQuantThreads) quant_kernel(FwdParams p) {
   __shared__ float s_red[33];
   const int t = blockIdx.x;
   if (p.mask && p.mask[t] == 0) return;
   const uint16_t* xr = p.x + static_cast<size_t>(t) * p.h;
-  quant_row(xr, p.smooth, p.h, ws_ptr<int8_t>(p, p.L.x_q) + static_cast<size_t>(t) * p.h,
-            ws_ptr<float>(p, p.L.x_scale) + t, s_red);
+  float* x_scale = ws_ptr<float>(p, p.L.x_scale);
+  float* xs_scale = ws_ptr<float>(p, p.L.xs_scale);
+  quant_row(xr, p.smooth, p.h, ws_ptr<int8_t>(p, p.L.x_q) + static_cast<size_t>(t) * p.h, x_scale + t, s_red);
   if (p.has_shared && !p.share_uses_xq) {
-    quant_row(xr, p.ssmooth, p.h, ws_ptr<int8_t>(p, p.L.xs_q) + static_cast<size_t>(t) * p.h,
-              ws_ptr<float>(p, p.L.xs_scale) + t, s_red);
+    quant_row(xr, p.ssmooth, p.h, ws_ptr<int8_t>(p, p.L.xs_q) + static_cast<size_t>(t) * p.h, xs_scale + t,
+              s_red);
+  }
+  __syncthreads();
+  float* row_scale = ws_ptr<float>(p, p.L.row_scale);
+  const int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
+  if (threadIdx.x < p.topk) {
+    const int r = row_of[t * p.topk + threadIdx.x];
+    if (r >= 0) row_scale[r] = x_scale[t];
+  }
+  if (p.has_shared && threadIdx.x == 32) {
+    const int r = ws_ptr<int32_t>(p, p.L.shared_row)[t];
+    if (r >= 0) row_scale[r] = p.share_uses_xq ? x_scale[t] : xs_scale[t];
   }
 }
 
@@ -285,7 +324,7 @@ cudaError_t dispatch_prepare_attributes(int E) {
 // device with cudaGetSymbolAddress.
 namespace moe {
 
-constexpr size_t kNoallocScratchBytes = size_t(1) << 20;  // 1 MiB
+constexpr size_t kNoallocScratchBytes = size_t(2) << 20;  // 2 MiB
 constexpr int kNoallocMaxPairs = 65536;                   // bs * topk
 constexpr int kNoallocMaxExperts = 1024;
 
@@ -315,6 +354,8 @@ WsLayout noalloc_layout(int bs, int topk, int E) {
   take(L.row_of, pairs * 4);
   take(L.tk_of_row, pairs * 4);
   take(L.active, static_cast<size_t>(bs) * 4);
+  take(L.row_token, pairs * 4);
+  take(L.shared_row, static_cast<size_t>(bs) * 4);
   take(L.slots, static_cast<size_t>(SlotTable::words(E)) * 4);
   L.total = off;
   return L;

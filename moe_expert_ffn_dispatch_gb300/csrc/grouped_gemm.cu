@@ -59,7 +59,7 @@ __device__ __forceinline__ Item decode_item(long it, int J, const int32_t* slots
   const int32_t* s_row0 = s_exp + st;
   const int32_t* s_rows = s_row0 + st;
   const int32_t* s_blk = s_rows + st;
-  const int n_slots = slots[0];
+  const int n_slots = slots[SlotTable::kNumBig];
   // last slot s with J * blk[s] <= it
   int lo = 0, hi = n_slots - 1;
   while (lo < hi) {
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(FwdParams p, 
   const int n_kc = (K + KC - 1) / KC;
   const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
   int32_t* status = ws_ptr<int32_t>(p, p.L.status);
-  const long total_items = static_cast<long>(slots[1]) * J;
+  const long total_items = static_cast<long>(slots[SlotTable::kBigBlocks]) * J;
   const int site = (G1 ? kKGemm1 : kKGemm2) * 16;
 
   if (threadIdx.x == 0) {
@@ -116,8 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(FwdParams p, 
     // ------------------------------------------------------------ producer
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_t = policy_evict_last();
-    const int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
-    const int32_t* active = ws_ptr<int32_t>(p, p.L.active);
+    const int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
     const int8_t* xq = ws_ptr<int8_t>(p, p.L.x_q);
     const int8_t* xsq = p.share_uses_xq ? xq : ws_ptr<int8_t>(p, p.L.xs_q);
     const int8_t* x2 = ws_ptr<int8_t>(p, p.L.x2);
@@ -146,8 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(FwdParams p, 
         if (i < mblk) {
           const int r = item.row0 + tok0 + i;
           if (G1) {
-            if (item.e >= 0) trow[q] = xq + static_cast<size_t>(tk_of_row[r] / p.topk) * p.h;
-            else trow[q] = xsq + static_cast<size_t>(active[r - p.bs * p.topk]) * p.h;
+            trow[q] = (item.e >= 0 ? xq : xsq) + static_cast<size_t>(row_token[r]) * p.h;
           } else {
             trow[q] = x2 + static_cast<size_t>(r) * p.I;
           }
@@ -183,11 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(FwdParams p, 
   const int gid = lane >> 2, tig = lane & 3;
   int32_t* epii = reinterpret_cast<int32_t*>(smem + OFF_EPI);
   float* epif = reinterpret_cast<float*>(smem + OFF_EPI);
-  const float* xsc = ws_ptr<float>(p, p.L.x_scale);
-  const float* xssc = p.share_uses_xq ? xsc : ws_ptr<float>(p, p.L.xs_scale);
-  const float* s2 = ws_ptr<float>(p, p.L.s2);
-  const int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
-  const int32_t* active = ws_ptr<int32_t>(p, p.L.active);
+  const float* row_scale = G1 ? ws_ptr<float>(p, p.L.row_scale) : ws_ptr<float>(p, p.L.s2);
+  const int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
   float* hbuf = ws_ptr<float>(p, p.L.hbuf);
   uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
 
@@ -201,18 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(FwdParams p, 
     named_barrier_sync(1, kConsumerWarps * 32);  // previous epilogue is done with info / epi
     if (ctid < mblk) {
       const int r = item.row0 + tok0 + ctid;
-      int t;
-      float sc;
-      if (item.e >= 0) {
-        t = tk_of_row[r] / p.topk;
-        sc = G1 ? xsc[t] : s2[r];
-      } else {
-        t = active[r - p.bs * p.topk];
-        sc = G1 ? xssc[t] : s2[r];
-      }
       tok_row[ctid] = r;
-      tok_tok[ctid] = t;
-      tok_scale[ctid] = sc;
+      tok_tok[ctid] = row_token[r];
+      tok_scale[ctid] = row_scale[r];
     }
 
     int32_t acc[2][8][4];

@@ -30,6 +30,9 @@ struct WsLayout {
   size_t row_of;     // [bs_max*topk] int32
   size_t tk_of_row;  // [bs_max*topk] int32
   size_t active;     // [bs_max] int32: i-th active token
+  size_t row_token;  // [rows] int32: token of each GEMM row (routed and shared)
+  size_t row_scale;  // [rows] f32: x quant scale of each GEMM1 row
+  size_t shared_row; // [bs_max] int32: shared-expert row of token t, -1 if inactive
   size_t slots;      // slot table (int32), see SlotTable
   size_t x_q;        // [bs_max, h] int8
   size_t x_scale;    // [bs_max] f32
@@ -40,20 +43,28 @@ struct WsLayout {
   size_t s2;         // [rows] f32
   size_t y2;         // [bs_max*topk, h] bf16 (== hbuf)
   size_t total;
-  size_t sizes[16];  // bytes per region id (debug_region)
+  size_t sizes[20];  // bytes per region id (debug_region)
 };
 
-// Slot table: one slot per expert with rows (ascending id), then the shared
-// expert.  Stored as int32 words at layout.slots:
-//   [0] n_slots  [1] total token blocks  [2] R  [3] S
-//   then four arrays of (E + 2) words: expert id (-1 = shared), first row,
-//   row count, exclusive prefix of token blocks.
+// Slot table: the experts that received rows, split by row count.  Experts
+// with at most kSmallRows rows ("small", decode-like) go to the weight-
+// streaming dp4a kernel, the others ("big") to the tensor-core kernel in
+// token blocks of kTokenBlock rows.  The shared expert is one more slot in
+// whichever list its row count selects (expert id -1).  Stored as int32
+// words at layout.slots:
+//   header: [0] n_big  [1] token blocks over big slots  [2] R  [3] S
+//           [4] n_small  [5..7] reserved
+//   then seven arrays of stride (E + 2):
+//     big:   expert id, first row, row count, exclusive prefix of blocks
+//     small: expert id, first row, row count
 struct SlotTable {
-  static constexpr int kHeader = 4;
+  static constexpr int kHeader = 8;
+  static constexpr int kNumBig = 0, kBigBlocks = 1, kRows = 2, kSharedRows = 3, kNumSmall = 4;
   static __host__ __device__ int stride(int E) { return E + 2; }
-  static __host__ __device__ int words(int E) { return kHeader + 4 * stride(E); }
+  static __host__ __device__ int words(int E) { return kHeader + 7 * stride(E); }
 };
 
+constexpr int kSmallRows = 8;   // experts with <= this many rows take the dp4a path
 constexpr int kTokenBlock = 64;  // token rows per GEMM work item
 
 // ---------------------------------------------------------------- params
@@ -87,7 +98,17 @@ __host__ __device__ inline T* ws_ptr(const FwdParams& p, size_t off) {
 }
 
 // kernel ids (timing / status sites)
-enum KernelId : int { kKDispatch = 0, kKQuant = 1, kKGemm1 = 2, kKRequant = 3, kKGemm2 = 4, kKCombine = 5, kNumKernels = 6 };
+enum KernelId : int {
+  kKDispatch = 0,
+  kKQuant = 1,
+  kKGemm1Small = 2,
+  kKGemm1 = 3,
+  kKRequant = 4,
+  kKGemm2Small = 5,
+  kKGemm2 = 6,
+  kKCombine = 7,
+  kNumKernels = 8
+};
 
 // GEMM modes
 enum GemmMode : int { kGemm1SwiGLU = 0, kGemm2Bf16 = 1, kGemm1Raw = 2, kGemm2Raw = 3 };
@@ -100,6 +121,8 @@ cudaError_t launch_gemm(const FwdParams& p, int mode, int32_t* raw_acc, int num_
 cudaError_t launch_requant(const FwdParams& p, int num_ctas, cudaStream_t s);
 cudaError_t launch_combine(const FwdParams& p, cudaStream_t s);
 cudaError_t gemm_prepare_attributes();
+cudaError_t launch_gemv(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);
+cudaError_t gemv_prepare_attributes();
 cudaError_t dispatch_prepare_attributes(int E);
 int dispatch_noalloc(const int32_t* expert_ids, const uint8_t* mask, int bs, int topk, int E,
                      int32_t* expert_token_nums, int32_t* expand_row, cudaStream_t s);

@@ -24,7 +24,7 @@ constexpr float kInv127 = 1.0f / 127.0f;  // the fp32 nearest to 1/127
 __global__ void __launch_bounds__(kRequantThreads) requant_kernel(FwdParams p) {
   __shared__ float s_red[33];
   const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
-  const int R = slots[2], S = slots[3];
+  const int R = slots[SlotTable::kRows], S = slots[SlotTable::kSharedRows];
   const int I = p.I;
   const float* hbuf = ws_ptr<float>(p, p.L.hbuf);
   int8_t* x2 = ws_ptr<int8_t>(p, p.L.x2);

@@ -73,5 +73,5 @@ def test_workspace_size_and_config_checks(built):
 def test_strerror_and_names(built):
     assert m.moe_fused_strerror(0) == "ok"
     assert "workspace" in m.moe_fused_strerror(m.MOE_ERR_WORKSPACE_TOO_SMALL)
-    assert [m.moe_fused_kernel_name(k) for k in range(6)] == m.KERNEL_NAMES
+    assert [m.moe_fused_kernel_name(k) for k in range(len(m.KERNEL_NAMES))] == m.KERNEL_NAMES
     assert m.moe_fused_destroy(0) == 0
