@@ -132,31 +132,28 @@ class ClockSampler:
                 "reasons": rs, "samples": len(sm)}
 
 
-SMALL_ROWS = 8  # experts with at most this many rows run in the weight-streaming kernels
-
-
 def algorithmic_bytes(wl, counts_per_expert, n_active):
     """Bytes each kernel must move at least once (the roofline numerator).
 
     Per touched expert (routed experts with >= 1 row, plus the shared expert
-    when it has rows): GEMM1 reads W1 (2I*h int8) and its scales (2I fp32);
-    GEMM2 reads W2 (h*I int8) and its scales (h fp32).  Per row GEMM1 reads
-    the row's x_q (h bytes) and writes h (I fp32); GEMM2 reads x2 (I bytes)
-    and s2 and writes a bf16 row of h.  Experts with at most SMALL_ROWS rows
-    run in the *_small kernels, the rest in the tensor-core kernels.  The
-    step total counts weights once plus the block's own inputs and outputs
-    (scratch that a fully fused kernel could keep on chip is not counted)."""
+    when it has rows) GEMM1 reads W1 (2I*h int8) and its scales (2I fp32);
+    per row it reads the row's x_q (h bytes), writes h (I fp32), and its fused
+    requant reads h back and writes x2 (I) and s2.  GEMM2 reads W2 (h*I int8)
+    and scales (h fp32); per row x2 and s2 in, a bf16 row of h out, and the
+    fused combine reads each routed row once more and writes bf16 outputs.
+    The step total counts weights once plus the block's own inputs and
+    outputs (scratch a fully fused kernel could keep on chip is not counted)."""
     h, I, K, bs = wl.hidden, wl.inter, wl.topk, wl.bs
     groups = [c for c in counts_per_expert if c > 0]
-    if wl.has_shared and n_active > 0:
-        groups.append(n_active)
-    out = {"gemm1_small": 0, "gemm1_swiglu": 0, "gemm2_small": 0, "gemm2_bf16": 0}
-    for m in groups:
-        small = m <= SMALL_ROWS
-        out["gemm1_small" if small else "gemm1_swiglu"] += 2 * I * h + 8 * I + m * (h + 4 * I)
-        out["gemm2_small" if small else "gemm2_bf16"] += h * I + 4 * h + m * (I + 4 + 2 * h)
+    R = sum(counts_per_expert)
+    shared = n_active if (wl.has_shared and n_active > 0) else 0
+    if shared:
+        groups.append(shared)
     touched = len(groups)
     rows = sum(groups)
+    out = {}
+    out["gemm1_swiglu_requant"] = touched * (2 * I * h + 8 * I) + rows * (h + 4 * I + 4 * I + I + 4)
+    out["gemm2_combine"] = touched * (h * I + 4 * h) + rows * (I + 4 + 2 * h) + R * 2 * h + bs * 2 * h
     out["step"] = touched * (2 * I * h + h * I + 4 * (2 * I + h)) + bs * h * 2 + bs * K * 8 + \
         bs * h * 2 * (2 if wl.has_shared else 1) + wl.num_experts * 4
     out["int_ops"] = 2 * rows * (2 * I * h + h * I)
@@ -165,8 +162,7 @@ def algorithmic_bytes(wl, counts_per_expert, n_active):
     return out
 
 
-KERNEL_SOURCES = {"gemm1_small": "grouped_gemv.cu", "gemm2_small": "grouped_gemv.cu",
-                  "gemm1_swiglu": "grouped_gemm.cu", "gemm2_bf16": "grouped_gemm.cu"}
+KERNEL_SOURCES = {"gemm1_swiglu_requant": "moe_gemm.cu", "gemm2_combine": "moe_gemm.cu"}
 
 
 # ---------------------------------------------------------------- our arm

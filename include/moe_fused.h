@@ -185,9 +185,8 @@ int moe_fused_dispatch_noalloc(const int32_t* expert_ids, const uint8_t* x_activ
  * `stream`.  get_timing synchronises the recorded events, writes for each
  * kernel id k < max_kernels the summed milliseconds ms[k] and launch count
  * launches[k] (host arrays), returns the number of kernel ids, and clears the
- * record.  Kernel ids: 0 dispatch, 1 quant, 2 gemm1 for experts with at most
- * 8 rows (weight streaming), 3 gemm1 for the others (tensor cores), 4 requant,
- * 5 gemm2 (at most 8 rows), 6 gemm2 (others), 7 combine. */
+ * record.  Kernel ids: 0 dispatch + quant, 1 GEMM1 + SwiGLU + requant,
+ * 2 GEMM2 + bf16 dequant + combine. */
 int moe_fused_set_timing(moe_fused_handle_t* handle, int enable);
 int moe_fused_get_timing(moe_fused_handle_t* handle, float* ms, int32_t* launches, int max_kernels);
 const char* moe_fused_kernel_name(int kernel_id);
@@ -200,6 +199,8 @@ const char* moe_fused_kernel_name(int kernel_id);
  *   7 x_scale [bs_max] f32  8 xs_q [bs_max,h] int8  9 xs_scale [bs_max]
  *   10 h [rows,inter] f32  11 x2 [rows,inter] int8  12 s2 [rows] f32
  *   13 y2 [bs_max*topk,h] bf16 (aliases region 10)  14 slot table
+ *   15 row_token [rows] int32  16 shared_row [bs_max] int32
+ *   17 row-block counters  18 token counters [bs_max]  19 token totals [bs_max]
  * `rows` = bs*topk + bs: routed row r at index r (r < R), the shared expert's
  * i-th active token at index bs*topk + i.  Writes *offset and *bytes. */
 int moe_fused_debug_region(moe_fused_handle_t* handle, int region, size_t* offset, size_t* bytes);

@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 SO = os.path.join(HERE, "_moe_fused.so")
-SOURCES = ["api.cu", "dispatch_quant.cu", "grouped_gemm.cu", "grouped_gemv.cu", "requant_combine.cu"]
+SOURCES = ["api.cu", "dispatch_quant.cu", "moe_gemm.cu"]
 HEADERS = ["device_prims.cuh", "moe_internal.h"]
 
 NVCC_FLAGS = [

@@ -1,11 +1,12 @@
 // C ABI of the fused MoE expert block: argument checks, workspace planning,
 // launch sequence, per-kernel timing and the test-only entry points.
 //
-// Launch sequence of one forward (the pages' Process(): dispatch, GMM1 with
-// SwiGLU + quant, GMM2, combine -- FusedDeepMoE analysis §3.2):
-//   dispatch (1 CTA) -> quant (1 CTA per token) -> GEMM1 + SwiGLU (persistent)
-//   -> requant (persistent) -> GEMM2 + bf16 dequant (persistent) -> combine.
-// Kernel boundaries carry the dependencies; no kernel waits on another.
+// Launch sequence of one forward (Process() of the FusedDeepMoE analysis
+// §3.2: dispatch, GMM1 with SwiGLU + quant, GMM2 with combine):
+//   dispatch + quant -> GEMM1 + SwiGLU + requant -> GEMM2 + bf16 dequant +
+//   combine.
+// Kernel boundaries carry the dependencies; inside a GEMM launch the fused
+// epilogues run in the CTA that finishes a block last.  No CTA waits.
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -59,26 +60,29 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
     L.sizes[id] = bytes;
     off = align_up(off + (bytes ? bytes : 1));
   };
-  take(L.status, 64 * sizeof(int32_t), 0);
-  take(L.counts, E * 4, 1);
-  take(L.offsets, (E + 1) * 4, 2);
-  take(L.row_of, routed * 4, 3);
-  take(L.tk_of_row, routed * 4, 4);
-  take(L.active, bs * 4, 5);
-  take(L.x_q, bs * h, 6);
-  take(L.x_scale, bs * 4, 7);
-  take(L.xs_q, c.has_shared ? bs * h : 0, 8);
-  take(L.xs_scale, c.has_shared ? bs * 4 : 0, 9);
+  const size_t big_blocks = (rows + moe::kTokenBlock - 1) / moe::kTokenBlock + E + 2;
+  take(L.status, 64 * sizeof(int32_t), moe::kRegStatus);
+  take(L.counts, E * 4, moe::kRegCounts);
+  take(L.offsets, (E + 1) * 4, moe::kRegOffsets);
+  take(L.row_of, routed * 4, moe::kRegRowOf);
+  take(L.tk_of_row, routed * 4, moe::kRegTkOfRow);
+  take(L.active, bs * 4, moe::kRegActive);
+  take(L.x_q, bs * h, moe::kRegXq);
+  take(L.x_scale, bs * 4, moe::kRegXScale);
+  take(L.xs_q, c.has_shared ? bs * h : 0, moe::kRegXsq);
+  take(L.xs_scale, c.has_shared ? bs * 4 : 0, moe::kRegXsScale);
   const size_t hbytes = rows * I * 4, ybytes = routed * h * 2;
-  take(L.hbuf, hbytes > ybytes ? hbytes : ybytes, 10);
-  take(L.x2, rows * I, 11);
-  take(L.s2, rows * 4, 12);
+  take(L.hbuf, hbytes > ybytes ? hbytes : ybytes, moe::kRegH);
+  take(L.x2, rows * I, moe::kRegX2);
+  take(L.s2, rows * 4, moe::kRegS2);
   L.y2 = L.hbuf;
-  L.sizes[13] = ybytes;
-  take(L.slots, static_cast<size_t>(moe::SlotTable::words(c.num_experts)) * 4, 14);
-  take(L.row_token, rows * 4, 15);
-  take(L.row_scale, rows * 4, 16);
-  take(L.shared_row, bs * 4, 17);
+  L.sizes[moe::kRegY2] = ybytes;
+  take(L.slots, static_cast<size_t>(moe::SlotTable::words(c.num_experts)) * 4, moe::kRegSlots);
+  take(L.row_token, rows * 4, moe::kRegRowToken);
+  take(L.shared_row, bs * 4, moe::kRegSharedRow);
+  take(L.blk_ticket, (static_cast<size_t>(moe::SlotTable::stride(c.num_experts)) + big_blocks) * 4, moe::kRegBlkTicket);
+  take(L.tok_ticket, bs * 4, moe::kRegTokTicket);
+  take(L.tok_expect, bs * 4, moe::kRegTokExpect);
   L.total = off;
   return L;
 }
@@ -120,6 +124,7 @@ int build_params(moe_fused_handle* hd, const moe_fused_args_t* a, void* ws, size
   p->I = c.inter;
   p->has_shared = c.has_shared;
   p->share_uses_xq = c.has_shared && (a->expert_smooth_scales == a->share_smooth_scales);
+  p->with_tickets = 1;
   p->x = static_cast<const uint16_t*>(a->x);
   p->ids = a->expert_ids;
   p->scales = a->expert_scales;
@@ -198,8 +203,7 @@ int moe_fused_create(const moe_fused_config_t* cfg, moe_fused_handle_t** out_han
   hd->timing = false;
   cudaError_t e = cudaGetDevice(&hd->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&hd->num_sms, cudaDevAttrMultiProcessorCount, hd->device);
-  if (e == cudaSuccess) e = moe::gemm_prepare_attributes();
-  if (e == cudaSuccess) e = moe::gemv_prepare_attributes();
+  if (e == cudaSuccess) e = moe::moe_gemm_prepare_attributes();
   if (e == cudaSuccess) e = moe::dispatch_prepare_attributes(1024);
   if (e != cudaSuccess) {
     delete hd;
@@ -232,14 +236,9 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
   const int sms = hd->num_sms;
   auto run = [&](int k) -> cudaError_t {
     switch (k) {
-      case moe::kKDispatch: return moe::launch_dispatch(p, s);
-      case moe::kKQuant: return moe::launch_quant(p, s);
-      case moe::kKGemm1Small: return moe::launch_gemv(p, moe::kGemm1SwiGLU, nullptr, sms, s);
-      case moe::kKGemm1: return moe::launch_gemm(p, moe::kGemm1SwiGLU, nullptr, sms, s);
-      case moe::kKRequant: return moe::launch_requant(p, sms * 8, s);
-      case moe::kKGemm2Small: return moe::launch_gemv(p, moe::kGemm2Bf16, nullptr, sms, s);
-      case moe::kKGemm2: return moe::launch_gemm(p, moe::kGemm2Bf16, nullptr, sms, s);
-      default: return moe::launch_combine(p, s);
+      case moe::kKDispatchQuant: return moe::launch_dispatch_quant(p, s);
+      case moe::kKGemm1: return moe::launch_moe_gemm(p, moe::kGemm1SwiGLU, nullptr, sms, s);
+      default: return moe::launch_moe_gemm(p, moe::kGemm2Bf16, nullptr, sms, s);
     }
   };
   e = cudaSuccess;
@@ -321,8 +320,7 @@ int moe_fused_get_timing(moe_fused_handle_t* hd, float* ms, int32_t* launches, i
 }
 
 const char* moe_fused_kernel_name(int k) {
-  static const char* names[] = {"dispatch", "quant", "gemm1_small", "gemm1_swiglu", "requant",
-                                "gemm2_small", "gemm2_bf16", "combine"};
+  static const char* names[] = {"dispatch_quant", "gemm1_swiglu_requant", "gemm2_combine"};
   return (k >= 0 && k < moe::kNumKernels) ? names[k] : "unknown";
 }
 
@@ -335,10 +333,10 @@ int moe_fused_dispatch_noalloc(const int32_t* expert_ids, const uint8_t* x_activ
 int moe_fused_debug_region(moe_fused_handle_t* hd, int region, size_t* offset, size_t* bytes) {
   if (!hd || !offset || !bytes) return MOE_ERR_INVALID_ARG;
   const moe::WsLayout& L = hd->L;
-  const size_t offs[18] = {L.status, L.counts, L.offsets, L.row_of, L.tk_of_row, L.active, L.x_q, L.x_scale,
-                           L.xs_q, L.xs_scale, L.hbuf, L.x2, L.s2, L.y2, L.slots, L.row_token, L.row_scale,
-                           L.shared_row};
-  if (region < 0 || region > 17) return MOE_ERR_INVALID_ARG;
+  const size_t offs[moe::kNumRegions] = {L.status, L.counts, L.offsets, L.row_of, L.tk_of_row, L.active, L.x_q,
+                                         L.x_scale, L.xs_q, L.xs_scale, L.hbuf, L.x2, L.s2, L.y2, L.slots,
+                                         L.row_token, L.shared_row, L.blk_ticket, L.tok_ticket, L.tok_expect};
+  if (region < 0 || region >= moe::kNumRegions) return MOE_ERR_INVALID_ARG;
   *offset = offs[region];
   *bytes = L.sizes[region];
   return MOE_OK;
@@ -352,9 +350,7 @@ int moe_fused_debug_gemm_acc(moe_fused_handle_t* hd, const moe_fused_args_t* arg
   if ((which != 1 && which != 2) || !acc) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int mode = which == 1 ? moe::kGemm1Raw : moe::kGemm2Raw;
-  cudaError_t e = moe::launch_gemv(p, mode, acc, hd->num_sms, s);
-  if (e == cudaSuccess) e = moe::launch_gemm(p, mode, acc, hd->num_sms, s);
-  return cuda_fail(e);
+  return cuda_fail(moe::launch_moe_gemm(p, mode, acc, hd->num_sms, s));
 }
 
 }  // extern "C"

@@ -8,6 +8,9 @@
 // is its rank by flat index t*topk + k -- the same stable order a sequential
 // counting sort produces, with no atomics deciding the order.
 //
+// Both run in one launch: CTA 0 dispatches while the other CTAs quantise
+// (they are independent; the GEMM kernels join them).
+//
 // Quant follows §4.1 / §7.3 and the W8A8 contract of the DeepSeek-V4 decode
 // case study: xs = x * smooth, amax = max(max|xs|, 1e-4), m = 127 / amax,
 // q = RNE(xs * m) clamped to +-127, scale = 1 / m.  Every fp32 operation is an
@@ -54,8 +57,9 @@ __device__ int block_exclusive_scan(int v, int* total, int* s_warp) {
   return excl;
 }
 
-__global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(FwdParams p) {
-  extern __shared__ int32_t dsm[];
+// Dispatch by one 1024-thread CTA.  dsm: dynamic shared memory of
+// dispatch_smem_bytes(E).
+__device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
   __shared__ int s_warp[32];
   __shared__ int s_skipped;
   const int E = p.E, K = p.topk, bs = p.bs;
@@ -206,32 +210,57 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(FwdParams
     status[kStSharedRows] = shared_rows;
     status[kStSlots] = n_small + n_big;
   }
+  if (p.with_tickets) {
+    // per-forward epoch of the last-arriver counters used by the GEMM kernels
+    int32_t* blk_ticket = ws_ptr<int32_t>(p, p.L.blk_ticket);
+    const int nt = static_cast<int>(p.L.sizes[kRegBlkTicket] / 4);
+    for (int i = tid; i < nt; i += kDispatchThreads) blk_ticket[i] = 0;
+    int32_t* tok_ticket = ws_ptr<int32_t>(p, p.L.tok_ticket);
+    int32_t* tok_expect = ws_ptr<int32_t>(p, p.L.tok_expect);
+    for (int t = tid; t < bs; t += kDispatchThreads) {
+      int nvalid = 0;
+      if ((p.mask == nullptr) || (p.mask[t] != 0)) {
+        for (int k = 0; k < K; ++k) {
+          const int id = p.ids[t * K + k];
+          nvalid += (id >= 0 && id < E);
+        }
+      }
+      tok_ticket[t] = 0;
+      tok_expect[t] = nvalid * p.h;
+    }
+  }
 }
 
-__device__ __forceinline__ float block_max(float v, float* s_red) {
+__global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(FwdParams p) {
+  extern __shared__ int32_t dsm[];
+  dispatch_block(p, dsm);
+}
+
+constexpr int kQuantGroups = kDispatchThreads / kQuantThreads;  // tokens per quant CTA
+
+// max over the 256 threads of one quant group (named barrier 1 + group)
+__device__ __forceinline__ float group_max(float v, float* s_red, int group) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gt = threadIdx.x & (kQuantThreads - 1);
+  const int lane = gt & 31, warp = gt >> 5;
   if (lane == 0) s_red[warp] = v;
-  __syncthreads();
-  float r = (lane < (int)(blockDim.x >> 5)) ? s_red[lane] : 0.0f;
-  if (warp == 0) {
+  named_barrier_sync(1 + group, kQuantThreads);
+  float r = s_red[0];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, o));
-    if (lane == 0) s_red[32] = r;
-  }
-  __syncthreads();
-  r = s_red[32];
-  __syncthreads();
+  for (int w = 1; w < kQuantThreads / 32; ++w) r = fmaxf(r, s_red[w]);
+  named_barrier_sync(1 + group, kQuantThreads);
   return r;
 }
 
-// Quantise one bf16 row (h multiple of 64) with optional smooth scales.
+// Quantise one bf16 row (h multiple of 64) with optional smooth scales, by
+// the 256 threads of one group.
 __device__ void quant_row(const uint16_t* __restrict__ x, const float* __restrict__ smooth, int h,
-                          int8_t* __restrict__ q, float* __restrict__ scale_out, float* s_red) {
+                          int8_t* __restrict__ q, float* __restrict__ scale_out, float* s_red, int group) {
+  const int gt = threadIdx.x & (kQuantThreads - 1);
   const int n8 = h >> 3;
   float amax = 0.0f;
-  for (int i = threadIdx.x; i < n8; i += kQuantThreads) {
+  for (int i = gt; i < n8; i += kQuantThreads) {
     const uint4 v = reinterpret_cast<const uint4*>(x)[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -241,10 +270,10 @@ __device__ void quant_row(const uint16_t* __restrict__ x, const float* __restric
       amax = fmaxf(amax, fabsf(f));
     }
   }
-  amax = block_max(amax, s_red);
+  amax = group_max(amax, s_red, group);
   if (amax < kAmaxEps) amax = kAmaxEps;
   const float m = __fdiv_rn(127.0f, amax);
-  for (int i = threadIdx.x; i < n8; i += kQuantThreads) {
+  for (int i = gt; i < n8; i += kQuantThreads) {
     const uint4 v = reinterpret_cast<const uint4*>(x)[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t packed[2] = {0u, 0u};
@@ -257,54 +286,72 @@ __device__ void quant_row(const uint16_t* __restrict__ x, const float* __restric
     }
     reinterpret_cast<uint2*>(q)[i] = make_uint2(packed[0], packed[1]);
   }
-  if (threadIdx.x == 0) *scale_out = __fdiv_rn(1.0f, m);
+  if (gt == 0) *scale_out = __fdiv_rn(1.0f, m);
 }
 
-// One CTA per token.  Besides x_q / x_scale it writes the scale of every
-// GEMM1 row that reads this token (row_scale[row]), so the GEMM kernels need
-// no token lookup to dequantise.
-__global__ void __launch_bounds__(kQuantThreads) quant_kernel(FwdParams p) {
-  __shared__ float s_red[33];
-  const int t = blockIdx.x;
-  if (p.mask && p.mask[t] == 0) return;
+// Quant of token t by one 256-thread group.  Tokens that no expert row will
+// combine into get their zero output rows here: inactive tokens (output and
+// share_output) and active tokens whose ids are all outside [0, E) (output).
+__device__ void quant_token(const FwdParams& p, int t, float* s_red, int group) {
+  const int gt = threadIdx.x & (kQuantThreads - 1);
+  const bool act = (p.mask == nullptr) || (p.mask[t] != 0);
+  int nvalid = 0;
+  if (act)
+    for (int k = 0; k < p.topk; ++k) {
+      const int id = p.ids[t * p.topk + k];
+      nvalid += (id >= 0 && id < p.E);
+    }
+  const int n8 = p.h >> 3;
+  if (nvalid == 0) {
+    uint4* out = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * p.h);
+    for (int i = gt; i < n8; i += kQuantThreads) out[i] = make_uint4(0, 0, 0, 0);
+  }
+  if (!act) {
+    if (p.has_shared) {
+      uint4* so = reinterpret_cast<uint4*>(p.sout + static_cast<size_t>(t) * p.h);
+      for (int i = gt; i < n8; i += kQuantThreads) so[i] = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
   const uint16_t* xr = p.x + static_cast<size_t>(t) * p.h;
-  float* x_scale = ws_ptr<float>(p, p.L.x_scale);
-  float* xs_scale = ws_ptr<float>(p, p.L.xs_scale);
-  quant_row(xr, p.smooth, p.h, ws_ptr<int8_t>(p, p.L.x_q) + static_cast<size_t>(t) * p.h, x_scale + t, s_red);
+  quant_row(xr, p.smooth, p.h, ws_ptr<int8_t>(p, p.L.x_q) + static_cast<size_t>(t) * p.h,
+            ws_ptr<float>(p, p.L.x_scale) + t, s_red, group);
   if (p.has_shared && !p.share_uses_xq) {
-    quant_row(xr, p.ssmooth, p.h, ws_ptr<int8_t>(p, p.L.xs_q) + static_cast<size_t>(t) * p.h, xs_scale + t,
-              s_red);
+    quant_row(xr, p.ssmooth, p.h, ws_ptr<int8_t>(p, p.L.xs_q) + static_cast<size_t>(t) * p.h,
+              ws_ptr<float>(p, p.L.xs_scale) + t, s_red, group);
   }
-  __syncthreads();
-  float* row_scale = ws_ptr<float>(p, p.L.row_scale);
-  const int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
-  if (threadIdx.x < p.topk) {
-    const int r = row_of[t * p.topk + threadIdx.x];
-    if (r >= 0) row_scale[r] = x_scale[t];
+}
+
+// CTA 0 dispatches; CTA b >= 1 quantises tokens 4(b-1) .. 4(b-1)+3, one per
+// 256-thread group.  The two halves are independent: nothing the quant
+// writes depends on the dispatch.
+__global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(FwdParams p) {
+  extern __shared__ int32_t dsm[];
+  __shared__ float s_red[kQuantGroups][8];
+  if (blockIdx.x == 0) {
+    dispatch_block(p, dsm);
+    return;
   }
-  if (p.has_shared && threadIdx.x == 32) {
-    const int r = ws_ptr<int32_t>(p, p.L.shared_row)[t];
-    if (r >= 0) row_scale[r] = p.share_uses_xq ? x_scale[t] : xs_scale[t];
-  }
+  const int group = threadIdx.x / kQuantThreads;
+  const int t = (blockIdx.x - 1) * kQuantGroups + group;
+  if (t < p.bs) quant_token(p, t, s_red[group], group);
 }
 
 }  // namespace
 
 size_t dispatch_smem_bytes(int E) { return sizeof(int32_t) * static_cast<size_t>(33 * E); }
 
-cudaError_t launch_dispatch(const FwdParams& p, cudaStream_t s) {
-  dispatch_kernel<<<1, kDispatchThreads, dispatch_smem_bytes(p.E), s>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_quant(const FwdParams& p, cudaStream_t s) {
-  if (p.bs == 0) return cudaSuccess;
-  quant_kernel<<<p.bs, kQuantThreads, 0, s>>>(p);
+cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s) {
+  const int blocks = 1 + (p.bs + kQuantGroups - 1) / kQuantGroups;
+  dispatch_quant_kernel<<<blocks, kDispatchThreads, dispatch_smem_bytes(p.E), s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t dispatch_prepare_attributes(int E) {
-  return cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(dispatch_smem_bytes(E)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(dispatch_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(dispatch_smem_bytes(E)));
 }
 
@@ -389,6 +436,7 @@ int dispatch_noalloc(const int32_t* expert_ids, const uint8_t* mask, int bs, int
   p.E = E;
   p.topk = topk;
   p.has_shared = 0;
+  p.with_tickets = 0;
   p.ids = expert_ids;
   p.mask = mask;
   p.token_nums = expert_token_nums;

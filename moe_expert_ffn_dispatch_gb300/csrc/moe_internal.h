@@ -30,10 +30,6 @@ struct WsLayout {
   size_t row_of;     // [bs_max*topk] int32
   size_t tk_of_row;  // [bs_max*topk] int32
   size_t active;     // [bs_max] int32: i-th active token
-  size_t row_token;  // [rows] int32: token of each GEMM row (routed and shared)
-  size_t row_scale;  // [rows] f32: x quant scale of each GEMM1 row
-  size_t shared_row; // [bs_max] int32: shared-expert row of token t, -1 if inactive
-  size_t slots;      // slot table (int32), see SlotTable
   size_t x_q;        // [bs_max, h] int8
   size_t x_scale;    // [bs_max] f32
   size_t xs_q;       // [bs_max, h] int8 (shared-expert quant)
@@ -42,8 +38,21 @@ struct WsLayout {
   size_t x2;         // [rows, I] int8
   size_t s2;         // [rows] f32
   size_t y2;         // [bs_max*topk, h] bf16 (== hbuf)
+  size_t slots;      // slot table (int32), see SlotTable
+  size_t row_token;  // [rows] int32: token of each GEMM row (routed and shared)
+  size_t shared_row; // [bs_max] int32: shared-expert row of token t, -1 if inactive
+  size_t blk_ticket; // int32 per row block: GEMM1 tiles done (last one requantises)
+  size_t tok_ticket; // [bs_max] int32: GEMM2 output columns done per token
+  size_t tok_expect; // [bs_max] int32: columns that complete a token (rows * h)
   size_t total;
-  size_t sizes[20];  // bytes per region id (debug_region)
+  size_t sizes[24];  // bytes per region id (debug_region)
+};
+
+// Region ids (moe_fused_debug_region); the order of WsLayout's fields.
+enum Region : int {
+  kRegStatus = 0, kRegCounts, kRegOffsets, kRegRowOf, kRegTkOfRow, kRegActive, kRegXq, kRegXScale,
+  kRegXsq, kRegXsScale, kRegH, kRegX2, kRegS2, kRegY2, kRegSlots, kRegRowToken, kRegSharedRow,
+  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kNumRegions
 };
 
 // Slot table: the experts that received rows, split by row count.  Experts
@@ -71,6 +80,7 @@ constexpr int kTokenBlock = 64;  // token rows per GEMM work item
 struct FwdParams {
   int32_t bs, h, E, topk, I, has_shared;
   int32_t share_uses_xq;  // shared quant identical to routed quant (same smooth vector)
+  int32_t with_tickets;   // dispatch resets the GEMM epilogue counters (forward path)
   const uint16_t* x;
   const int32_t* ids;
   const float* scales;
@@ -98,31 +108,16 @@ __host__ __device__ inline T* ws_ptr(const FwdParams& p, size_t off) {
 }
 
 // kernel ids (timing / status sites)
-enum KernelId : int {
-  kKDispatch = 0,
-  kKQuant = 1,
-  kKGemm1Small = 2,
-  kKGemm1 = 3,
-  kKRequant = 4,
-  kKGemm2Small = 5,
-  kKGemm2 = 6,
-  kKCombine = 7,
-  kNumKernels = 8
-};
+enum KernelId : int { kKDispatchQuant = 0, kKGemm1 = 1, kKGemm2 = 2, kNumKernels = 3 };
 
 // GEMM modes
 enum GemmMode : int { kGemm1SwiGLU = 0, kGemm2Bf16 = 1, kGemm1Raw = 2, kGemm2Raw = 3 };
 
 // ---------------------------------------------------------------- launches
 size_t dispatch_smem_bytes(int E);
-cudaError_t launch_dispatch(const FwdParams& p, cudaStream_t s);
-cudaError_t launch_quant(const FwdParams& p, cudaStream_t s);
-cudaError_t launch_gemm(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);
-cudaError_t launch_requant(const FwdParams& p, int num_ctas, cudaStream_t s);
-cudaError_t launch_combine(const FwdParams& p, cudaStream_t s);
-cudaError_t gemm_prepare_attributes();
-cudaError_t launch_gemv(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);
-cudaError_t gemv_prepare_attributes();
+cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_moe_gemm(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);
+cudaError_t moe_gemm_prepare_attributes();
 cudaError_t dispatch_prepare_attributes(int E);
 int dispatch_noalloc(const int32_t* expert_ids, const uint8_t* mask, int bs, int topk, int E,
                      int32_t* expert_token_nums, int32_t* expand_row, cudaStream_t s);

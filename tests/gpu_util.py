@@ -105,8 +105,8 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
     di = device_inputs(inp, dev)
     dw = device_weights(inp, dev)
     if staged and bs > 0:
-        # stop after requant: h is reused by y2 once GEMM2 runs
-        blk.forward_inputs(di, dw, until=m.KERNEL_ID["requant"])
+        # stop after GEMM1 (SwiGLU + requant): h is reused by y2 once GEMM2 runs
+        blk.forward_inputs(di, dw, until=m.KERNEL_ID["gemm1_swiglu_requant"])
         torch.cuda.synchronize()
         staged_h = blk.region("h").clone().cpu()
     out, sout, nums = blk.forward_inputs(di, dw)
