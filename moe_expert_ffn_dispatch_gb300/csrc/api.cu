@@ -83,6 +83,7 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
   take(L.blk_ticket, (static_cast<size_t>(moe::SlotTable::stride(c.num_experts)) + big_blocks) * 4, moe::kRegBlkTicket);
   take(L.tok_ticket, bs * 4, moe::kRegTokTicket);
   take(L.tok_expect, bs * 4, moe::kRegTokExpect);
+  take(L.ranges, 2 * (moe::kMaxCtas + 1) * 4, moe::kRegRanges);
   L.total = off;
   return L;
 }
@@ -125,6 +126,8 @@ int build_params(moe_fused_handle* hd, const moe_fused_args_t* a, void* ws, size
   p->has_shared = c.has_shared;
   p->share_uses_xq = c.has_shared && (a->expert_smooth_scales == a->share_smooth_scales);
   p->with_tickets = 1;
+  p->small_rows = (c.hidden <= moe::kSmallMaxK && c.inter <= moe::kSmallMaxK) ? moe::kSmallRows : 0;
+  p->num_ctas = hd->num_sms < moe::kMaxCtas ? hd->num_sms : moe::kMaxCtas;
   p->x = static_cast<const uint16_t*>(a->x);
   p->ids = a->expert_ids;
   p->scales = a->expert_scales;
@@ -233,7 +236,7 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
     if (e == cudaSuccess) e = cudaMemsetAsync(p.ws + p.L.status, 0, 64 * sizeof(int32_t), s);
     return cuda_fail(e);
   }
-  const int sms = hd->num_sms;
+  const int sms = p.num_ctas;
   auto run = [&](int k) -> cudaError_t {
     switch (k) {
       case moe::kKDispatchQuant: return moe::launch_dispatch_quant(p, s);
@@ -335,7 +338,8 @@ int moe_fused_debug_region(moe_fused_handle_t* hd, int region, size_t* offset, s
   const moe::WsLayout& L = hd->L;
   const size_t offs[moe::kNumRegions] = {L.status, L.counts, L.offsets, L.row_of, L.tk_of_row, L.active, L.x_q,
                                          L.x_scale, L.xs_q, L.xs_scale, L.hbuf, L.x2, L.s2, L.y2, L.slots,
-                                         L.row_token, L.shared_row, L.blk_ticket, L.tok_ticket, L.tok_expect};
+                                         L.row_token, L.shared_row, L.blk_ticket, L.tok_ticket, L.tok_expect,
+                                         L.ranges};
   if (region < 0 || region >= moe::kNumRegions) return MOE_ERR_INVALID_ARG;
   *offset = offs[region];
   *bytes = L.sizes[region];
@@ -350,7 +354,7 @@ int moe_fused_debug_gemm_acc(moe_fused_handle_t* hd, const moe_fused_args_t* arg
   if ((which != 1 && which != 2) || !acc) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int mode = which == 1 ? moe::kGemm1Raw : moe::kGemm2Raw;
-  return cuda_fail(moe::launch_moe_gemm(p, mode, acc, hd->num_sms, s));
+  return cuda_fail(moe::launch_moe_gemm(p, mode, acc, p.num_ctas, s));
 }
 
 }  // extern "C"

@@ -164,8 +164,8 @@ __device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
   int32_t* s_exp = b_blk + st;
   int32_t* s_row0 = s_exp + st;
   int32_t* s_rows = s_row0 + st;
-  const int is_small = (tid < E) && (c > 0) && (c <= kSmallRows);
-  const int is_big = (tid < E) && (c > kSmallRows);
+  const int is_small = (tid < E) && (c > 0) && (c <= p.small_rows);
+  const int is_big = (tid < E) && (c > p.small_rows);
   const int nblk = is_big ? (c + kTokenBlock - 1) / kTokenBlock : 0;
   int n_small = 0, n_big = 0, big_blk = 0;
   const int si = block_exclusive_scan(is_small, &n_small, s_warp);
@@ -184,12 +184,12 @@ __device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
   }
   if (tid == 0) {
     const int shared_rows = p.has_shared ? S : 0;
-    if (shared_rows > 0 && shared_rows <= kSmallRows) {
+    if (shared_rows > 0 && shared_rows <= p.small_rows) {
       s_exp[n_small] = -1;
       s_row0[n_small] = bs * K;
       s_rows[n_small] = shared_rows;
       n_small += 1;
-    } else if (shared_rows > kSmallRows) {
+    } else if (shared_rows > p.small_rows) {
       b_exp[n_big] = -1;
       b_row0[n_big] = bs * K;
       b_rows[n_big] = shared_rows;
@@ -211,6 +211,47 @@ __device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
     status[kStSlots] = n_small + n_big;
   }
   if (p.with_tickets) {
+    // Split of the small-phase items over the GEMM CTAs, by cost: an item of
+    // an expert with m rows streams the same weight bytes as any other but
+    // does m dot products per weight, so it counts 8 + m.  CTA b takes the
+    // items whose cumulative cost starts in [total*b/G, total*(b+1)/G).
+    __syncthreads();
+    const int ns = slots[SlotTable::kNumSmall];  // written by thread 0 above
+    int32_t* wp = dsm;       // exclusive prefix of (8 + m) over the small slots; [ns + 1]
+    int carry = 0;
+    for (int base = 0; base <= ns; base += kDispatchThreads) {
+      const int i = base + tid;
+      const int cost = (i < ns) ? 8 + s_rows[i] : 0;
+      int tot = 0;
+      const int ex = block_exclusive_scan(cost, &tot, s_warp);
+      if (i <= ns) wp[i] = carry + ex;
+      carry += tot;
+    }
+    __syncthreads();
+    const int G = p.num_ctas;
+    int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges);
+    for (int g = 0; g < 2; ++g) {
+      const long J = g == 0 ? p.I / 16 : p.h / 32;   // items per small slot, GEMM1 / GEMM2
+      const long total = J * wp[ns];
+      for (int b = tid; b <= G; b += kDispatchThreads) {
+        long it;
+        if (b == G || ns == 0) {
+          it = static_cast<long>(ns) * J;
+        } else {
+          const long target = total * b / G;
+          int lo = 0, hi = ns - 1;  // last slot whose first item starts at or before target
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (J * wp[mid] <= target) lo = mid;
+            else hi = mid - 1;
+          }
+          const long cost = wp[lo + 1] - wp[lo];
+          const long k = (target - J * wp[lo] + cost - 1) / cost;
+          it = lo * J + (k < J ? k : J);
+        }
+        ranges[g * (kMaxCtas + 1) + b] = static_cast<int32_t>(it);
+      }
+    }
     // per-forward epoch of the last-arriver counters used by the GEMM kernels
     int32_t* blk_ticket = ws_ptr<int32_t>(p, p.L.blk_ticket);
     const int nt = static_cast<int>(p.L.sizes[kRegBlkTicket] / 4);
@@ -437,6 +478,7 @@ int dispatch_noalloc(const int32_t* expert_ids, const uint8_t* mask, int bs, int
   p.topk = topk;
   p.has_shared = 0;
   p.with_tickets = 0;
+  p.small_rows = kSmallRows;
   p.ids = expert_ids;
   p.mask = mask;
   p.token_nums = expert_token_nums;

@@ -19,9 +19,10 @@
 //   small phase: experts with <= kSmallRows rows (decode).  The weights are
 //     read once from HBM and used for M <= 8 multiply-adds each, so the work
 //     is a batch of matrix-vector products: dp4a on exactly M rows, fed by
-//     2 KiB-per-row bulk copies (one producer warp, a 2-stage mbarrier
+//     2 KiB-per-row bulk copies (one producer warp, a 3-stage mbarrier
 //     full/empty ring -- the FIFO of the Mega-MoE analysis §4), items of 32
-//     weight rows, each CTA one contiguous run of items.
+//     weight rows, each CTA one contiguous run of items; the token rows of a
+//     run of items on one expert are loaded once and stay resident.
 //   big phase: the other experts in blocks of 64 rows, mma.sync s8 m16n8k32
 //     with the weights as the M operand ("swap AB"), 128 weight rows per item,
 //     3-stage ring of 256-byte chunks with padded rows for ldmatrix.
@@ -142,7 +143,7 @@ __device__ void gemm1_item_done(const FwdParams& p, int blk, int tiles, int done
 
 // GEMM2: each routed row of the item adds the columns it completed to its
 // token's counter; tokens that reach rows * h are combined by this CTA.
-// s_tok: kConsumers ints of scratch.
+// s_tok: at least m ints of scratch.
 __device__ void gemm2_item_done(const FwdParams& p, bool routed, int m, const int32_t* tok_of, int cols,
                                 int* s_tok, int ctid) {
   if (ctid < m) {
@@ -170,19 +171,20 @@ namespace small_path {
 constexpr int BN = 32;                 // weight rows per item
 constexpr int MT = kSmallRows;         // token rows per item (<= 8)
 constexpr int KC = 2048;               // K bytes per stage (one bulk copy per row)
-constexpr int STAGES = 2;
-constexpr int kInfoSlots = 8;          // > STAGES: per-item token info ring
+constexpr int STAGES = 3;
+constexpr int kMaxK = kSmallMaxK;      // token rows of a run stay resident: MT x K bytes
+constexpr int kInfoSlots = 6;          // > STAGES: per-item token info ring
 constexpr int kSlotCache = 16;         // small-slot table entries a CTA can touch
 constexpr int kRowsPerWarp = BN / kConsumerWarps;  // 4
 
-constexpr int OFF_W = 0;
-constexpr int OFF_T = OFF_W + STAGES * BN * KC;
-constexpr int OFF_Y = OFF_T + STAGES * MT * KC;                 // 2 x [BN][MT] fp32
-constexpr int OFF_BAR = OFF_Y + 2 * BN * MT * 4;
-constexpr int OFF_INFO = OFF_BAR + 2 * STAGES * 8;              // kInfoSlots x {scale, row, token}[MT]
+constexpr int OFF_W = 0;                                        // STAGES x [BN][KC] weights
+constexpr int OFF_T = OFF_W + STAGES * BN * KC;                 // [m][K] token rows of the current run
+constexpr int OFF_Y = OFF_T + MT * kMaxK;                       // 2 x [BN][MT] fp32
+constexpr int OFF_BAR = OFF_Y + 2 * BN * MT * 4;                // full, empty [STAGES]; tok_full, tok_empty
+constexpr int OFF_INFO = OFF_BAR + (2 * STAGES + 2) * 8;        // kInfoSlots x {scale, row, token}[MT]
 constexpr int OFF_SLOT = OFF_INFO + kInfoSlots * 3 * MT * 4;    // kSlotCache x {e, row0, rows}
-constexpr int OFF_MISC = OFF_SLOT + kSlotCache * 3 * 4;         // abort, flag, red[8], tok[256]
-constexpr int SMEM_BYTES = OFF_MISC + (2 + kConsumerWarps + kConsumers) * 4;
+constexpr int OFF_MISC = OFF_SLOT + kSlotCache * 3 * 4;         // abort, flag, red[8], tok[MT]
+constexpr int SMEM_BYTES = OFF_MISC + (2 + kConsumerWarps + MT) * 4;
 static_assert(kRowsPerWarp * MT == 32, "one reduced value per lane");
 static_assert(kInfoSlots > STAGES, "info ring must outlive the stage ring");
 
@@ -212,8 +214,8 @@ __device__ __forceinline__ int warp_reduce_scatter32(int (&v)[32], int lane) {
 // column slices.  M is a template argument so the loop body is straight-line
 // code with 4*M independent dp4a chains.
 template <int M, bool FULL>
-__device__ __forceinline__ void stage_dot(const char* __restrict__ Ws, const char* __restrict__ Ts, int bytes,
-                                          int lane, int (&acc)[kRowsPerWarp * MT]) {
+__device__ __forceinline__ void stage_dot(const char* __restrict__ Ws, const char* __restrict__ Ts, int tstride,
+                                          int bytes, int lane, int (&acc)[kRowsPerWarp * MT]) {
   constexpr int kSteps = KC / 512;
 #pragma unroll
   for (int i = 0; i < kSteps; ++i) {
@@ -221,7 +223,7 @@ __device__ __forceinline__ void stage_dot(const char* __restrict__ Ws, const cha
     if (!FULL && c >= bytes) break;
     uint4 tv[M];
 #pragma unroll
-    for (int t = 0; t < M; ++t) tv[t] = *reinterpret_cast<const uint4*>(Ts + t * KC + c);
+    for (int t = 0; t < M; ++t) tv[t] = *reinterpret_cast<const uint4*>(Ts + t * tstride + c);
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
       const uint4 wv = *reinterpret_cast<const uint4*>(Ws + rr * KC + c);
@@ -239,17 +241,17 @@ __device__ __forceinline__ void stage_dot(const char* __restrict__ Ws, const cha
 }
 
 template <bool FULL>
-__device__ __forceinline__ void stage_dot_m(int m, const char* Ws, const char* Ts, int bytes, int lane,
+__device__ __forceinline__ void stage_dot_m(int m, const char* Ws, const char* Ts, int tstride, int bytes, int lane,
                                             int (&acc)[kRowsPerWarp * MT]) {
   switch (m) {
-    case 1: stage_dot<1, FULL>(Ws, Ts, bytes, lane, acc); break;
-    case 2: stage_dot<2, FULL>(Ws, Ts, bytes, lane, acc); break;
-    case 3: stage_dot<3, FULL>(Ws, Ts, bytes, lane, acc); break;
-    case 4: stage_dot<4, FULL>(Ws, Ts, bytes, lane, acc); break;
-    case 5: stage_dot<5, FULL>(Ws, Ts, bytes, lane, acc); break;
-    case 6: stage_dot<6, FULL>(Ws, Ts, bytes, lane, acc); break;
-    case 7: stage_dot<7, FULL>(Ws, Ts, bytes, lane, acc); break;
-    default: stage_dot<MT, FULL>(Ws, Ts, bytes, lane, acc); break;
+    case 1: stage_dot<1, FULL>(Ws, Ts, tstride, bytes, lane, acc); break;
+    case 2: stage_dot<2, FULL>(Ws, Ts, tstride, bytes, lane, acc); break;
+    case 3: stage_dot<3, FULL>(Ws, Ts, tstride, bytes, lane, acc); break;
+    case 4: stage_dot<4, FULL>(Ws, Ts, tstride, bytes, lane, acc); break;
+    case 5: stage_dot<5, FULL>(Ws, Ts, tstride, bytes, lane, acc); break;
+    case 6: stage_dot<6, FULL>(Ws, Ts, tstride, bytes, lane, acc); break;
+    case 7: stage_dot<7, FULL>(Ws, Ts, tstride, bytes, lane, acc); break;
+    default: stage_dot<MT, FULL>(Ws, Ts, tstride, bytes, lane, acc); break;
   }
 }
 
@@ -263,6 +265,8 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
   constexpr bool RAW = (MODE == kGemm1Raw || MODE == kGemm2Raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* empty = full + STAGES;
+  uint64_t* tok_full = empty + STAGES;
+  uint64_t* tok_empty = tok_full + 1;
   float* info_scale = reinterpret_cast<float*>(smem + OFF_INFO);                 // [slot][MT]
   int32_t* info_row = reinterpret_cast<int32_t*>(smem + OFF_INFO) + kInfoSlots * MT;
   int32_t* info_tok = info_row + kInfoSlots * MT;
@@ -282,11 +286,11 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
   const int32_t* sm_exp = slots + SlotTable::kHeader + 4 * st;
   const int32_t* sm_row0 = sm_exp + st;
   const int32_t* sm_rows = sm_row0 + st;
-  const long total = static_cast<long>(slots[SlotTable::kNumSmall]) * J;
-  // contiguous run of items for this CTA: consecutive tiles of the same expert
-  // are contiguous in memory
-  const long it_begin = total * blockIdx.x / gridDim.x;
-  const long it_end = total * (blockIdx.x + 1) / gridDim.x;
+  // contiguous run of items for this CTA (consecutive tiles of one expert are
+  // contiguous in memory), split by cost in the dispatch kernel
+  const int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges) + (G1 ? 0 : kMaxCtas + 1);
+  const long it_begin = ranges[blockIdx.x];
+  const long it_end = ranges[blockIdx.x + 1];
   const int slot_first = static_cast<int>(it_begin / J);
   const int n_cached = it_end > it_begin ? static_cast<int>((it_end - 1) / J) - slot_first + 1 : 0;
   const int site = (G1 ? kKGemm1 : kKGemm2) * 16;
@@ -296,6 +300,8 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
+    mbar_init(tok_full, 1);
+    mbar_init(tok_empty, kConsumerWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -351,25 +357,32 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       nx = item_at(it_begin);
       load_info(nx, nx_tok, nx_scale);
     }
-    int stage_it = 0, item_no = 0;
+    int stage_it = 0, item_no = 0, run_slot = -1, run_no = 0;
     for (long it = it_begin; it < it_end; ++it, ++item_no) {
       const SmallItem cur = nx;
       const int cur_tok = nx_tok;
       const float cur_scale = nx_scale;
-      if (it + 1 < it_end) {
-        nx = item_at(it + 1);
-        load_info(nx, nx_tok, nx_scale);
-      }
       const int8_t* wbase = G1 ? (cur.e >= 0 ? p.w1 + static_cast<size_t>(cur.e) * NW * K : p.sw1)
                                : (cur.e >= 0 ? p.w2 + static_cast<size_t>(cur.e) * NW * K : p.sw2);
       int n;
       if (G1) n = (lane < BN / 2) ? cur.jt * (BN / 2) + lane : p.I + cur.jt * (BN / 2) + (lane - BN / 2);
       else n = cur.jt * BN + lane;
       const int8_t* wrow = wbase + static_cast<size_t>(n) * K;
-      const int8_t* trow = nullptr;
-      if (lane < cur.m) {
-        if (G1) trow = (cur.e >= 0 ? xq : xsq) + static_cast<size_t>(cur_tok) * p.h;
-        else trow = x2 + static_cast<size_t>(cur.row0 + lane) * p.I;
+      if (cur.slot != run_slot) {
+        // a new run of items on one expert: load its token rows (whole K) once,
+        // after the consumers are done with the previous run's rows
+        if (run_no > 0) {
+          if (!mbar_wait_bounded(tok_empty, (run_no - 1) & 1, abort_flag, status, site + 3, false)) return;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(tok_full, static_cast<uint32_t>(cur.m * K));
+        __syncwarp();
+        if (lane < cur.m) {
+          const int8_t* trow = G1 ? (cur.e >= 0 ? xq : xsq) + static_cast<size_t>(cur_tok) * p.h
+                                  : x2 + static_cast<size_t>(cur.row0 + lane) * p.I;
+          bulk_g2s(smem + OFF_T + lane * K, trow, static_cast<uint32_t>(K), tok_full, pol_t);
+        }
+        run_slot = cur.slot;
+        ++run_no;
       }
       for (int kc = 0; kc < n_kc; ++kc, ++stage_it) {
         const int s = stage_it % STAGES;
@@ -387,10 +400,14 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
         const int k0 = kc * KC;
         const int bytes = min(KC, K - k0);
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>((BN + cur.m) * bytes));
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(BN * bytes));
         __syncwarp();
         bulk_g2s(smem + OFF_W + (s * BN + lane) * KC, wrow + k0, bytes, &full[s], pol_w);
-        if (trow) bulk_g2s(smem + OFF_T + (s * MT + lane) * KC, trow + k0, bytes, &full[s], pol_t);
+      }
+      // next item's token info: its dependent loads run while this item's copies fly
+      if (it + 1 < it_end) {
+        nx = item_at(it + 1);
+        load_info(nx, nx_tok, nx_scale);
       }
     }
     return;
@@ -400,11 +417,18 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
   const int ctid = threadIdx.x;
   float* hbuf = ws_ptr<float>(p, p.L.hbuf);
   uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
-  int stage_it = 0, item_no = 0, run_items = 0;
+  int stage_it = 0, item_no = 0, run_items = 0, run_slot = -1, run_no = 0;
+  bool tok_ok = true;
   for (long it = it_begin; it < it_end; ++it, ++item_no) {
     const SmallItem cur = item_at(it);
     const int m = cur.m, jt = cur.jt;
     const int is = item_no % kInfoSlots;
+    const bool run_end = (it + 1 == it_end) || ((it + 1) / J != cur.slot);
+    if (cur.slot != run_slot) {
+      tok_ok = mbar_wait_bounded(tok_full, run_no & 1, abort_flag, status, site + 4);
+      run_slot = cur.slot;
+      ++run_no;
+    }
     float* ytile = reinterpret_cast<float*>(smem + OFF_Y) + (item_no & 1) * BN * MT;  // [BN][MT]
 
     int acc[kRowsPerWarp * MT];
@@ -415,16 +439,17 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       const int s = stage_it % STAGES;
       const int round = stage_it / STAGES;
       const bool ok = mbar_wait_bounded(&full[s], round & 1, abort_flag, status, site + 2);
-      if (ok) {
+      if (ok && tok_ok) {
         const int bytes = min(KC, K - kc * KC);
         const char* Ws = smem + OFF_W + (s * BN + kRowsPerWarp * warp) * KC;
-        const char* Ts = smem + OFF_T + s * MT * KC;
-        if (bytes == KC) stage_dot_m<true>(m, Ws, Ts, bytes, lane, acc);
-        else stage_dot_m<false>(m, Ws, Ts, bytes, lane, acc);
+        const char* Ts = smem + OFF_T + kc * KC;
+        if (bytes == KC) stage_dot_m<true>(m, Ws, Ts, K, bytes, lane, acc);
+        else stage_dot_m<false>(m, Ws, Ts, K, bytes, lane, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
+    if (run_end && lane == 0) mbar_arrive(tok_empty);  // this run's token rows are no longer read
 
     // lane (rr * MT + t) receives the dot product of row rr of this warp with token t
     const int mine = warp_reduce_scatter32(acc, lane);
@@ -466,7 +491,7 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       }
       // report once per run of this CTA's items on one expert
       ++run_items;
-      if (it + 1 == it_end || (it + 1) / J != cur.slot) {
+      if (run_end) {
         __threadfence();
         consumer_sync();
         if (G1) gemm1_item_done(p, cur.slot, J, run_items, cur.row0, m, s_flag, s_red, ctid);
@@ -480,7 +505,7 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
 
 __device__ void inval_barriers(char* smem) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  for (int s = 0; s < 2 * STAGES; ++s) mbar_inval(full + s);
+  for (int s = 0; s < 2 * STAGES + 2; ++s) mbar_inval(full + s);
 }
 
 }  // namespace small_path

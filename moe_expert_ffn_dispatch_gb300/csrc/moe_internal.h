@@ -44,6 +44,7 @@ struct WsLayout {
   size_t blk_ticket; // int32 per row block: GEMM1 tiles done (last one requantises)
   size_t tok_ticket; // [bs_max] int32: GEMM2 output columns done per token
   size_t tok_expect; // [bs_max] int32: columns that complete a token (rows * h)
+  size_t ranges;     // [2][kMaxCtas + 1] int32: small-phase item range of each CTA (GEMM1, GEMM2)
   size_t total;
   size_t sizes[24];  // bytes per region id (debug_region)
 };
@@ -52,8 +53,10 @@ struct WsLayout {
 enum Region : int {
   kRegStatus = 0, kRegCounts, kRegOffsets, kRegRowOf, kRegTkOfRow, kRegActive, kRegXq, kRegXScale,
   kRegXsq, kRegXsScale, kRegH, kRegX2, kRegS2, kRegY2, kRegSlots, kRegRowToken, kRegSharedRow,
-  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kNumRegions
+  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kRegRanges, kNumRegions
 };
+
+constexpr int kMaxCtas = 1023;  // persistent grid size limit (one CTA per SM)
 
 // Slot table: the experts that received rows, split by row count.  Experts
 // with at most kSmallRows rows ("small", decode-like) go to the weight-
@@ -73,7 +76,8 @@ struct SlotTable {
   static __host__ __device__ int words(int E) { return kHeader + 7 * stride(E); }
 };
 
-constexpr int kSmallRows = 8;   // experts with <= this many rows take the dp4a path
+constexpr int kSmallRows = 8;     // experts with <= this many rows take the dp4a path ...
+constexpr int kSmallMaxK = 4096;  // ... when both contraction lengths are at most this
 constexpr int kTokenBlock = 64;  // token rows per GEMM work item
 
 // ---------------------------------------------------------------- params
@@ -81,6 +85,8 @@ struct FwdParams {
   int32_t bs, h, E, topk, I, has_shared;
   int32_t share_uses_xq;  // shared quant identical to routed quant (same smooth vector)
   int32_t with_tickets;   // dispatch resets the GEMM epilogue counters (forward path)
+  int32_t small_rows;     // row count up to which an expert takes the dp4a path (0: never)
+  int32_t num_ctas;       // grid of the GEMM launches (<= kMaxCtas)
   const uint16_t* x;
   const int32_t* ids;
   const float* scales;
