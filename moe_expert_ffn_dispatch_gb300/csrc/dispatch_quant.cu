@@ -369,6 +369,9 @@ __device__ void quant_token(const FwdParams& p, int t, float* s_red, int group) 
 __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(FwdParams p) {
   extern __shared__ int32_t dsm[];
   __shared__ float s_red[kQuantGroups][8];
+  // the previous forward's GEMM2 may still read the workspace and write outputs
+  grid_dependency_wait();
+  grid_launch_dependents();
   if (blockIdx.x == 0) {
     dispatch_block(p, dsm);
     return;
@@ -384,8 +387,9 @@ size_t dispatch_smem_bytes(int E) { return sizeof(int32_t) * static_cast<size_t>
 
 cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s) {
   const int blocks = 1 + (p.bs + kQuantGroups - 1) / kQuantGroups;
-  dispatch_quant_kernel<<<blocks, kDispatchThreads, dispatch_smem_bytes(p.E), s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(blocks), dim3(kDispatchThreads), dispatch_smem_bytes(p.E), s, attr);
+  return cudaLaunchKernelEx(&cfg, dispatch_quant_kernel, p);
 }
 
 cudaError_t dispatch_prepare_attributes(int E) {

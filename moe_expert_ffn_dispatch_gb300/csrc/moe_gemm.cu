@@ -821,6 +821,9 @@ static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(FwdParams p, int32_t* raw) {
   extern __shared__ __align__(128) char smem[];
+  // everything below reads what the preceding kernel wrote
+  grid_dependency_wait();
+  grid_launch_dependents();
   small_path::run<MODE>(p, raw, smem);
   __syncthreads();
   if (threadIdx.x == 0) small_path::inval_barriers(smem);
@@ -844,14 +847,15 @@ cudaError_t moe_gemm_prepare_attributes() {
 
 cudaError_t launch_moe_gemm(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(num_ctas), dim3(kThreads), SMEM_BYTES, s, attr);
   switch (mode) {
-    case kGemm1SwiGLU: moe_gemm_kernel<kGemm1SwiGLU><<<num_ctas, kThreads, SMEM_BYTES, s>>>(p, raw_acc); break;
-    case kGemm2Bf16: moe_gemm_kernel<kGemm2Bf16><<<num_ctas, kThreads, SMEM_BYTES, s>>>(p, raw_acc); break;
-    case kGemm1Raw: moe_gemm_kernel<kGemm1Raw><<<num_ctas, kThreads, SMEM_BYTES, s>>>(p, raw_acc); break;
-    case kGemm2Raw: moe_gemm_kernel<kGemm2Raw><<<num_ctas, kThreads, SMEM_BYTES, s>>>(p, raw_acc); break;
+    case kGemm1SwiGLU: return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<kGemm1SwiGLU>, p, raw_acc);
+    case kGemm2Bf16: return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<kGemm2Bf16>, p, raw_acc);
+    case kGemm1Raw: return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<kGemm1Raw>, p, raw_acc);
+    case kGemm2Raw: return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<kGemm2Raw>, p, raw_acc);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -119,6 +119,21 @@ enum KernelId : int { kKDispatchQuant = 0, kKGemm1 = 1, kKGemm2 = 2, kNumKernels
 // GEMM modes
 enum GemmMode : int { kGemm1SwiGLU = 0, kGemm2Bf16 = 1, kGemm1Raw = 2, kGemm2Raw = 3 };
 
+// Launch attributes shared by the forward's kernels: programmatic stream
+// serialisation (each kernel waits on its predecessor in-kernel).
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 // ---------------------------------------------------------------- launches
 size_t dispatch_smem_bytes(int E);
 cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s);
