@@ -61,7 +61,7 @@ def kernel_sha(kernel: str) -> str:
     """Hash of the kernel's source file and the headers it includes."""
     csrc = os.path.join(ROOT, "moe_expert_ffn_dispatch_gb300", "csrc")
     hsh = hashlib.sha256()
-    for name in (KERNEL_SOURCES[kernel], "device_prims.cuh", "moe_internal.h"):
+    for name in (KERNEL_SOURCES[kernel], "device_prims.cuh", "epilogue_ops.cuh", "moe_internal.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             hsh.update(f.read())
     return hsh.hexdigest()[:16]
@@ -132,6 +132,9 @@ class ClockSampler:
                 "reasons": rs, "samples": len(sm)}
 
 
+SMALL_ROWS = 8  # experts with at most this many rows run in the weight-streaming kernels
+
+
 def algorithmic_bytes(wl, counts_per_expert, n_active):
     """Bytes each kernel must move at least once (the roofline numerator).
 
@@ -141,19 +144,24 @@ def algorithmic_bytes(wl, counts_per_expert, n_active):
     requant reads h back and writes x2 (I) and s2.  GEMM2 reads W2 (h*I int8)
     and scales (h fp32); per row x2 and s2 in, a bf16 row of h out, and the
     fused combine reads each routed row once more and writes bf16 outputs.
-    The step total counts weights once plus the block's own inputs and
-    outputs (scratch a fully fused kernel could keep on chip is not counted)."""
+    Experts with at most SMALL_ROWS rows (when h, I <= 4096) run in the *_small
+    kernels, the others in the tensor-core *_big kernels.  The step total
+    counts weights once plus the block's own inputs and outputs."""
     h, I, K, bs = wl.hidden, wl.inter, wl.topk, wl.bs
-    groups = [c for c in counts_per_expert if c > 0]
+    small_ok = h <= 4096 and I <= 4096
+    groups = [(c, True) for c in counts_per_expert if c > 0]
     R = sum(counts_per_expert)
     shared = n_active if (wl.has_shared and n_active > 0) else 0
     if shared:
-        groups.append(shared)
+        groups.append((shared, False))
+    out = {"gemm1_small": 0, "gemm1_big": 0, "gemm2_small": 0, "gemm2_big": 0}
+    for m, routed in groups:
+        sfx = "small" if (small_ok and m <= SMALL_ROWS) else "big"
+        out["gemm1_" + sfx] += 2 * I * h + 8 * I + m * (h + 4 * I + 4 * I + I + 4)
+        out["gemm2_" + sfx] += h * I + 4 * h + m * (I + 4 + 2 * h) + (m * 2 * h if routed else 0)
+    out["gemm2_small" if small_ok else "gemm2_big"] += bs * 2 * h  # combined outputs
     touched = len(groups)
-    rows = sum(groups)
-    out = {}
-    out["gemm1_swiglu_requant"] = touched * (2 * I * h + 8 * I) + rows * (h + 4 * I + 4 * I + I + 4)
-    out["gemm2_combine"] = touched * (h * I + 4 * h) + rows * (I + 4 + 2 * h) + R * 2 * h + bs * 2 * h
+    rows = sum(m for m, _ in groups)
     out["step"] = touched * (2 * I * h + h * I + 4 * (2 * I + h)) + bs * h * 2 + bs * K * 8 + \
         bs * h * 2 * (2 if wl.has_shared else 1) + wl.num_experts * 4
     out["int_ops"] = 2 * rows * (2 * I * h + h * I)
@@ -162,7 +170,8 @@ def algorithmic_bytes(wl, counts_per_expert, n_active):
     return out
 
 
-KERNEL_SOURCES = {"gemm1_swiglu_requant": "moe_gemm.cu", "gemm2_combine": "moe_gemm.cu"}
+KERNEL_SOURCES = {"gemm1_small": "moe_gemm.cu", "gemm2_small": "moe_gemm.cu",
+                  "gemm1_big": "tc_gemm.cu", "gemm2_big": "tc_gemm.cu"}
 
 
 # ---------------------------------------------------------------- our arm

@@ -185,8 +185,11 @@ int moe_fused_dispatch_noalloc(const int32_t* expert_ids, const uint8_t* x_activ
  * `stream`.  get_timing synchronises the recorded events, writes for each
  * kernel id k < max_kernels the summed milliseconds ms[k] and launch count
  * launches[k] (host arrays), returns the number of kernel ids, and clears the
- * record.  Kernel ids: 0 dispatch + quant, 1 GEMM1 + SwiGLU + requant,
- * 2 GEMM2 + bf16 dequant + combine. */
+ * record.  Kernel ids: 0 dispatch + quant, 1 expand (f16 token rows for the
+ * tensor-core GEMMs), 2 GEMM1 + SwiGLU (+ requant) for experts with at most
+ * 8 rows (dp4a weight streaming), 3 GEMM1 + SwiGLU for the other experts
+ * (tcgen05), 4 requant of their rows, 5 GEMM2 + dequant (+ combine when every
+ * expert has at most 8 rows), 6 GEMM2 + dequant (tcgen05), 7 combine. */
 int moe_fused_set_timing(moe_fused_handle_t* handle, int enable);
 int moe_fused_get_timing(moe_fused_handle_t* handle, float* ms, int32_t* launches, int max_kernels);
 const char* moe_fused_kernel_name(int kernel_id);
@@ -201,6 +204,7 @@ const char* moe_fused_kernel_name(int kernel_id);
  *   13 y2 [bs_max*topk,h] bf16 (aliases region 10)  14 slot table
  *   15 row_token [rows] int32  16 shared_row [bs_max] int32
  *   17 row-block counters  18 token counters [bs_max]  19 token totals [bs_max]
+ *   20 small-expert item ranges  21 x1h [rows,h] f16  22 x2h [rows,inter] f16
  * `rows` = bs*topk + bs: routed row r at index r (r < R), the shared expert's
  * i-th active token at index bs*topk + i.  Writes *offset and *bytes. */
 int moe_fused_debug_region(moe_fused_handle_t* handle, int region, size_t* offset, size_t* bytes);

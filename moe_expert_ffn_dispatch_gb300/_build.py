@@ -15,8 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 SO = os.path.join(HERE, "_moe_fused.so")
-SOURCES = ["api.cu", "dispatch_quant.cu", "moe_gemm.cu"]
-HEADERS = ["device_prims.cuh", "moe_internal.h"]
+SOURCES = ["api.cu", "dispatch_quant.cu", "moe_gemm.cu", "tc_gemm.cu"]
+HEADERS = ["device_prims.cuh", "epilogue_ops.cuh", "moe_internal.h"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

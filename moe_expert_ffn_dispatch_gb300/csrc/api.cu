@@ -3,14 +3,18 @@
 //
 // Launch sequence of one forward (Process() of the FusedDeepMoE analysis
 // §3.2: dispatch, GMM1 with SwiGLU + quant, GMM2 with combine):
-//   dispatch + quant -> GEMM1 + SwiGLU + requant -> GEMM2 + bf16 dequant +
-//   combine.
+//   dispatch + quant -> expand (f16 token rows of big blocks) ->
+//   GEMM1 + SwiGLU (+ requant, small experts) -> GEMM1 + SwiGLU (big) ->
+//   requant of big blocks -> GEMM2 + bf16 dequant (+ combine when no big
+//   blocks) -> GEMM2 (big) -> combine (when big blocks exist).
 // Kernel boundaries carry the dependencies; inside a GEMM launch the fused
 // epilogues run in the CTA that finishes a block last.  No CTA waits.
 #include <cstdio>
 #include <cstring>
 #include <new>
 #include <vector>
+
+#include <cuda.h>
 
 #include "moe_fused.h"
 #include "moe_internal.h"
@@ -28,6 +32,9 @@ struct moe_fused_handle {
   bool timing;
   std::vector<TimingRecord> records;
   std::vector<cudaEvent_t> pool;
+  moe::TcMaps maps;          // tensor maps of the last forward's operands
+  const void* map_key[5];    // pointers they were built for
+  bool maps_valid;
 };
 
 namespace {
@@ -84,6 +91,8 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
   take(L.tok_ticket, bs * 4, moe::kRegTokTicket);
   take(L.tok_expect, bs * 4, moe::kRegTokExpect);
   take(L.ranges, 2 * (moe::kMaxCtas + 1) * 4, moe::kRegRanges);
+  take(L.x1h, rows * h * 2, moe::kRegX1h);
+  take(L.x2h, rows * I * 2, moe::kRegX2h);
   L.total = off;
   return L;
 }
@@ -177,6 +186,67 @@ cudaError_t timed(moe_fused_handle* hd, int kernel, cudaStream_t s, F fn) {
   return cudaSuccess;
 }
 
+// ---- TMA descriptors for the tensor-core path -----------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// 2-D row-major [rows][cols] tensor, box {box_cols, box_rows}
+bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, size_t elem, uint64_t rows, uint64_t cols,
+               uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * elem};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Build (or reuse) the tensor maps of this forward's operands.
+int prepare_maps(moe_fused_handle* hd, const moe::FwdParams& p) {
+  const void* key[5] = {p.w1, p.w2, p.sw1, p.sw2, p.ws};
+  if (hd->maps_valid && std::memcmp(key, hd->map_key, sizeof(key)) == 0) return MOE_OK;
+  const moe_fused_config_t& c = hd->cfg;
+  const uint64_t E = c.num_experts, h = c.hidden, I = c.inter;
+  const uint64_t rows = static_cast<uint64_t>(c.bs_max) * c.topk + (c.has_shared ? c.bs_max : 0);
+  const uint64_t brows = rows > 0 ? rows : 1;
+  const void* sw1 = p.sw1 ? p.sw1 : p.w1;
+  const void* sw2 = p.sw2 ? p.sw2 : p.w2;
+  moe::TcMaps& m = hd->maps;
+  bool ok = encode_2d(&m.a1, p.w1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, E * 2 * I, h, 64, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            encode_2d(&m.a1s, sw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 2 * I, h, 64, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            encode_2d(&m.a2, p.w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, E * h, I, 64, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            encode_2d(&m.a2s, sw2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, h, I, 64, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            encode_2d(&m.b1, p.ws + p.L.x1h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, brows, h, 64, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_2d(&m.b2, p.ws + p.L.x2h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, brows, I, 64, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) {
+    hd->maps_valid = false;
+    return MOE_ERR_CUDA;
+  }
+  std::memcpy(hd->map_key, key, sizeof(key));
+  hd->maps_valid = true;
+  return MOE_OK;
+}
+
 int cuda_fail(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
   std::fprintf(stderr, "moe_fused: CUDA error %s\n", cudaGetErrorString(e));
@@ -204,9 +274,11 @@ int moe_fused_create(const moe_fused_config_t* cfg, moe_fused_handle_t** out_han
   if (!hd) return MOE_ERR_INVALID_ARG;
   hd->cfg = *cfg;
   hd->timing = false;
+  hd->maps_valid = false;
   cudaError_t e = cudaGetDevice(&hd->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&hd->num_sms, cudaDevAttrMultiProcessorCount, hd->device);
-  if (e == cudaSuccess) e = moe::moe_gemm_prepare_attributes();
+  if (e == cudaSuccess) e = moe::moe_gemm_small_prepare_attributes();
+  if (e == cudaSuccess) e = moe::moe_gemm_big_prepare_attributes();
   if (e == cudaSuccess) e = moe::dispatch_prepare_attributes(1024);
   if (e != cudaSuccess) {
     delete hd;
@@ -236,12 +308,20 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
     if (e == cudaSuccess) e = cudaMemsetAsync(p.ws + p.L.status, 0, 64 * sizeof(int32_t), s);
     return cuda_fail(e);
   }
+  rc = prepare_maps(hd, p);
+  if (rc) return rc;
   const int sms = p.num_ctas;
+  const moe::TcMaps& maps = hd->maps;
   auto run = [&](int k) -> cudaError_t {
     switch (k) {
       case moe::kKDispatchQuant: return moe::launch_dispatch_quant(p, s);
-      case moe::kKGemm1: return moe::launch_moe_gemm(p, moe::kGemm1SwiGLU, nullptr, sms, s);
-      default: return moe::launch_moe_gemm(p, moe::kGemm2Bf16, nullptr, sms, s);
+      case moe::kKExpand: return moe::launch_expand(p, s);
+      case moe::kKGemm1Small: return moe::launch_moe_gemm_small(p, moe::kGemm1SwiGLU, nullptr, sms, s);
+      case moe::kKGemm1Big: return moe::launch_moe_gemm_big(p, maps, moe::kGemm1SwiGLU, nullptr, sms, s);
+      case moe::kKRequantBig: return moe::launch_requant_big(p, s);
+      case moe::kKGemm2Small: return moe::launch_moe_gemm_small(p, moe::kGemm2Bf16, nullptr, sms, s);
+      case moe::kKGemm2Big: return moe::launch_moe_gemm_big(p, maps, moe::kGemm2Bf16, nullptr, sms, s);
+      default: return moe::launch_combine(p, s);
     }
   };
   e = cudaSuccess;
@@ -323,7 +403,8 @@ int moe_fused_get_timing(moe_fused_handle_t* hd, float* ms, int32_t* launches, i
 }
 
 const char* moe_fused_kernel_name(int k) {
-  static const char* names[] = {"dispatch_quant", "gemm1_swiglu_requant", "gemm2_combine"};
+  static const char* names[] = {"dispatch_quant", "expand",      "gemm1_small", "gemm1_big",
+                                "requant_big",    "gemm2_small", "gemm2_big",   "combine"};
   return (k >= 0 && k < moe::kNumKernels) ? names[k] : "unknown";
 }
 
@@ -339,7 +420,7 @@ int moe_fused_debug_region(moe_fused_handle_t* hd, int region, size_t* offset, s
   const size_t offs[moe::kNumRegions] = {L.status, L.counts, L.offsets, L.row_of, L.tk_of_row, L.active, L.x_q,
                                          L.x_scale, L.xs_q, L.xs_scale, L.hbuf, L.x2, L.s2, L.y2, L.slots,
                                          L.row_token, L.shared_row, L.blk_ticket, L.tok_ticket, L.tok_expect,
-                                         L.ranges};
+                                         L.ranges, L.x1h, L.x2h};
   if (region < 0 || region >= moe::kNumRegions) return MOE_ERR_INVALID_ARG;
   *offset = offs[region];
   *bytes = L.sizes[region];
@@ -354,7 +435,11 @@ int moe_fused_debug_gemm_acc(moe_fused_handle_t* hd, const moe_fused_args_t* arg
   if ((which != 1 && which != 2) || !acc) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int mode = which == 1 ? moe::kGemm1Raw : moe::kGemm2Raw;
-  return cuda_fail(moe::launch_moe_gemm(p, mode, acc, p.num_ctas, s));
+  rc = prepare_maps(hd, p);
+  if (rc) return rc;
+  cudaError_t e = moe::launch_moe_gemm_small(p, mode, acc, p.num_ctas, s);
+  if (e == cudaSuccess) e = moe::launch_moe_gemm_big(p, hd->maps, mode, acc, p.num_ctas, s);
+  return cuda_fail(e);
 }
 
 }  // extern "C"

@@ -14,156 +14,29 @@
 //     output[t] = bf16(sum_k float(y2[row(t,k)]) * expert_scales[t, k]),
 //     fp32 sum from 0, k ascending, multiply and add rounded separately.
 //
-// One persistent launch per GEMM runs two phases over the slot table that
-// dispatch built:
-//   small phase: experts with <= kSmallRows rows (decode).  The weights are
+// This file holds the small-expert kernel; tc_gemm.cu the big-expert one.
+// Both walk the slot table that dispatch built:
+//   small experts: <= kSmallRows rows (decode).  The weights are
 //     read once from HBM and used for M <= 8 multiply-adds each, so the work
 //     is a batch of matrix-vector products: dp4a on exactly M rows, fed by
 //     2 KiB-per-row bulk copies (one producer warp, a 3-stage mbarrier
 //     full/empty ring -- the FIFO of the Mega-MoE analysis §4), items of 32
 //     weight rows, each CTA one contiguous run of items; the token rows of a
 //     run of items on one expert are loaded once and stay resident.
-//   big phase: the other experts in blocks of 64 rows, mma.sync s8 m16n8k32
-//     with the weights as the M operand ("swap AB"), 128 weight rows per item,
-//     3-stage ring of 256-byte chunks with padded rows for ldmatrix.
+//   big experts: blocks of up to 128 rows on the tcgen05 tensor cores
+//     (tc_gemm.cu).
 // The requant and the combine run in the CTA that completes the last tile of
 // a row block (GEMM1) or of a token (GEMM2): each such CTA fences its
 // writes and bumps a per-forward counter (reset by the dispatch kernel); the
 // one that brings a counter to its total does the work.  No CTA waits for
 // another.
 #include "device_prims.cuh"
+#include "epilogue_ops.cuh"
 #include "moe_internal.h"
 
 namespace moe {
 
 namespace {
-
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
-constexpr float kAmaxEps = 1e-4f;
-constexpr float kInv127 = 1.0f / 127.0f;  // the fp32 nearest to 1/127
-
-__device__ __forceinline__ void consumer_sync() { named_barrier_sync(1, kConsumers); }
-
-__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
-  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// ------------------------------------------------------------ epilogue ops
-// Requant of rows [r0, r0 + n) of h into x2 / s2, by the consumer threads.
-// h was written by other CTAs in this launch: read it through L2 (ld.cg).
-__device__ void requant_rows(const FwdParams& p, int r0, int n, float* s_red, int ctid) {
-  const int I = p.I, n4 = I >> 2;
-  const float* hbuf = ws_ptr<float>(p, p.L.hbuf);
-  int8_t* x2 = ws_ptr<int8_t>(p, p.L.x2);
-  float* s2 = ws_ptr<float>(p, p.L.s2);
-  const int lane = ctid & 31, warp = ctid >> 5;
-  for (int i = 0; i < n; ++i) {
-    const int r = r0 + i;
-    const float4* hr = reinterpret_cast<const float4*>(hbuf + static_cast<size_t>(r) * I);
-    float amax = 0.0f;
-    for (int c = ctid; c < n4; c += kConsumers) {
-      const float4 v = __ldcg(hr + c);
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0) s_red[warp] = amax;
-    consumer_sync();
-    amax = s_red[0];
-#pragma unroll
-    for (int w = 1; w < kConsumerWarps; ++w) amax = fmaxf(amax, s_red[w]);
-    consumer_sync();
-    if (amax < kAmaxEps) amax = kAmaxEps;
-    const float inv = __fdiv_rn(1.0f, amax);
-    uint32_t* q4 = reinterpret_cast<uint32_t*>(x2 + static_cast<size_t>(r) * I);
-    for (int c = ctid; c < n4; c += kConsumers) {
-      const float4 v = __ldcg(hr + c);
-      const float f[4] = {v.x, v.y, v.z, v.w};
-      uint32_t packed = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t b = static_cast<uint8_t>(f32_to_q(__fmul_rn(__fmul_rn(f[j], 127.0f), inv)));
-        packed |= b << (8 * j);
-      }
-      q4[c] = packed;
-    }
-    if (ctid == 0) s2[r] = __fmul_rn(amax, kInv127);
-  }
-}
-
-// Combine of token t, by the consumer threads (y2 through L2).
-__device__ void combine_token(const FwdParams& p, int t, int ctid) {
-  const int h = p.h, K = p.topk, n8 = h >> 3;
-  const int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
-  const uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
-  uint4* out = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * h);
-  for (int i = ctid; i < n8; i += kConsumers) {
-    float acc[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int k = 0; k < K; ++k) {
-      const int r = row_of[t * K + k];
-      if (r < 0) continue;
-      const float sc = p.scales[t * K + k];
-      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(y2 + static_cast<size_t>(r) * h) + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float f = bf16_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
-        acc[j] = __fadd_rn(acc[j], __fmul_rn(f, sc));
-      }
-    }
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      o[j] = static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * j])) |
-             (static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * j + 1])) << 16);
-    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
-
-// After a CTA's outputs for a row block are written (every writer fenced,
-// then a consumer barrier): GEMM1 adds the tiles it finished to the block's
-// counter; the CTA that completes the block requantises its rows.
-// `done` tiles of the block were finished by this CTA since its last report.
-__device__ void gemm1_item_done(const FwdParams& p, int blk, int tiles, int done, int r0, int n, int* s_flag,
-                                float* s_red, int ctid) {
-  if (ctid == 0) {
-    const int old = atomicAdd(ws_ptr<int32_t>(p, p.L.blk_ticket) + blk, done);
-    *s_flag = (old + done == tiles);
-  }
-  consumer_sync();
-  if (*s_flag) {
-    __threadfence();
-    requant_rows(p, r0, n, s_red, ctid);
-  }
-}
-
-// GEMM2: each routed row of the item adds the columns it completed to its
-// token's counter; tokens that reach rows * h are combined by this CTA.
-// s_tok: at least m ints of scratch.
-__device__ void gemm2_item_done(const FwdParams& p, bool routed, int m, const int32_t* tok_of, int cols,
-                                int* s_tok, int ctid) {
-  if (ctid < m) {
-    int done = -1;
-    if (routed) {
-      const int t = tok_of[ctid];
-      const int old = atomicAdd(ws_ptr<int32_t>(p, p.L.tok_ticket) + t, cols);
-      if (old + cols == ws_ptr<int32_t>(p, p.L.tok_expect)[t]) done = t;
-    }
-    s_tok[ctid] = done;
-  }
-  consumer_sync();
-  for (int i = 0; i < m; ++i) {
-    const int t = s_tok[i];
-    if (t >= 0) {
-      __threadfence();
-      combine_token(p, t, ctid);
-    }
-  }
-}
 
 // ===================================================================== small
 namespace small_path {
@@ -288,12 +161,14 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
   const int32_t* sm_rows = sm_row0 + st;
   // contiguous run of items for this CTA (consecutive tiles of one expert are
   // contiguous in memory), split by cost in the dispatch kernel
+  // with big blocks in the forward, tokens are combined by the combine kernel
+  const bool has_big = slots[SlotTable::kBigBlocks] > 0;
   const int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges) + (G1 ? 0 : kMaxCtas + 1);
   const long it_begin = ranges[blockIdx.x];
   const long it_end = ranges[blockIdx.x + 1];
   const int slot_first = static_cast<int>(it_begin / J);
   const int n_cached = it_end > it_begin ? static_cast<int>((it_end - 1) / J) - slot_first + 1 : 0;
-  const int site = (G1 ? kKGemm1 : kKGemm2) * 16;
+  const int site = (G1 ? kKGemm1Small : kKGemm2Small) * 16;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -494,8 +369,8 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       if (run_end) {
         __threadfence();
         consumer_sync();
-        if (G1) gemm1_item_done(p, cur.slot, J, run_items, cur.row0, m, s_flag, s_red, ctid);
-        else gemm2_item_done(p, cur.e >= 0, m, info_tok + is * MT, BN * run_items, s_tok, ctid);
+        if (G1) gemm1_item_done(p, cur.slot, J, run_items, cur.row0, m, s_flag, s_red, ctid, false);
+        else if (!has_big) gemm2_item_done(p, cur.e >= 0, m, info_tok + is * MT, BN * run_items, s_tok, ctid);
         run_items = 0;
       }
     }
@@ -503,341 +378,27 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
   }
 }
 
-__device__ void inval_barriers(char* smem) {
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  for (int s = 0; s < 2 * STAGES + 2; ++s) mbar_inval(full + s);
-}
-
 }  // namespace small_path
 
-// ======================================================================= big
-namespace big_path {
-
-constexpr int BM = 128;                  // weight rows per item
-constexpr int TB = kTokenBlock;          // token rows per item
-constexpr int KC = 256;                  // K bytes per stage
-constexpr int ROWB = KC + 16;            // smem row stride (16 B pad: conflict-free ldmatrix)
-constexpr int STAGES = 3;
-constexpr int EPI_STRIDE = BM + 4;       // floats per token row of the epilogue tile
-
-constexpr int OFF_W = 0;
-constexpr int OFF_T = OFF_W + STAGES * BM * ROWB;
-constexpr int OFF_EPI = OFF_T + STAGES * TB * ROWB;
-constexpr int OFF_BAR = OFF_EPI + TB * EPI_STRIDE * 4;
-constexpr int OFF_INFO = OFF_BAR + 2 * STAGES * 8;
-constexpr int OFF_MISC = OFF_INFO + 3 * TB * 4;                // abort, flag, red[8], tok[256]
-constexpr int SMEM_BYTES = OFF_MISC + (2 + kConsumerWarps + kConsumers) * 4;
-static_assert(OFF_T % 16 == 0 && OFF_EPI % 16 == 0 && OFF_BAR % 8 == 0, "smem alignment");
-
-struct Item {
-  int slot, e, row0, rows, tb, jt;
-};
-
-__device__ __forceinline__ Item decode_item(long it, int J, const int32_t* slots, int E) {
-  const int st = SlotTable::stride(E);
-  const int32_t* s_exp = slots + SlotTable::kHeader;
-  const int32_t* s_row0 = s_exp + st;
-  const int32_t* s_rows = s_row0 + st;
-  const int32_t* s_blk = s_rows + st;
-  const int n_slots = slots[SlotTable::kNumBig];
-  // last slot s with J * blk[s] <= it
-  int lo = 0, hi = n_slots - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<long>(J) * s_blk[mid] <= it) lo = mid;
-    else hi = mid - 1;
-  }
-  const int s = lo;
-  const long local = it - static_cast<long>(J) * s_blk[s];
-  const int T = s_blk[s + 1] - s_blk[s];
-  Item item;
-  item.slot = s;
-  item.e = s_exp[s];
-  item.row0 = s_row0[s];
-  item.rows = s_rows[s];
-  item.jt = static_cast<int>(local / T);
-  item.tb = static_cast<int>(local % T);
-  return item;
-}
-
-template <int MODE>
-__device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
-  constexpr bool G1 = (MODE == kGemm1SwiGLU || MODE == kGemm1Raw);
-  constexpr bool RAW = (MODE == kGemm1Raw || MODE == kGemm2Raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* empty = full + STAGES;
-  float* tok_scale = reinterpret_cast<float*>(smem + OFF_INFO);
-  int32_t* tok_row = reinterpret_cast<int32_t*>(smem + OFF_INFO + TB * 4);
-  int32_t* tok_tok = reinterpret_cast<int32_t*>(smem + OFF_INFO + 2 * TB * 4);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC);
-  int* s_flag = reinterpret_cast<int*>(smem + OFF_MISC) + 1;
-  float* s_red = reinterpret_cast<float*>(smem + OFF_MISC) + 2;
-  int* s_tok = reinterpret_cast<int*>(smem + OFF_MISC) + 2 + kConsumerWarps;
-
-  const int K = G1 ? p.h : p.I;                       // contraction length
-  const int NW = G1 ? 2 * p.I : p.h;                  // weight rows per expert
-  const int J = G1 ? p.I / 64 : (p.h + BM - 1) / BM;  // output tiles per token block
-  const int n_kc = (K + KC - 1) / KC;
-  const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
-  int32_t* status = ws_ptr<int32_t>(p, p.L.status);
-  const int32_t* s_blk = slots + SlotTable::kHeader + 3 * SlotTable::stride(p.E);
-  const long total_items = static_cast<long>(slots[SlotTable::kBigBlocks]) * J;
-  const int site = (G1 ? kKGemm1 : kKGemm2) * 16 + 8;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_t = policy_evict_last();
-    const int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
-    const int8_t* xq = ws_ptr<int8_t>(p, p.L.x_q);
-    const int8_t* xsq = p.share_uses_xq ? xq : ws_ptr<int8_t>(p, p.L.xs_q);
-    const int8_t* x2 = ws_ptr<int8_t>(p, p.L.x2);
-    int stage_it = 0;
-    for (long it = blockIdx.x; it < total_items; it += gridDim.x) {
-      const Item item = decode_item(it, J, slots, p.E);
-      const int tok0 = item.tb * TB;
-      const int mblk = min(TB, item.rows - tok0);
-      const int8_t* wbase = G1 ? (item.e >= 0 ? p.w1 + static_cast<size_t>(item.e) * NW * K : p.sw1)
-                               : (item.e >= 0 ? p.w2 + static_cast<size_t>(item.e) * NW * K : p.sw2);
-      const int rows_valid = G1 ? BM : min(BM, p.h - item.jt * BM);
-      const int8_t* wrow[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = lane + 32 * q;
-        int n;
-        if (G1) n = (i < 64) ? item.jt * 64 + i : p.I + item.jt * 64 + (i - 64);
-        else n = item.jt * BM + i;
-        wrow[q] = (i < rows_valid) ? wbase + static_cast<size_t>(n) * K : nullptr;
-      }
-      const int8_t* trow[2];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int i = lane + 32 * q;
-        trow[q] = nullptr;
-        if (i < mblk) {
-          const int r = item.row0 + tok0 + i;
-          if (G1) trow[q] = (item.e >= 0 ? xq : xsq) + static_cast<size_t>(row_token[r]) * p.h;
-          else trow[q] = x2 + static_cast<size_t>(r) * p.I;
-        }
-      }
-      for (int kc = 0; kc < n_kc; ++kc, ++stage_it) {
-        const int s = stage_it % STAGES;
-        const int round = stage_it / STAGES;
-        if (round > 0) {
-          if (!mbar_wait_bounded(&empty[s], (round - 1) & 1, abort_flag, status, site + 1, false)) return;
-        }
-        const int k0 = kc * KC;
-        const int bytes = min(KC, K - k0);
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>((rows_valid + mblk) * bytes));
-        __syncwarp();
-        char* wdst = smem + OFF_W + s * BM * ROWB;
-        char* tdst = smem + OFF_T + s * TB * ROWB;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (wrow[q]) bulk_g2s(wdst + (lane + 32 * q) * ROWB, wrow[q] + k0, bytes, &full[s], pol_w);
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-          if (trow[q]) bulk_g2s(tdst + (lane + 32 * q) * ROWB, trow[q] + k0, bytes, &full[s], pol_t);
-      }
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int ctid = threadIdx.x;       // 0..255
-  const int mg = warp & 3;            // rows 32*mg .. 32*mg+31
-  const int kh = warp >> 2;           // K-step parity handled by this warp
-  const int gid = lane >> 2, tig = lane & 3;
-  int32_t* epii = reinterpret_cast<int32_t*>(smem + OFF_EPI);
-  float* epif = reinterpret_cast<float*>(smem + OFF_EPI);
-  const int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
-  const float* xsc = ws_ptr<float>(p, p.L.x_scale);
-  const float* xssc = p.share_uses_xq ? xsc : ws_ptr<float>(p, p.L.xs_scale);
-  const float* s2 = ws_ptr<float>(p, p.L.s2);
-  float* hbuf = ws_ptr<float>(p, p.L.hbuf);
-  uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
-
-  int stage_it = 0;
-  for (long it = blockIdx.x; it < total_items; it += gridDim.x) {
-    const Item item = decode_item(it, J, slots, p.E);
-    const int tok0 = item.tb * TB;
-    const int mblk = min(TB, item.rows - tok0);
-    const int nblk = (mblk + 7) >> 3;
-
-    consumer_sync();  // previous epilogue is done with info / epi
-    if (ctid < mblk) {
-      const int r = item.row0 + tok0 + ctid;
-      const int t = row_token[r];
-      tok_row[ctid] = r;
-      tok_tok[ctid] = t;
-      tok_scale[ctid] = G1 ? (item.e >= 0 ? xsc : xssc)[t] : s2[r];
-    }
-
-    int32_t acc[2][8][4];
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 8; ++b)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[a][b][c] = 0;
-
-    for (int kc = 0; kc < n_kc; ++kc, ++stage_it) {
-      const int s = stage_it % STAGES;
-      const int round = stage_it / STAGES;
-      const bool ok = mbar_wait_bounded(&full[s], round & 1, abort_flag, status, site + 2);
-      if (ok) {
-        const int bytes = min(KC, K - kc * KC);
-        const int nks = bytes >> 5;
-        const char* Ws = smem + OFF_W + s * BM * ROWB;
-        const char* Ts = smem + OFF_T + s * TB * ROWB;
-        for (int ks = kh; ks < nks; ks += 2) {
-          uint32_t a[2][4];
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            const int row = 32 * mg + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int col = ks * 32 + (lane >> 4) * 16;
-            ldmatrix_x4(a[mt][0], a[mt][1], a[mt][2], a[mt][3], Ws + row * ROWB + col);
-          }
-#pragma unroll
-          for (int nbp = 0; nbp < 8; nbp += 2) {
-            if (nbp < nblk) {
-              const int tok = nbp * 8 + (lane & 7) + (lane >> 4) * 8;
-              const int col = ks * 32 + ((lane >> 3) & 1) * 16;
-              uint32_t b0, b1, b2, b3;
-              ldmatrix_x4(b0, b1, b2, b3, Ts + tok * ROWB + col);
-#pragma unroll
-              for (int mt = 0; mt < 2; ++mt) {
-                mma_s8_16832(acc[mt][nbp], a[mt][0], a[mt][1], a[mt][2], a[mt][3], b0, b1);
-                if (nbp + 1 < nblk)
-                  mma_s8_16832(acc[mt][nbp + 1], a[mt][0], a[mt][1], a[mt][2], a[mt][3], b2, b3);
-              }
-            }
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
-
-    // ---- epilogue: combine the two K halves in smem, dequantise, activate
-    if (kh == 1) {
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nb = 0; nb < 8; ++nb)
-          if (nb < nblk)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int n = 32 * mg + 16 * mt + gid + (c >> 1) * 8;
-              const int tok = 8 * nb + 2 * tig + (c & 1);
-              epii[tok * EPI_STRIDE + n] = acc[mt][nb][c];
-            }
-    }
-    consumer_sync();
-    // every consumer warp has left its K loop: the abort flag is final for this item
-    const bool stop = *abort_flag != 0;
-    if (kh == 0) {
-      const float* wsc;
-      if (G1) wsc = item.e >= 0 ? p.w1s + static_cast<size_t>(item.e) * NW : p.sw1s;
-      else wsc = item.e >= 0 ? p.w2s + static_cast<size_t>(item.e) * NW : p.sw2s;
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nb = 0; nb < 8; ++nb)
-          if (nb < nblk)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int n = 32 * mg + 16 * mt + gid + (c >> 1) * 8;
-              const int tok = 8 * nb + 2 * tig + (c & 1);
-              const int v = acc[mt][nb][c] + epii[tok * EPI_STRIDE + n];
-              int ng;
-              if (G1) ng = (n < 64) ? item.jt * 64 + n : p.I + item.jt * 64 + (n - 64);
-              else ng = item.jt * BM + n;
-              if (RAW) {
-                if (tok < mblk && ng < NW) raw[static_cast<size_t>(tok_row[tok]) * NW + ng] = v;
-              } else {
-                float y = 0.0f;
-                if (tok < mblk && ng < NW) y = __fmul_rn(__fmul_rn(__int2float_rn(v), wsc[ng]), tok_scale[tok]);
-                epif[tok * EPI_STRIDE + n] = y;
-              }
-            }
-    }
-    if (!RAW) {
-      consumer_sync();
-      if (G1) {
-        const int jbase = item.jt * 64;
-        for (int idx = ctid; idx < mblk * 64; idx += kConsumers) {
-          const int tok = idx >> 6, j = idx & 63;
-          const float g = epif[tok * EPI_STRIDE + j];
-          const float u = epif[tok * EPI_STRIDE + 64 + j];
-          const float d = __fadd_rn(1.0f, expf(-g));
-          const float hv = __fmul_rn(__fdiv_rn(g, d), u);
-          hbuf[static_cast<size_t>(tok_row[tok]) * p.I + jbase + j] = hv;
-        }
-        __threadfence();
-        consumer_sync();
-        gemm1_item_done(p, SlotTable::stride(p.E) + s_blk[item.slot] + item.tb, J, 1, item.row0 + tok0, mblk,
-                        s_flag, s_red, ctid);
-      } else {
-        const int nbase = item.jt * BM;
-        const int nvalid = min(BM, p.h - nbase);
-        for (int idx = ctid; idx < mblk * BM; idx += kConsumers) {
-          const int tok = idx >> 7, n = idx & (BM - 1);
-          if (n >= nvalid) continue;
-          const uint16_t b = f32_to_bf16_bits(epif[tok * EPI_STRIDE + n]);
-          if (item.e >= 0) y2[static_cast<size_t>(tok_row[tok]) * p.h + nbase + n] = b;
-          else p.sout[static_cast<size_t>(tok_tok[tok]) * p.h + nbase + n] = b;
-        }
-        __threadfence();
-        consumer_sync();
-        gemm2_item_done(p, item.e >= 0, mblk, tok_tok, nvalid, s_tok, ctid);
-      }
-    }
-    if (stop) break;
-  }
-}
-
-}  // namespace big_path
-
-constexpr int SMEM_BYTES = small_path::SMEM_BYTES > big_path::SMEM_BYTES ? small_path::SMEM_BYTES
-                                                                          : big_path::SMEM_BYTES;
+constexpr int SMEM_BYTES = small_path::SMEM_BYTES;
 static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
 
-// Small phase, then big phase, in one persistent launch.  The phases reuse
-// the same shared memory: every copy of the small phase has landed before
-// its consumers finish, and its barriers are invalidated before reuse.
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) moe_gemm_kernel(FwdParams p, int32_t* raw) {
+__global__ void __launch_bounds__(kThreads, 1) moe_gemm_small_kernel(FwdParams p, int32_t* raw) {
   extern __shared__ __align__(128) char smem[];
   // everything below reads what the preceding kernel wrote
   grid_dependency_wait();
   grid_launch_dependents();
   small_path::run<MODE>(p, raw, smem);
-  __syncthreads();
-  if (threadIdx.x == 0) small_path::inval_barriers(smem);
-  __syncthreads();
-  big_path::run<MODE>(p, raw, smem);
 }
 
 }  // namespace
 
-cudaError_t moe_gemm_prepare_attributes() {
-  const void* fns[] = {reinterpret_cast<const void*>(moe_gemm_kernel<kGemm1SwiGLU>),
-                       reinterpret_cast<const void*>(moe_gemm_kernel<kGemm2Bf16>),
-                       reinterpret_cast<const void*>(moe_gemm_kernel<kGemm1Raw>),
-                       reinterpret_cast<const void*>(moe_gemm_kernel<kGemm2Raw>)};
+cudaError_t moe_gemm_small_prepare_attributes() {
+  const void* fns[] = {reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm1SwiGLU>),
+                       reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm2Bf16>),
+                       reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm1Raw>),
+                       reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm2Raw>)};
   for (const void* f : fns) {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -845,15 +406,15 @@ cudaError_t moe_gemm_prepare_attributes() {
   return cudaSuccess;
 }
 
-cudaError_t launch_moe_gemm(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s) {
+cudaError_t launch_moe_gemm_small(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(num_ctas), dim3(kThreads), SMEM_BYTES, s, attr);
   switch (mode) {
-    case kGemm1SwiGLU: return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<kGemm1SwiGLU>, p, raw_acc);
-    case kGemm2Bf16: return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<kGemm2Bf16>, p, raw_acc);
-    case kGemm1Raw: return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<kGemm1Raw>, p, raw_acc);
-    case kGemm2Raw: return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<kGemm2Raw>, p, raw_acc);
+    case kGemm1SwiGLU: return cudaLaunchKernelEx(&cfg, moe_gemm_small_kernel<kGemm1SwiGLU>, p, raw_acc);
+    case kGemm2Bf16: return cudaLaunchKernelEx(&cfg, moe_gemm_small_kernel<kGemm2Bf16>, p, raw_acc);
+    case kGemm1Raw: return cudaLaunchKernelEx(&cfg, moe_gemm_small_kernel<kGemm1Raw>, p, raw_acc);
+    case kGemm2Raw: return cudaLaunchKernelEx(&cfg, moe_gemm_small_kernel<kGemm2Raw>, p, raw_acc);
     default: return cudaErrorInvalidValue;
   }
 }

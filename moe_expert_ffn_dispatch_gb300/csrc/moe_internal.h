@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace moe {
@@ -45,6 +46,8 @@ struct WsLayout {
   size_t tok_ticket; // [bs_max] int32: GEMM2 output columns done per token
   size_t tok_expect; // [bs_max] int32: columns that complete a token (rows * h)
   size_t ranges;     // [2][kMaxCtas + 1] int32: small-phase item range of each CTA (GEMM1, GEMM2)
+  size_t x1h;        // [rows, h] f16: GEMM1 token operand of the rows in big blocks (codes as f16)
+  size_t x2h;        // [rows, I] f16: GEMM2 token operand of the rows in big blocks
   size_t total;
   size_t sizes[24];  // bytes per region id (debug_region)
 };
@@ -53,7 +56,7 @@ struct WsLayout {
 enum Region : int {
   kRegStatus = 0, kRegCounts, kRegOffsets, kRegRowOf, kRegTkOfRow, kRegActive, kRegXq, kRegXScale,
   kRegXsq, kRegXsScale, kRegH, kRegX2, kRegS2, kRegY2, kRegSlots, kRegRowToken, kRegSharedRow,
-  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kRegRanges, kNumRegions
+  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kRegRanges, kRegX1h, kRegX2h, kNumRegions
 };
 
 constexpr int kMaxCtas = 1023;  // persistent grid size limit (one CTA per SM)
@@ -78,7 +81,7 @@ struct SlotTable {
 
 constexpr int kSmallRows = 8;     // experts with <= this many rows take the dp4a path ...
 constexpr int kSmallMaxK = 4096;  // ... when both contraction lengths are at most this
-constexpr int kTokenBlock = 64;  // token rows per GEMM work item
+constexpr int kTokenBlock = 128;  // token rows per big-phase work item (the MMA's N)
 
 // ---------------------------------------------------------------- params
 struct FwdParams {
@@ -114,7 +117,27 @@ __host__ __device__ inline T* ws_ptr(const FwdParams& p, size_t off) {
 }
 
 // kernel ids (timing / status sites)
-enum KernelId : int { kKDispatchQuant = 0, kKGemm1 = 1, kKGemm2 = 2, kNumKernels = 3 };
+enum KernelId : int {
+  kKDispatchQuant = 0,
+  kKExpand = 1,
+  kKGemm1Small = 2,
+  kKGemm1Big = 3,
+  kKRequantBig = 4,
+  kKGemm2Small = 5,
+  kKGemm2Big = 6,
+  kKCombine = 7,
+  kNumKernels = 8
+};
+
+// TMA descriptors of the big-phase operands (built on the host per forward).
+struct alignas(64) TcMaps {
+  CUtensorMap a1;   // W1 [E*2I, h] int8, box {64, 64}
+  CUtensorMap a1s;  // shared W1 [2I, h] int8, box {64, 64}
+  CUtensorMap a2;   // W2 [E*h, I] int8, box {64, 128}
+  CUtensorMap a2s;  // shared W2 [h, I] int8, box {64, 128}
+  CUtensorMap b1;   // x1h [rows, h] f16, box {64, 128}, 128-byte swizzle
+  CUtensorMap b2;   // x2h [rows, I] f16, box {64, 128}, 128-byte swizzle
+};
 
 // GEMM modes
 enum GemmMode : int { kGemm1SwiGLU = 0, kGemm2Bf16 = 1, kGemm1Raw = 2, kGemm2Raw = 3 };
@@ -137,8 +160,14 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStr
 // ---------------------------------------------------------------- launches
 size_t dispatch_smem_bytes(int E);
 cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s);
-cudaError_t launch_moe_gemm(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);
-cudaError_t moe_gemm_prepare_attributes();
+cudaError_t launch_expand(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_requant_big(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_combine(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_moe_gemm_small(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);
+cudaError_t launch_moe_gemm_big(const FwdParams& p, const TcMaps& maps, int mode, int32_t* raw_acc, int num_ctas,
+                                cudaStream_t s);
+cudaError_t moe_gemm_small_prepare_attributes();
+cudaError_t moe_gemm_big_prepare_attributes();
 cudaError_t dispatch_prepare_attributes(int E);
 int dispatch_noalloc(const int32_t* expert_ids, const uint8_t* mask, int bs, int topk, int E,
                      int32_t* expert_token_nums, int32_t* expand_row, cudaStream_t s);

@@ -106,7 +106,7 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
     dw = device_weights(inp, dev)
     if staged and bs > 0:
         # stop after GEMM1 (SwiGLU + requant): h is reused by y2 once GEMM2 runs
-        blk.forward_inputs(di, dw, until=m.KERNEL_ID["gemm1_swiglu_requant"])
+        blk.forward_inputs(di, dw, until=m.KERNEL_ID["requant_big"])
         torch.cuda.synchronize()
         staged_h = blk.region("h").clone().cpu()
     out, sout, nums = blk.forward_inputs(di, dw)
@@ -185,11 +185,15 @@ def check_raw_accumulators(blk, inp, ref, di, dw, dev):
     assert torch.equal(a1[:R], ref["acc1"]), "acc1 routed differs"
     if S:
         assert torch.equal(a1[bs * K:bs * K + S], ref["share_acc1"][act]), "acc1 shared differs"
-    # plant the oracle's x2 and contract it
+    # plant the oracle's x2 (int8 for the small-expert kernel, f16 codes for the
+    # tensor-core kernel) and contract it
     x2v = blk.region("x2").view(torch.int8)[:rows * I].view(rows, I)
+    x2hv = blk.region("x2h").view(torch.float16)[:rows * I].view(rows, I)
     x2v[:R] = ref["x2"].to(dev)
+    x2hv[:R] = ref["x2"].to(dev).to(torch.float16)
     if S:
         x2v[bs * K:bs * K + S] = ref["share_x2"][act].to(dev)
+        x2hv[bs * K:bs * K + S] = ref["share_x2"][act].to(dev).to(torch.float16)
     acc2 = torch.zeros(rows, h, dtype=torch.int32, device=dev)
     blk.debug_gemm_acc(2, acc2, *fargs)
     torch.cuda.synchronize()
