@@ -230,13 +230,17 @@ int prepare_maps(moe_fused_handle* hd, const moe::FwdParams& p) {
   const void* sw1 = p.sw1 ? p.sw1 : p.w1;
   const void* sw2 = p.sw2 ? p.sw2 : p.w2;
   moe::TcMaps& m = hd->maps;
-  bool ok = encode_2d(&m.a1, p.w1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, E * 2 * I, h, 64, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_2d(&m.a1s, sw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 2 * I, h, 64, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_2d(&m.a2, p.w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, E * h, I, 64, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_2d(&m.a2s, sw2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, h, I, 64, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+  bool ok = encode_2d(&m.a1, p.w1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, E * 2 * I, h, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_2d(&m.a1s, sw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 2 * I, h, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_2d(&m.a2, p.w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, E * h, I, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_2d(&m.a2s, sw2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, h, I, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
             encode_2d(&m.b1, p.ws + p.L.x1h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, brows, h, 64, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B) &&
             encode_2d(&m.b2, p.ws + p.L.x2h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, brows, I, 64, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_2d(&m.b1n, p.ws + p.L.x1h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, brows, h, 64, 16,
+                      CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_2d(&m.b2n, p.ws + p.L.x2h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, brows, I, 64, 16,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) {
     hd->maps_valid = false;

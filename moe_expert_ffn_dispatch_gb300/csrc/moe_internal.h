@@ -131,12 +131,14 @@ enum KernelId : int {
 
 // TMA descriptors of the big-phase operands (built on the host per forward).
 struct alignas(64) TcMaps {
-  CUtensorMap a1;   // W1 [E*2I, h] int8, box {64, 64}
-  CUtensorMap a1s;  // shared W1 [2I, h] int8, box {64, 64}
-  CUtensorMap a2;   // W2 [E*h, I] int8, box {64, 128}
-  CUtensorMap a2s;  // shared W2 [h, I] int8, box {64, 128}
+  CUtensorMap a1;   // W1 [E*2I, h] int8, box {128, 16} (16-row gate / up groups), 128-byte swizzle
+  CUtensorMap a1s;  // shared W1 [2I, h] int8, box {128, 16}, 128-byte swizzle
+  CUtensorMap a2;   // W2 [E*h, I] int8, box {128, 128}, 128-byte swizzle
+  CUtensorMap a2s;  // shared W2 [h, I] int8, box {128, 128}, 128-byte swizzle
   CUtensorMap b1;   // x1h [rows, h] f16, box {64, 128}, 128-byte swizzle
   CUtensorMap b2;   // x2h [rows, I] f16, box {64, 128}, 128-byte swizzle
+  CUtensorMap b1n;  // x1h, box {64, 16}: blocks of at most 64 rows
+  CUtensorMap b2n;  // x2h, box {64, 16}
 };
 
 // GEMM modes

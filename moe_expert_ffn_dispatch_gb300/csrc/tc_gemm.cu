@@ -13,19 +13,30 @@
 // accumulator covers 1024 K at most and is then drained into int32 registers,
 // which keeps the result bit-identical to an int32 GEMM.
 //
-// Tile: 128 weight rows (GEMM1: 64 gate + the 64 matching up rows) x up to
-// 128 token rows of one expert x all of K, weights as the MMA's M operand.
+// Tile: 128 weight rows x up to 128 token rows of one expert x all of K,
+// weights as the MMA's M operand (tensor-memory lanes, read by the MMA from
+// tensor memory), tokens as N (shared memory).  Shared-memory bandwidth is
+// what bounds this kernel: per 128 of K it carries the int8 weight stage
+// (TMA write + converter read) and the f16 token stage (TMA write + MMA read).  For
+// GEMM1 the 128 rows are 64 gate rows and the 64 matching up rows, laid out
+// so that each 32-lane quadrant of tensor memory holds 16 gate rows in its
+// lanes 0..15 and the 16 matching up rows in lanes 16..31: SwiGLU pairs meet
+// inside one warp and swap halves with a shuffle.
 // The requant of big blocks and the combine of forwards with big blocks run
 // as separate parallel kernels (below): done by the CTA that finishes a block
 // last, they would serialise 128-row blocks and 128-token tiles on a few SMs.
 // Warp roles (one CTA per SM, persistent):
-//   warp 0      TMA of the int8 weight boxes into an 8-deep staging ring
-//   warp 2      TMA of the f16 token boxes (128-byte swizzle) into a 3-deep ring
-//   warps 4..7  convert int8 weight stages to f16 tiles in the 128-byte swizzle
+// A stage is 128 of K: two 64-wide atoms of the 128-byte swizzle per f16 tile.
+//   warp 0      TMA of the int8 weight boxes into a 4-deep staging ring
+//   warp 2      TMA of the f16 token boxes (128-byte swizzle) into a 3-deep
+//               ring; 16-row boxes when the block has at most 64 rows
+//   warps 4..7  convert int8 weight stages to f16, one weight row per
+//               thread, into a 4-deep ring in tensor memory (the MMA's A
+//               operand), which keeps the f16 weights off shared memory
 //   warp 1      one thread issues tcgen05.mma (M128, N = rows rounded to 16,
 //               K16) into two tensor-memory accumulators, alternating per
 //               1024 of K, and commits to the ring and accumulator barriers
-//   warps 8..15 drain accumulators (tcgen05.ld) into int32, then the fused
+//   warps 8..15 drain accumulators (tcgen05.ld) into int32, then the
 //               epilogue; two warps per tensor-memory lane quadrant
 // All rings are mbarrier full/empty pairs (the FIFO of the Mega-MoE
 // analysis §4); every wait is bounded.
@@ -41,30 +52,36 @@ namespace {
 
 constexpr int BM = 128;               // weight rows per tile (MMA M)
 constexpr int TB = kTokenBlock;       // token rows per tile (MMA N <= 128)
-constexpr int KB = 64;                // K elements per stage: one 128-byte f16 row
-constexpr int CHUNK_KB = 16;          // stages per exact accumulation chunk (1024 of K)
-constexpr int S8 = 8;                 // int8 weight staging ring
-constexpr int S16 = 3;                // f16 operand ring
-constexpr int kTmemCols = 2 * TB;     // two accumulators
+constexpr int KB = 128;               // K elements per stage
+constexpr int KA = 64;                // K elements per swizzle atom (one 128-byte f16 row)
+constexpr int ATOMS = KB / KA;        // swizzle atoms per f16 stage
+constexpr int CHUNK_KB = 1024 / KB;   // stages per exact accumulation chunk (1024 of K)
+constexpr int S8 = 8;                 // int8 weight staging ring (from HBM)
+constexpr int SA = 4;                 // f16 weight ring in tensor memory (converted in the CTA)
+constexpr int SB = 3;                 // f16 token ring (from L2)
+constexpr int kAccCols = 2 * TB;      // two fp32 accumulators of TB columns
+constexpr int kAStageCols = KB / 2;   // one f16 weight stage: 128 lanes x 64 columns of f16 pairs
+constexpr int kTmemCols = 512;        // kAccCols + SA * kAStageCols, rounded to a power of two
+static_assert(kAccCols + SA * kAStageCols <= kTmemCols, "tensor memory budget");
+constexpr int kSmallBox = 16;         // rows of the narrow token box
 
 constexpr int kBigWarps = 16;
 constexpr int kBigThreads = kBigWarps * 32;
 constexpr int kWarpA = 0, kWarpMma = 1, kWarpB = 2;
 constexpr int kConvWarp0 = 4, kConvWarps = 4;
 constexpr int kEpiWarp0 = 8;          // epilogue warps 8..15 = the 256 "consumer" threads
-constexpr int XSTRIDE = TB + 1;       // floats per row of the exchange tile (bank spread)
 
-constexpr int A8_BYTES = BM * KB;                    // 8 KB
-constexpr int F16_TILE = 128 * KB * 2;               // 16 KB
-constexpr int OFF_A16 = 0;                           // S16 x [128][64] f16, swizzled
-constexpr int OFF_B16 = OFF_A16 + S16 * F16_TILE;    // S16 x [128][64] f16, swizzled (TMA)
-constexpr int OFF_A8 = OFF_B16 + S16 * F16_TILE;     // S8 x [128][64] int8
-constexpr int OFF_X = OFF_A8 + S8 * A8_BYTES;        // [64][XSTRIDE] fp32 (GEMM1 up half)
-constexpr int OFF_BAR = OFF_X + 64 * XSTRIDE * 4;
-constexpr int NBAR = 2 * S8 + 3 * S16 + 4;
+constexpr int A8_BYTES = BM * KB;                    // 16 KB: [128 rows][128] int8, 128-byte swizzle
+constexpr int F16_ATOM = 128 * KA * 2;               // 16 KB: [128 rows][64] f16, 128-byte swizzle
+constexpr int F16_TILE = ATOMS * F16_ATOM;           // 32 KB
+constexpr int OFF_B16 = 0;                           // SB x ATOMS x [128][64] f16, swizzled (TMA)
+constexpr int OFF_A8 = OFF_B16 + SB * F16_TILE;      // S8 x [128][128] int8, swizzled (TMA)
+constexpr int OFF_BAR = OFF_A8 + S8 * A8_BYTES;
+constexpr int NBAR = 2 * S8 + 2 * SA + 2 * SB + 4;
 constexpr int OFF_INFO = OFF_BAR + NBAR * 8;         // tok_scale, tok_row, tok_tok [TB]
 constexpr int OFF_MISC = OFF_INFO + 3 * TB * 4;      // tmem slot, abort flag
-constexpr int SMEM_BYTES = OFF_MISC + (3 + kConsumerWarps + TB) * 4;
+constexpr int SMEM_BYTES = OFF_MISC + 16;
+static_assert(KB == 128 && KA == 64, "the MMA loop issues two atoms of four K16 steps per stage");
 static_assert(OFF_B16 % 1024 == 0 && OFF_A8 % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
@@ -117,10 +134,6 @@ __device__ __forceinline__ void int8x16_to_f16(uint4 in, uint4& lo, uint4& hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// byte offset of 16-byte chunk j of row r in a [rows][64] f16 tile with the
-// 128-byte swizzle (the layout the UMMA descriptor and the TMA expect)
-__device__ __forceinline__ int sw128_chunk(int r, int j) { return (r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4); }
-
 template <int MODE>
 __global__ void __launch_bounds__(kBigThreads, 1)
     moe_gemm_big_kernel(const __grid_constant__ TcMaps maps, FwdParams p, int32_t* raw) {
@@ -129,10 +142,11 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   extern __shared__ __align__(1024) char smem[];
   uint64_t* a8_full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* a8_empty = a8_full + S8;
-  uint64_t* b_full = a8_empty + S8;
-  uint64_t* f16_empty = b_full + S16;
-  uint64_t* cv_full = f16_empty + S16;
-  uint64_t* acc_full = cv_full + S16;
+  uint64_t* a16_full = a8_empty + S8;
+  uint64_t* a16_empty = a16_full + SA;
+  uint64_t* b_full = a16_empty + SA;
+  uint64_t* b_empty = b_full + SB;
+  uint64_t* acc_full = b_empty + SB;
   uint64_t* acc_empty = acc_full + 2;
   float* tok_scale = reinterpret_cast<float*>(smem + OFF_INFO);
   int32_t* tok_row = reinterpret_cast<int32_t*>(smem + OFF_INFO) + TB;
@@ -146,10 +160,9 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   const int K = G1 ? p.h : p.I;
   const int NW = G1 ? 2 * p.I : p.h;
   const int J = G1 ? p.I / 64 : (p.h + BM - 1) / BM;   // weight tiles per token block
-  const int n_kb = K / KB;
+  const int n_kb = (K + KB - 1) / KB;  // a last half stage reads zeros beyond K (TMA fill)
   const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
   int32_t* status = ws_ptr<int32_t>(p, p.L.status);
-  const int32_t* s_blk = slots + SlotTable::kHeader + 3 * SlotTable::stride(p.E);
   const long total = static_cast<long>(slots[SlotTable::kBigBlocks]) * J;
   const int site = (G1 ? kKGemm1Big : kKGemm2Big) * 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,10 +175,13 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       mbar_init(&a8_full[s], 1);
       mbar_init(&a8_empty[s], kConvWarps);
     }
-    for (int s = 0; s < S16; ++s) {
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(&a16_full[s], kConvWarps);
+      mbar_init(&a16_empty[s], 1);
+    }
+    for (int s = 0; s < SB; ++s) {
       mbar_init(&b_full[s], 1);
-      mbar_init(&f16_empty[s], 1);
-      mbar_init(&cv_full[s], kConvWarps);
+      mbar_init(&b_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -185,24 +201,31 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     if (lane == 0) {
       const void* map = G1 ? &maps.a1 : &maps.a2;
       const void* map_s = G1 ? &maps.a1s : &maps.a2s;
-      long n = 0;
+      int s = 0;
+      uint32_t ph = 0;
+      bool wrapped = false;
       for (long it = blockIdx.x; it < total; it += gridDim.x) {
         const BigItem x = decode_item(it, J, slots, p.E);
         const bool sh = x.e < 0;
         const int rbase = sh ? 0 : x.e * NW;
-        for (int kb = 0; kb < n_kb; ++kb, ++n) {
-          const int s = static_cast<int>(n % S8);
-          const long round = n / S8;
-          if (round > 0 && !mbar_wait_bounded(&a8_empty[s], (round - 1) & 1, abort_flag, status, site + 1, false))
+        const void* mp = sh ? map_s : map;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (wrapped && !mbar_wait_bounded(&a8_empty[s], ph ^ 1u, abort_flag, status, site + 1, false))
             goto done_a;
           mbar_arrive_expect_tx(&a8_full[s], A8_BYTES);
           char* dst = smem + OFF_A8 + s * A8_BYTES;
           if (G1) {
-            tma_load_2d(dst, sh ? map_s : map, kb * KB, rbase + x.jt * 64, &a8_full[s]);
-            tma_load_2d(dst + 64 * KB, sh ? map_s : map, kb * KB, rbase + p.I + x.jt * 64, &a8_full[s]);
+            // tile rows 32 g .. 32 g + 15: gate rows 16 g ..; 32 g + 16 ..: the matching up rows
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const int gate = rbase + x.jt * 64 + 16 * g;
+              tma_load_2d(dst + (32 * g) * KB, mp, kb * KB, gate, &a8_full[s]);
+              tma_load_2d(dst + (32 * g + 16) * KB, mp, kb * KB, gate + p.I, &a8_full[s]);
+            }
           } else {
-            tma_load_2d(dst, sh ? map_s : map, kb * KB, rbase + x.jt * BM, &a8_full[s]);
+            tma_load_2d(dst, mp, kb * KB, rbase + x.jt * BM, &a8_full[s]);
           }
+          if (++s == S8) { s = 0; ph ^= 1u; wrapped = true; }
         }
       }
     done_a:;
@@ -211,88 +234,141 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     // ---------------------------------------------------- token TMA (f16)
     if (lane == 0) {
       const void* map = G1 ? &maps.b1 : &maps.b2;
-      long n = 0;
+      const void* map_n = G1 ? &maps.b1n : &maps.b2n;
+      int s = 0;
+      uint32_t ph = 0;
+      bool wrapped = false;
       for (long it = blockIdx.x; it < total; it += gridDim.x) {
         const BigItem x = decode_item(it, J, slots, p.E);
         const int r0 = x.row0 + x.tb * TB;
-        for (int kb = 0; kb < n_kb; ++kb, ++n) {
-          const int s = static_cast<int>(n % S16);
-          const long round = n / S16;
-          if (round > 0 && !mbar_wait_bounded(&f16_empty[s], (round - 1) & 1, abort_flag, status, site + 2, false))
+        const int mblk = min(TB, x.rows - x.tb * TB);
+        // narrow boxes for short blocks: the MMA reads only the first mblk rows
+        const int nbox = mblk > 64 ? 1 : (mblk + kSmallBox - 1) / kSmallBox;
+        const uint32_t bytes = ATOMS * (mblk > 64 ? F16_ATOM : nbox * kSmallBox * KA * 2);
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (wrapped && !mbar_wait_bounded(&b_empty[s], ph ^ 1u, abort_flag, status, site + 2, false))
             goto done_b;
-          mbar_arrive_expect_tx(&b_full[s], F16_TILE);
-          tma_load_2d(smem + OFF_B16 + s * F16_TILE, map, kb * KB, r0, &b_full[s]);
+          mbar_arrive_expect_tx(&b_full[s], bytes);
+          char* dst = smem + OFF_B16 + s * F16_TILE;
+#pragma unroll
+          for (int a = 0; a < ATOMS; ++a) {
+            const int kx = kb * KB + a * KA;
+            if (mblk > 64) {
+              tma_load_2d(dst + a * F16_ATOM, map, kx, r0, &b_full[s]);
+            } else {
+              for (int b = 0; b < nbox; ++b)
+                tma_load_2d(dst + a * F16_ATOM + b * kSmallBox * KA * 2, map_n, kx, r0 + b * kSmallBox, &b_full[s]);
+            }
+          }
+          if (++s == SB) { s = 0; ph ^= 1u; wrapped = true; }
         }
       }
     done_b:;
     }
   } else if (aligned && warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
-    // ------------------------------------------- int8 -> f16 weight stages
-    const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
-    long n = 0;
-    for (long it = blockIdx.x; it < total; it += gridDim.x) {
-      for (int kb = 0; kb < n_kb; ++kb, ++n) {
-        const int s8 = static_cast<int>(n % S8), s16 = static_cast<int>(n % S16);
-        const long r8 = n / S8, r16 = n / S16;
-        bool ok = mbar_wait_bounded(&a8_full[s8], r8 & 1, abort_flag, status, site + 3);
-        if (ok && r16 > 0) ok = mbar_wait_bounded(&f16_empty[s16], (r16 - 1) & 1, abort_flag, status, site + 4);
+    // ------------------------------- int8 -> f16 weight rows, into tensor memory
+    // Thread = weight row = tensor-memory lane (warp 4 + q owns lanes 32 q ..).
+    // Row r's 16-byte chunk j sits at chunk j ^ (r % 8) of its 128-byte line
+    // (the TMA's 128-byte swizzle), so the 32 rows of a warp read 8 distinct
+    // bank groups per load.  Codes 16 j .. 16 j + 15 become the f16 pairs of
+    // columns 8 j .. 8 j + 7 of the stage.
+    const int row = (warp - kConvWarp0) * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kAccCols;
+    int s8 = 0, sa = 0;
+    uint32_t p8 = 0, pa = 0;
+    bool wrapped = false;
+    bool ok = true;
+    for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      for (int kb = 0; kb < n_kb; ++kb) {
+        ok = mbar_wait_bounded(&a8_full[s8], p8, abort_flag, status, site + 3);
+        if (ok && wrapped) ok = mbar_wait_bounded(&a16_empty[sa], pa ^ 1u, abort_flag, status, site + 4);
         if (ok) {
-          const char* src = smem + OFF_A8 + s8 * A8_BYTES;
-          char* dst = smem + OFF_A16 + s16 * F16_TILE;
+          tc_fence_after();
+          const char* src = smem + OFF_A8 + s8 * A8_BYTES + row * KB;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int task = ct + 128 * i;
-            const int row = task >> 2, c = task & 3;
-            const uint4 v = *reinterpret_cast<const uint4*>(src + row * KB + c * 16);
-            uint4 lo, hi;
-            int8x16_to_f16(v, lo, hi);
-            *reinterpret_cast<uint4*>(dst + sw128_chunk(row, 2 * c)) = lo;
-            *reinterpret_cast<uint4*>(dst + sw128_chunk(row, 2 * c + 1)) = hi;
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t v[32];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int j = 4 * h2 + jj;
+              const uint4 c = *reinterpret_cast<const uint4*>(src + ((j ^ (row & 7)) << 4));
+              uint4 lo, hi;
+              int8x16_to_f16(c, lo, hi);
+              v[8 * jj + 0] = lo.x; v[8 * jj + 1] = lo.y; v[8 * jj + 2] = lo.z; v[8 * jj + 3] = lo.w;
+              v[8 * jj + 4] = hi.x; v[8 * jj + 5] = hi.y; v[8 * jj + 6] = hi.z; v[8 * jj + 7] = hi.w;
+            }
+            tmem_st32(lane_base + sa * kAStageCols + 32 * h2, v);
           }
-          fence_proxy_async_smem();
+          tmem_st_wait();
+          tc_fence_before();
         }
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&a8_empty[s8]);
-          mbar_arrive(&cv_full[s16]);
+          mbar_arrive(&a16_full[sa]);
         }
         if (!ok) break;
+        if (++s8 == S8) { s8 = 0; p8 ^= 1u; }
+        if (++sa == SA) { sa = 0; pa ^= 1u; wrapped = true; }
       }
       if (*abort_flag) break;
     }
   } else if (aligned && warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
+    // One thread issues everything; the loop keeps its per-stage work to the
+    // two waits, eight MMAs and the commits (ring slots and phases as running
+    // counters; the token descriptor advances by addition in its address
+    // field, which counts 16-byte units: +2 per K16 step, +1024 per 16 KB
+    // atom; the weight operand is read from tensor memory, 8 columns per K16).
     if (lane == 0) {
-      long n = 0, acc_n = 0;
+      const uint32_t a_tmem0 = tmem + kAccCols;
+      const uint64_t b_desc0 = umma_desc_sw128(smem_u32(smem + OFF_B16));
+      int sa = 0, sb = 0;
+      uint32_t pa = 0, pb = 0;
+      long acc_n = 0;
       bool ok = true;
       for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const BigItem x = decode_item(it, J, slots, p.E);
         const int mblk = min(TB, x.rows - x.tb * TB);
         const uint32_t idesc = umma_idesc_f16(BM, (mblk + 15) & ~15);
-        int buf = 0;
-        for (int kb = 0; kb < n_kb && ok; ++kb, ++n) {
-          const int s16 = static_cast<int>(n % S16);
-          const long r16 = n / S16;
-          if (kb % CHUNK_KB == 0) {
-            buf = static_cast<int>(acc_n & 1);
-            if (acc_n >= 2) ok = mbar_wait_bounded(&acc_empty[buf], ((acc_n >> 1) - 1) & 1, abort_flag, status, site + 5);
+        uint32_t d_tmem = tmem;
+        int kc = 0;  // stage inside the current 1024-K chunk
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (kc == 0) {
+            const int buf = static_cast<int>(acc_n & 1);
+            d_tmem = tmem + buf * TB;
+            if (acc_n >= 2 &&
+                !mbar_wait_bounded(&acc_empty[buf], ((acc_n >> 1) - 1) & 1, abort_flag, status, site + 5)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
           }
-          if (ok) ok = mbar_wait_bounded(&cv_full[s16], r16 & 1, abort_flag, status, site + 6);
-          if (ok) ok = mbar_wait_bounded(&b_full[s16], r16 & 1, abort_flag, status, site + 7);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + OFF_A16 + s16 * F16_TILE);
-          const uint32_t b_base = smem_u32(smem + OFF_B16 + s16 * F16_TILE);
-#pragma unroll
-          for (int ks = 0; ks < KB / 16; ++ks) {
-            umma_f16(tmem + buf * TB, umma_desc_sw128(a_base + ks * 32), umma_desc_sw128(b_base + ks * 32), idesc,
-                     (kb % CHUNK_KB != 0 || ks > 0) ? 1u : 0u);
+          if (!mbar_wait_bounded(&a16_full[sa], pa, abort_flag, status, site + 6) ||
+              !mbar_wait_bounded(&b_full[sb], pb, abort_flag, status, site + 7)) {
+            ok = false;
+            break;
           }
-          umma_commit(&f16_empty[s16]);
-          if (kb % CHUNK_KB == CHUNK_KB - 1 || kb == n_kb - 1) {
-            umma_commit(&acc_full[buf]);
+          tc_fence_after();
+          const uint32_t at = a_tmem0 + sa * kAStageCols;  // 8 columns per K16 step
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>(sb * (F16_TILE >> 4));
+          constexpr uint64_t kAtom = F16_ATOM >> 4;
+          umma_f16_ts(d_tmem, at, bd, idesc, kc != 0 ? 1u : 0u);
+          umma_f16_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 32, bd + kAtom, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 40, bd + kAtom + 2, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
+          umma_commit(&a16_empty[sa]);
+          umma_commit(&b_empty[sb]);
+          if (++sa == SA) { sa = 0; pa ^= 1u; }
+          if (++sb == SB) { sb = 0; pb ^= 1u; }
+          if (++kc == CHUNK_KB || kb == n_kb - 1) {
+            umma_commit(&acc_full[acc_n & 1]);
             ++acc_n;
+            kc = 0;
           }
         }
       }
@@ -304,13 +380,13 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     const int q = warp & 3;                           // tensor-memory lane quadrant
     const int half = (warp - kEpiWarp0) >> 2;         // token columns [64 half, 64 half + 64)
     const int m = 32 * q + lane;                      // weight row inside the tile
+    const bool gate = lane < 16;                      // GEMM1: gate lane (else the matching up lane)
     const int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
     const float* xsc = ws_ptr<float>(p, p.L.x_scale);
     const float* xssc = p.share_uses_xq ? xsc : ws_ptr<float>(p, p.L.xs_scale);
     const float* s2 = ws_ptr<float>(p, p.L.s2);
     float* hbuf = ws_ptr<float>(p, p.L.hbuf);
     uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
-    float* xch = reinterpret_cast<float*>(smem + OFF_X);
     long acc_n = 0;
     for (long it = blockIdx.x; it < total; it += gridDim.x) {
       const BigItem x = decode_item(it, J, slots, p.E);
@@ -351,47 +427,44 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       consumer_sync();
       const bool stop = *abort_flag != 0;  // a failed wait raised it before this barrier
       if (!aligned) break;
-      int ng;
-      if (G1) ng = (m < 64) ? x.jt * 64 + m : p.I + x.jt * 64 + (m - 64);
-      else ng = x.jt * BM + m;
+      // GEMM1: output column of this lane's gate / up pair; GEMM2: output column
+      const int col = G1 ? x.jt * 64 + 16 * q + (lane & 15) : x.jt * BM + m;
       if (RAW) {
+        const int ng = G1 ? (gate ? col : p.I + col) : col;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
           const int tok = 64 * half + j;
           if (tok < mblk && ng < NW) raw[static_cast<size_t>(tok_row[tok]) * NW + ng] = acc[j];
         }
       } else if (G1) {
-        const float ws = (x.e >= 0 ? p.w1s + static_cast<size_t>(x.e) * NW : p.sw1s)[ng];
-        if (m >= 64) {
+        const float* w1s = x.e >= 0 ? p.w1s + static_cast<size_t>(x.e) * NW : p.sw1s;
+        const float wsg = w1s[col], wsu = w1s[p.I + col];
+        // the gate lane finishes tokens 0..31 of this half, its up partner 32..63
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int tok = 64 * half + j;
-            if (tok < mblk) xch[(m - 64) * XSTRIDE + tok] = __fmul_rn(__fmul_rn(__int2float_rn(acc[j]), ws), tok_scale[tok]);
-          }
-        }
-        consumer_sync();
-        if (m < 64) {
-#pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int tok = 64 * half + j;
-            if (tok < mblk) {
-              const float g = __fmul_rn(__fmul_rn(__int2float_rn(acc[j]), ws), tok_scale[tok]);
-              const float u = xch[m * XSTRIDE + tok];
-              const float d = __fadd_rn(1.0f, expf(-g));
-              hbuf[static_cast<size_t>(tok_row[tok]) * p.I + x.jt * 64 + m] = __fmul_rn(__fdiv_rn(g, d), u);
-            }
+        for (int j = 0; j < 32; ++j) {
+          const int send = gate ? acc[32 + j] : acc[j];
+          const int recv = __shfl_xor_sync(0xffffffffu, send, 16);
+          const int gi = gate ? acc[j] : recv;
+          const int ui = gate ? recv : acc[32 + j];
+          const int tok = 64 * half + (gate ? j : 32 + j);
+          if (tok < mblk) {
+            const float ts = tok_scale[tok];
+            const float g = __fmul_rn(__fmul_rn(__int2float_rn(gi), wsg), ts);
+            const float u = __fmul_rn(__fmul_rn(__int2float_rn(ui), wsu), ts);
+            const float d = __fadd_rn(1.0f, expf(-g));
+            hbuf[static_cast<size_t>(tok_row[tok]) * p.I + col] = __fmul_rn(__fdiv_rn(g, d), u);
           }
         }
       } else {
-        const float ws = (x.e >= 0 ? p.w2s + static_cast<size_t>(x.e) * NW : p.sw2s)[ng];
-        const bool valid_n = ng < p.h;
+        const float ws = (x.e >= 0 ? p.w2s + static_cast<size_t>(x.e) * NW : p.sw2s)[col];
+        const bool valid_n = col < p.h;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
           const int tok = 64 * half + j;
           if (tok < mblk && valid_n) {
             const uint16_t b = f32_to_bf16_bits(__fmul_rn(__fmul_rn(__int2float_rn(acc[j]), ws), tok_scale[tok]));
-            if (x.e >= 0) y2[static_cast<size_t>(tok_row[tok]) * p.h + ng] = b;
-            else p.sout[static_cast<size_t>(tok_tok[tok]) * p.h + ng] = b;
+            if (x.e >= 0) y2[static_cast<size_t>(tok_row[tok]) * p.h + col] = b;
+            else p.sout[static_cast<size_t>(tok_tok[tok]) * p.h + col] = b;
           }
         }
       }
