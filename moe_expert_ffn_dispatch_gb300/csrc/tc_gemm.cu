@@ -196,22 +196,26 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool aligned = (smem_u32(smem) & 1023u) == 0;
 
+  // The single-issuer roles (the two TMA producers and the MMA issuer) run
+  // their loops on the whole warp, so every address and descriptor is
+  // warp-uniform; one elected lane issues the copies and tensor-core work.
   if (aligned && warp == kWarpA) {
     // ---------------------------------------------------- weight TMA (int8)
-    if (lane == 0) {
-      const void* map = G1 ? &maps.a1 : &maps.a2;
-      const void* map_s = G1 ? &maps.a1s : &maps.a2s;
-      int s = 0;
-      uint32_t ph = 0;
-      bool wrapped = false;
-      for (long it = blockIdx.x; it < total; it += gridDim.x) {
-        const BigItem x = decode_item(it, J, slots, p.E);
-        const bool sh = x.e < 0;
-        const int rbase = sh ? 0 : x.e * NW;
-        const void* mp = sh ? map_s : map;
-        for (int kb = 0; kb < n_kb; ++kb) {
-          if (wrapped && !mbar_wait_bounded(&a8_empty[s], ph ^ 1u, abort_flag, status, site + 1, false))
-            goto done_a;
+    const void* map = G1 ? &maps.a1 : &maps.a2;
+    const void* map_s = G1 ? &maps.a1s : &maps.a2s;
+    int s = 0;
+    uint32_t ph = 0;
+    bool wrapped = false;
+    for (long it = blockIdx.x; it < total; it += gridDim.x) {
+      const BigItem x = decode_item(it, J, slots, p.E);
+      const bool sh = x.e < 0;
+      const int rbase = sh ? 0 : x.e * NW;
+      const void* mp = sh ? map_s : map;
+      for (int kb = 0; kb < n_kb; ++kb) {
+        if (wrapped &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(&a8_empty[s], ph ^ 1u, abort_flag, status, site + 1, false)))
+          goto done_a;
+        if (elect_one()) {
           mbar_arrive_expect_tx(&a8_full[s], A8_BYTES);
           char* dst = smem + OFF_A8 + s * A8_BYTES;
           if (G1) {
@@ -225,29 +229,31 @@ __global__ void __launch_bounds__(kBigThreads, 1)
           } else {
             tma_load_2d(dst, mp, kb * KB, rbase + x.jt * BM, &a8_full[s]);
           }
-          if (++s == S8) { s = 0; ph ^= 1u; wrapped = true; }
         }
+        __syncwarp();
+        if (++s == S8) { s = 0; ph ^= 1u; wrapped = true; }
       }
-    done_a:;
     }
+  done_a:;
   } else if (aligned && warp == kWarpB) {
     // ---------------------------------------------------- token TMA (f16)
-    if (lane == 0) {
-      const void* map = G1 ? &maps.b1 : &maps.b2;
-      const void* map_n = G1 ? &maps.b1n : &maps.b2n;
-      int s = 0;
-      uint32_t ph = 0;
-      bool wrapped = false;
-      for (long it = blockIdx.x; it < total; it += gridDim.x) {
-        const BigItem x = decode_item(it, J, slots, p.E);
-        const int r0 = x.row0 + x.tb * TB;
-        const int mblk = min(TB, x.rows - x.tb * TB);
-        // narrow boxes for short blocks: the MMA reads only the first mblk rows
-        const int nbox = mblk > 64 ? 1 : (mblk + kSmallBox - 1) / kSmallBox;
-        const uint32_t bytes = ATOMS * (mblk > 64 ? F16_ATOM : nbox * kSmallBox * KA * 2);
-        for (int kb = 0; kb < n_kb; ++kb) {
-          if (wrapped && !mbar_wait_bounded(&b_empty[s], ph ^ 1u, abort_flag, status, site + 2, false))
-            goto done_b;
+    const void* map = G1 ? &maps.b1 : &maps.b2;
+    const void* map_n = G1 ? &maps.b1n : &maps.b2n;
+    int s = 0;
+    uint32_t ph = 0;
+    bool wrapped = false;
+    for (long it = blockIdx.x; it < total; it += gridDim.x) {
+      const BigItem x = decode_item(it, J, slots, p.E);
+      const int r0 = x.row0 + x.tb * TB;
+      const int mblk = min(TB, x.rows - x.tb * TB);
+      // narrow boxes for short blocks: the MMA reads only the first mblk rows
+      const int nbox = mblk > 64 ? 1 : (mblk + kSmallBox - 1) / kSmallBox;
+      const uint32_t bytes = ATOMS * (mblk > 64 ? F16_ATOM : nbox * kSmallBox * KA * 2);
+      for (int kb = 0; kb < n_kb; ++kb) {
+        if (wrapped &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(&b_empty[s], ph ^ 1u, abort_flag, status, site + 2, false)))
+          goto done_b;
+        if (elect_one()) {
           mbar_arrive_expect_tx(&b_full[s], bytes);
           char* dst = smem + OFF_B16 + s * F16_TILE;
 #pragma unroll
@@ -260,11 +266,12 @@ __global__ void __launch_bounds__(kBigThreads, 1)
                 tma_load_2d(dst + a * F16_ATOM + b * kSmallBox * KA * 2, map_n, kx, r0 + b * kSmallBox, &b_full[s]);
             }
           }
-          if (++s == SB) { s = 0; ph ^= 1u; wrapped = true; }
         }
+        __syncwarp();
+        if (++s == SB) { s = 0; ph ^= 1u; wrapped = true; }
       }
-    done_b:;
     }
+  done_b:;
   } else if (aligned && warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
     // ------------------------------- int8 -> f16 weight rows, into tensor memory
     // Thread = weight row = tensor-memory lane (warp 4 + q owns lanes 32 q ..).
@@ -315,42 +322,40 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     }
   } else if (aligned && warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
-    // One thread issues everything; the loop keeps its per-stage work to the
-    // two waits, eight MMAs and the commits (ring slots and phases as running
-    // counters; the token descriptor advances by addition in its address
-    // field, which counts 16-byte units: +2 per K16 step, +1024 per 16 KB
-    // atom; the weight operand is read from tensor memory, 8 columns per K16).
-    if (lane == 0) {
-      const uint32_t a_tmem0 = tmem + kAccCols;
-      const uint64_t b_desc0 = umma_desc_sw128(smem_u32(smem + OFF_B16));
-      int sa = 0, sb = 0;
-      uint32_t pa = 0, pb = 0;
-      long acc_n = 0;
-      bool ok = true;
-      for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
-        const BigItem x = decode_item(it, J, slots, p.E);
-        const int mblk = min(TB, x.rows - x.tb * TB);
-        const uint32_t idesc = umma_idesc_f16(BM, (mblk + 15) & ~15);
-        uint32_t d_tmem = tmem;
-        int kc = 0;  // stage inside the current 1024-K chunk
-        for (int kb = 0; kb < n_kb; ++kb) {
-          if (kc == 0) {
-            const int buf = static_cast<int>(acc_n & 1);
-            d_tmem = tmem + buf * TB;
-            if (acc_n >= 2 &&
-                !mbar_wait_bounded(&acc_empty[buf], ((acc_n >> 1) - 1) & 1, abort_flag, status, site + 5)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
-          if (!mbar_wait_bounded(&a16_full[sa], pa, abort_flag, status, site + 6) ||
-              !mbar_wait_bounded(&b_full[sb], pb, abort_flag, status, site + 7)) {
-            ok = false;
-            break;
-          }
+    // Per stage: two waits, eight MMAs and the commits (ring slots and phases
+    // as running counters; the token descriptor advances by addition in its
+    // address field, which counts 16-byte units: +2 per K16 step, +1024 per
+    // 16 KB atom; the weight operand is read from tensor memory, 8 columns
+    // per K16 step).
+    const uint32_t a_tmem0 = tmem + kAccCols;
+    const uint64_t b_desc0 = umma_desc_sw128(smem_u32(smem + OFF_B16));
+    int sa = 0, sb = 0;
+    uint32_t pa = 0, pb = 0;
+    long acc_n = 0;
+    bool ok = true;
+    for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      const BigItem x = decode_item(it, J, slots, p.E);
+      const int mblk = min(TB, x.rows - x.tb * TB);
+      const uint32_t idesc = umma_idesc_f16(BM, (mblk + 15) & ~15);
+      uint32_t d_tmem = tmem;
+      int kc = 0;  // stage inside the current 1024-K chunk
+      for (int kb = 0; kb < n_kb; ++kb) {
+        if (kc == 0) {
+          const int buf = static_cast<int>(acc_n & 1);
+          d_tmem = tmem + buf * TB;
+          if (acc_n >= 2)
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_empty[buf], ((acc_n >> 1) - 1) & 1, abort_flag,
+                                                           status, site + 5));
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t at = a_tmem0 + sa * kAStageCols;  // 8 columns per K16 step
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a16_full[sa], pa, abort_flag, status, site + 6) &&
+                                         mbar_wait_bounded(&b_full[sb], pb, abort_flag, status, site + 7));
+        if (!ok) break;
+        tc_fence_after();
+        const bool last = (kc == CHUNK_KB - 1 || kb == n_kb - 1);
+        if (elect_one()) {
+          const uint32_t at = a_tmem0 + sa * kAStageCols;
           const uint64_t bd = b_desc0 + static_cast<uint64_t>(sb * (F16_TILE >> 4));
           constexpr uint64_t kAtom = F16_ATOM >> 4;
           umma_f16_ts(d_tmem, at, bd, idesc, kc != 0 ? 1u : 0u);
@@ -363,17 +368,19 @@ __global__ void __launch_bounds__(kBigThreads, 1)
           umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
           umma_commit(&a16_empty[sa]);
           umma_commit(&b_empty[sb]);
-          if (++sa == SA) { sa = 0; pa ^= 1u; }
-          if (++sb == SB) { sb = 0; pb ^= 1u; }
-          if (++kc == CHUNK_KB || kb == n_kb - 1) {
-            umma_commit(&acc_full[acc_n & 1]);
-            ++acc_n;
-            kc = 0;
-          }
+          if (last) umma_commit(&acc_full[acc_n & 1]);
+        }
+        __syncwarp();
+        if (++sa == SA) { sa = 0; pa ^= 1u; }
+        if (++sb == SB) { sb = 0; pb ^= 1u; }
+        if (last) {
+          ++acc_n;
+          kc = 0;
+        } else {
+          ++kc;
         }
       }
     }
-    __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
     const int ctid = threadIdx.x - kEpiWarp0 * 32;   // 0..255
