@@ -2,11 +2,13 @@
 //
 // Dispatch follows the FusedDeepMoE analysis §4.1 (local token counting into
 // expert_token_nums; for small batches a (bs+1) x E table whose prefix sums
-// give the expand index, §8.4).  On the GPU the table becomes a per-warp
-// count table built with __match_any_sync: one CTA walks the (t, k) pairs in
-// flat order, 1024 at a time, so every row's position inside its expert group
-// is its rank by flat index t*topk + k -- the same stable order a sequential
-// counting sort produces, with no atomics deciding the order.
+// give the expand index, §8.4).  On the GPU the table becomes a (warp,
+// expert) count table: each warp of one CTA ranks a contiguous segment of the
+// flat (t, k) order 32 pairs at a time (equal experts inside a step found by
+// one ballot per expert-id bit), and an exclusive prefix over the warps turns
+// segment ranks into group ranks, so every row's position inside its expert
+// group is its rank by flat index t*topk + k -- the same stable order a
+// sequential counting sort produces, with no atomics deciding the order.
 //
 // Both run in one launch: CTA 0 dispatches while the other CTAs quantise
 // (they are independent; the GEMM kernels join them).
@@ -30,37 +32,51 @@ constexpr int kQuantThreads = 256;
 constexpr float kAmaxEps = 1e-4f;
 
 // Exclusive scan of one int per thread over a 1024-thread block.
-__device__ int block_exclusive_scan(int v, int* total, int* s_warp) {
+template <typename T>
+__device__ T block_exclusive_scan(T v, T* total, T* s_warp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+  T incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    T y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = s_warp[lane];
-    int wi = w;
+    T w = s_warp[lane];
+    T wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, wi, o);
+      T y = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += y;
     }
     s_warp[lane] = wi;  // inclusive over warps
   }
   __syncthreads();
-  int excl = incl - v + (warp > 0 ? s_warp[warp - 1] : 0);
+  T excl = incl - v + (warp > 0 ? s_warp[warp - 1] : T(0));
   *total = s_warp[31];
   __syncthreads();
   return excl;
+}
+
+// Lanes of the warp whose key equals this lane's, for keys in [0, 2^nbits):
+// one ballot per key bit (the warp multi-split), far cheaper than match_any.
+__device__ __forceinline__ unsigned warp_peers(int key, int nbits) {
+  unsigned m = 0xffffffffu;
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (key >> b) & 1;
+    const unsigned bb = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? bb : ~bb;
+  }
+  return m;
 }
 
 // Dispatch by one 1024-thread CTA.  dsm: dynamic shared memory of
 // dispatch_smem_bytes(E).
 __device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
   __shared__ int s_warp[32];
+  __shared__ unsigned long long s_warp64[32];
   __shared__ int s_skipped;
   const int E = p.E, K = p.topk, bs = p.bs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -80,40 +96,63 @@ __device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
   if (tid == 0) s_skipped = 0;
   __syncthreads();
 
-  // 1. rank of every active, valid pair inside its expert group (flat order)
+  // 1. rank of every active, valid pair inside its expert group, stable in
+  //    the flat order: warp w ranks the contiguous segment [w seg, (w+1) seg)
+  //    of the flat (t, k) index 32 pairs at a time (match_any groups equal
+  //    experts; wcnt[w][e] keeps the warp's running count), then the
+  //    per-expert exclusive prefix over the warps turns (warp, rank) into the
+  //    rank inside the expert group.
   const int nf = bs * K;
-  for (int base = 0; base < nf; base += kDispatchThreads) {
-    const int f = base + tid;
-    int e = -1;
-    if (f < nf) {
-      const int t = f / K;
-      const bool act = (p.mask == nullptr) || (p.mask[t] != 0);
-      const int id = p.ids[f];
-      if (act) {
-        if (id >= 0 && id < E) e = id;
-        else atomicAdd(&s_skipped, 1);
+  const int seg = ((nf + 31) / 32 + 31) & ~31;  // pairs per warp, a multiple of 32
+  const int key_bits = 32 - __clz(E);            // keys 0..E (E = not routed)
+  const int f_begin = warp * seg, f_end = min(nf, (warp + 1) * seg);
+  for (int i = tid; i < 32 * E; i += kDispatchThreads) wcnt[i] = 0;
+  __syncthreads();
+  {
+    int32_t* mycnt = wcnt + warp * E;
+    for (int f0 = f_begin; f0 < f_end; f0 += 32 * 8) {
+      int ev[8];  // the ids of 8 steps are loaded before any is ranked
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int f = f0 + 32 * u + lane;
+        int e = E;
+        if (f < f_end) {
+          const int t = f / K;
+          const bool act = (p.mask == nullptr) || (p.mask[t] != 0);
+          const int id = p.ids[f];
+          if (act) {
+            if (id >= 0 && id < E) e = id;
+            else atomicAdd(&s_skipped, 1);
+          }
+        }
+        ev[u] = e;
       }
-      row_of[f] = -1;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (f0 + 32 * u >= f_end) break;  // warp-uniform
+        const int f = f0 + 32 * u + lane;
+        const int e = ev[u];
+        const unsigned peers = warp_peers(e, key_bits);
+        const int rank_w = __popc(peers & ((1u << lane) - 1u));
+        const int before = (e < E) ? mycnt[e] : 0;
+        __syncwarp();
+        if (f < f_end) row_of[f] = (e < E) ? before + rank_w : -1;
+        if (e < E && rank_w == 0) mycnt[e] = before + __popc(peers);
+        __syncwarp();
+      }
     }
-    for (int i = tid; i < 32 * E; i += kDispatchThreads) wcnt[i] = 0;
-    __syncthreads();
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank_w = __popc(peers & ((1u << lane) - 1u));
-    if (e >= 0 && rank_w == 0) wcnt[warp * E + e] = __popc(peers);
-    __syncthreads();
-    if (e >= 0) {
-      int pos = running[e] + rank_w;
-      for (int w = 0; w < warp; ++w) pos += wcnt[w * E + e];
-      row_of[f] = pos;  // rank inside the expert group; the offset is added below
-    }
-    __syncthreads();
-    for (int e2 = tid; e2 < E; e2 += kDispatchThreads) {
-      int s = 0;
-      for (int w = 0; w < 32; ++w) s += wcnt[w * E + e2];
-      running[e2] += s;
-    }
-    __syncthreads();
   }
+  __syncthreads();
+  if (tid < E) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int v = wcnt[w * E + tid];
+      wcnt[w * E + tid] = run;  // rows of expert tid in the segments before warp w
+      run += v;
+    }
+    running[tid] = run;
+  }
+  __syncthreads();
 
   // 2. counts -> exclusive offsets (E <= 1024: one expert per thread)
   const int c = tid < E ? running[tid] : 0;
@@ -128,16 +167,33 @@ __device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
   if (tid == 0) offsets[E] = R;
   __syncthreads();
 
-  // 3. final row index and its inverse
-  for (int f = tid; f < nf; f += kDispatchThreads) {
-    const int rank = row_of[f];
-    if (rank >= 0) {
-      const int r = running[p.ids[f]] + rank;
-      row_of[f] = r;
-      tk_of_row[r] = f;
-      row_token[r] = f / K;
+  // 3. final row index and its inverse: each warp walks its own segment
+  //    again (its ranks were written by the same lanes), 8 steps of loads at
+  //    a time before the writes.
+  {
+    const int32_t* mypre = wcnt + warp * E;
+    for (int f0 = f_begin; f0 < f_end; f0 += 32 * 8) {
+      int rk[8], ev[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int f = f0 + 32 * u + lane;
+        rk[u] = (f < f_end) ? row_of[f] : -1;
+        ev[u] = (f < f_end) ? p.ids[f] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (rk[u] >= 0) {
+          const int f = f0 + 32 * u + lane;
+          const int e = ev[u];
+          const int r = running[e] + mypre[e] + rk[u];
+          row_of[f] = r;
+          tk_of_row[r] = f;
+          row_token[r] = f / K;
+        }
+      }
     }
   }
+  __syncthreads();
 
   // 4. active tokens in ascending order (rows of the shared expert)
   int S = 0;
@@ -167,10 +223,19 @@ __device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
   const int is_small = (tid < E) && (c > 0) && (c <= p.small_rows);
   const int is_big = (tid < E) && (c > p.small_rows);
   const int nblk = is_big ? (c + kTokenBlock - 1) / kTokenBlock : 0;
-  int n_small = 0, n_big = 0, big_blk = 0;
-  const int si = block_exclusive_scan(is_small, &n_small, s_warp);
-  const int bi = block_exclusive_scan(is_big, &n_big, s_warp);
-  const int ki = block_exclusive_scan(nblk, &big_blk, s_warp);
+  // one scan of the three counters packed in 21-bit fields (each total < 2^21)
+  unsigned long long packed_total = 0;
+  const unsigned long long packed = block_exclusive_scan<unsigned long long>(
+      static_cast<unsigned long long>(is_small) | (static_cast<unsigned long long>(is_big) << 21) |
+          (static_cast<unsigned long long>(nblk) << 42),
+      &packed_total, s_warp64);
+  constexpr unsigned long long kField = (1ull << 21) - 1;
+  const int si = static_cast<int>(packed & kField);
+  const int bi = static_cast<int>((packed >> 21) & kField);
+  const int ki = static_cast<int>(packed >> 42);
+  int n_small = static_cast<int>(packed_total & kField);
+  int n_big = static_cast<int>((packed_total >> 21) & kField);
+  int big_blk = static_cast<int>(packed_total >> 42);
   if (is_small) {
     s_exp[si] = tid;
     s_row0[si] = off;

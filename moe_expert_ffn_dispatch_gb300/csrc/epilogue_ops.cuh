@@ -77,26 +77,38 @@ __device__ void requant_rows(const FwdParams& p, int r0, int n, float* s_red, in
   }
 }
 
-// Combine of token t, by the consumer threads (y2 through L2).
+// Combine of token t, by the consumer threads (y2 through L2): each thread
+// owns 8 output columns at a time, issues the loads of up to 8 expert rows
+// before using any, and adds the terms in ascending k (fp32, each product and
+// each sum rounded once, from 0.0f).
 __device__ void combine_token(const FwdParams& p, int t, int ctid) {
   const int h = p.h, K = p.topk, n8 = h >> 3;
-  const int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
+  const int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of) + static_cast<size_t>(t) * K;
+  const float* scales = p.scales + static_cast<size_t>(t) * K;
   const uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
   uint4* out = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * h);
   for (int i = ctid; i < n8; i += kConsumers) {
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int k = 0; k < K; ++k) {
-      const int r = row_of[t * K + k];
-      if (r < 0) continue;
-      const float sc = p.scales[t * K + k];
-      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(y2 + static_cast<size_t>(r) * h) + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int k0 = 0; k0 < K; k0 += 8) {
+      int r[8];
+      uint4 v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float f = bf16_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
-        acc[j] = __fadd_rn(acc[j], __fmul_rn(f, sc));
+      for (int u = 0; u < 8; ++u) {
+        r[u] = (k0 + u < K) ? row_of[k0 + u] : -1;
+        if (r[u] >= 0) v[u] = __ldcg(reinterpret_cast<const uint4*>(y2 + static_cast<size_t>(r[u]) * h) + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (r[u] < 0) continue;
+        const float sc = scales[k0 + u];
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float f = bf16_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
+          acc[j] = __fadd_rn(acc[j], __fmul_rn(f, sc));
+        }
       }
     }
     uint32_t o[4];

@@ -503,6 +503,7 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
   const int8_t* xq = ws_ptr<int8_t>(p, p.L.x_q);
   const int8_t* xsq = p.share_uses_xq ? xq : ws_ptr<int8_t>(p, p.L.xs_q);
   __half* x1h = ws_ptr<__half>(p, p.L.x1h);
+  __shared__ int s_tok[TB];
   const int n16 = p.h >> 4;
   for (int b = blockIdx.x; b < total; b += gridDim.x) {
     int lo = 0, hi = n_slots - 1;  // slot of block b
@@ -515,15 +516,30 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
     const int r0 = s_row0[lo] + tb * TB;
     const int n = min(TB, s_rows[lo] - tb * TB);
     const int8_t* src = s_exp[lo] >= 0 ? xq : xsq;
-    for (int idx = threadIdx.x; idx < n * n16; idx += blockDim.x) {
-      const int i = idx / n16, c = idx % n16;
-      const int r = r0 + i;
-      const uint4 v = reinterpret_cast<const uint4*>(src + static_cast<size_t>(row_token[r]) * p.h)[c];
-      uint4 lo16, hi16;
-      int8x16_to_f16(v, lo16, hi16);
-      uint4* dst = reinterpret_cast<uint4*>(x1h + static_cast<size_t>(r) * p.h) + 2 * c;
-      dst[0] = lo16;
-      dst[1] = hi16;
+    __syncthreads();  // the previous block's readers are done with s_tok
+    if (threadIdx.x < n) s_tok[threadIdx.x] = row_token[r0 + threadIdx.x];
+    __syncthreads();
+    // four independent 16-byte loads in flight per thread
+    const int tasks = n * n16;
+    for (int base = threadIdx.x; base < tasks; base += 4 * blockDim.x) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * blockDim.x;
+        if (idx < tasks)
+          v[u] = reinterpret_cast<const uint4*>(src + static_cast<size_t>(s_tok[idx / n16]) * p.h)[idx % n16];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * blockDim.x;
+        if (idx < tasks) {
+          uint4 lo16, hi16;
+          int8x16_to_f16(v[u], lo16, hi16);
+          uint4* dst = reinterpret_cast<uint4*>(x1h + static_cast<size_t>(r0 + idx / n16) * p.h) + 2 * (idx % n16);
+          dst[0] = lo16;
+          dst[1] = hi16;
+        }
+      }
     }
   }
 }
@@ -638,7 +654,7 @@ cudaError_t moe_gemm_big_prepare_attributes() {
 cudaError_t launch_expand(const FwdParams& p, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas), dim3(256), 0, s, attr);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 4), dim3(256), 0, s, attr);
   return cudaLaunchKernelEx(&cfg, expand_kernel, p);
 }
 
