@@ -136,38 +136,73 @@ SMALL_ROWS = 8  # experts with at most this many rows run in the weight-streamin
 
 
 def algorithmic_bytes(wl, counts_per_expert, n_active):
-    """Bytes each kernel must move at least once (the roofline numerator).
+    """Bytes (and int ops) each kernel must handle at least once: the roofline numerator.
 
     Per touched expert (routed experts with >= 1 row, plus the shared expert
-    when it has rows) GEMM1 reads W1 (2I*h int8) and its scales (2I fp32);
-    per row it reads the row's x_q (h bytes), writes h (I fp32), and its fused
-    requant reads h back and writes x2 (I) and s2.  GEMM2 reads W2 (h*I int8)
-    and scales (h fp32); per row x2 and s2 in, a bf16 row of h out, and the
-    fused combine reads each routed row once more and writes bf16 outputs.
-    Experts with at most SMALL_ROWS rows (when h, I <= 4096) run in the *_small
-    kernels, the others in the tensor-core *_big kernels.  The step total
-    counts weights once plus the block's own inputs and outputs."""
+    when it has rows) GEMM1 reads W1 (2I*h int8) and its scales (2I fp32) and
+    GEMM2 reads W2 (h*I int8) and its scales (h fp32).  Activations count at
+    the sizes the method defines, once per kernel that consumes or produces
+    them; scratch round trips (the fp32 h read back by a fused requant, y2 read
+    back by a fused combine, f16 operand copies) are not algorithmic.
+      gemm1_small  W1 + m*(h x_q in + I x2 out + 4 s2 out)      (requant fused)
+      gemm1_big    W1 + m*(h x_q in + 4I h out)
+      requant_big  m*(4I h in + I x2 out + 4 s2 out)
+      gemm2_small  W2 + m*(I + 4 in) + 2h per shared row, + 2h*bs out when it combines
+      gemm2_big    W2 + m*(I + 4 in + 2h y2 out)
+      combine      2h per routed row in + 2h*bs out
+    Experts with at most SMALL_ROWS rows (when h, I <= 4096) run in the
+    *_small kernels, the others in the tensor-core *_big kernels.  The step
+    total counts weights once plus the block's own inputs and outputs."""
     h, I, K, bs = wl.hidden, wl.inter, wl.topk, wl.bs
     small_ok = h <= 4096 and I <= 4096
     groups = [(c, True) for c in counts_per_expert if c > 0]
-    R = sum(counts_per_expert)
     shared = n_active if (wl.has_shared and n_active > 0) else 0
     if shared:
         groups.append((shared, False))
-    out = {"gemm1_small": 0, "gemm1_big": 0, "gemm2_small": 0, "gemm2_big": 0}
+    keys = ["gemm1_small", "gemm1_big", "gemm2_small", "gemm2_big", "requant_big", "combine"]
+    out = {k: 0 for k in keys}
+    ops = {k: 0 for k in keys}
+    any_big = False
     for m, routed in groups:
-        sfx = "small" if (small_ok and m <= SMALL_ROWS) else "big"
-        out["gemm1_" + sfx] += 2 * I * h + 8 * I + m * (h + 4 * I + 4 * I + I + 4)
-        out["gemm2_" + sfx] += h * I + 4 * h + m * (I + 4 + 2 * h) + (m * 2 * h if routed else 0)
-    out["gemm2_small" if small_ok else "gemm2_big"] += bs * 2 * h  # combined outputs
+        small = small_ok and m <= SMALL_ROWS
+        any_big |= not small
+        if small:
+            out["gemm1_small"] += 2 * I * h + 8 * I + m * (h + I + 4)
+            out["gemm2_small"] += h * I + 4 * h + m * (I + 4) + (0 if routed else m * 2 * h)
+        else:
+            out["gemm1_big"] += 2 * I * h + 8 * I + m * (h + 4 * I)
+            out["requant_big"] += m * (4 * I + I + 4)
+            out["gemm2_big"] += h * I + 4 * h + m * (I + 4 + 2 * h)
+        g = "small" if small else "big"
+        ops["gemm1_" + g] += 2 * m * 2 * I * h
+        ops["gemm2_" + g] += 2 * m * h * I
+    routed_rows = sum(m for m, r in groups if r)
+    if any_big:
+        out["combine"] += routed_rows * 2 * h + bs * 2 * h
+    else:
+        out["gemm2_small"] += bs * 2 * h  # the small GEMM2 combines every token
     touched = len(groups)
     rows = sum(m for m, _ in groups)
     out["step"] = touched * (2 * I * h + h * I + 4 * (2 * I + h)) + bs * h * 2 + bs * K * 8 + \
         bs * h * 2 * (2 if wl.has_shared else 1) + wl.num_experts * 4
     out["int_ops"] = 2 * rows * (2 * I * h + h * I)
+    out["ops"] = ops
     out["touched_experts"] = touched
     out["rows"] = rows
     return out
+
+
+def roofline_of(bytes_, ops, seconds, peaks):
+    """Bound = the larger of T_mem (bytes at the measured HBM copy rate) and
+    T_ops (int ops at the measured dense bf16 rate: the exact int8 products run
+    as f16 codes on the tensor cores, whose f16 rate equals the bf16 rate)."""
+    t_mem = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    t_ops = ops / (peaks["bf16_tflops"] * 1e12)
+    if t_ops > t_mem:
+        return {"bound": "tensor", "achieved": ops / seconds / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": t_ops / seconds}
+    return {"bound": "hbm", "achieved": bytes_ / seconds / 1e9, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": t_mem / seconds}
 
 
 KERNEL_SOURCES = {"gemm1_small": "moe_gemm.cu", "gemm2_small": "moe_gemm.cu",
@@ -290,7 +325,7 @@ def run_ours(args, wl, ws, rank, local):
     dom = max(KERNEL_SOURCES, key=lambda k: ktimes[k][0])
     d_ms, d_n = ktimes[dom]
     d_avg_s = d_ms / max(d_n, 1) / 1e3
-    achieved = alg[dom] / d_avg_s / 1e9
+    roof = roofline_of(alg[dom], alg["ops"][dom], d_avg_s, peaks)
     traffic = recorded_traffic(dom, wl.name)
     step_s = ms_total / args.steps / 1e3
     tokens = wl.bs * ws
@@ -313,14 +348,13 @@ def run_ours(args, wl, ws, rank, local):
                    "touched_experts": alg["touched_experts"], "rows": alg["rows"],
                    "l2": "inputs larger than L2 (%.2f GB of touched weights per step vs 0.13 GB L2)" % (alg["step"] / 1e9),
                    "parallelism": "replicas x%d (independent batches, no collective)" % ws},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic, "peak_kind": peak_kind,
-                     "alg_bytes_per_launch": alg[dom], "avg_launch_us": d_avg_s * 1e6,
+        "roofline": {**roof, "traffic": traffic, "kernel": dom, "peak_kind": peak_kind,
+                     "alg_bytes_per_launch": alg[dom], "int_ops_per_launch": alg["ops"][dom],
+                     "avg_launch_us": d_avg_s * 1e6,
                      "timing": "CUDA events around each launch, second pass of the same %d forwards "
                                "(%.1f us per forward instrumented)" % (args.steps, ms_instrumented / args.steps * 1e3)},
-        "roofline_step": {"bound": "hbm", "alg_bytes": alg["step"], "achieved": alg["step"] / step_s / 1e9,
-                          "frac": alg["step"] / step_s / 1e9 / peaks["hbm_gbs"], "unit": "GB/s"},
+        "roofline_step": {**roofline_of(alg["step"], alg["int_ops"], ms_total / args.steps / 1e3, peaks),
+                          "alg_bytes": alg["step"], "int_ops": alg["int_ops"]},
         "kernels_us": {k: (v[0] / max(v[1], 1) * 1e3) for k, v in ktimes.items()},
         "gpu_launches": launches,
         "e2e": {"value": tokens * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
