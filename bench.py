@@ -210,6 +210,44 @@ KERNEL_SOURCES = {"gemm1_small": "moe_gemm.cu", "gemm2_small": "moe_gemm.cu",
 
 
 # ---------------------------------------------------------------- our arm
+# ---------------------------------------------------------------- replicas
+def rank_workload(wl, rank):
+    """The batch rank `rank` runs: same shapes and weights, its own token draw
+    (the path shards by independent batches; there is no data-path collective)."""
+    return synth.Workload(**{**wl.__dict__, "seed": wl.seed + 7919 * rank})
+
+
+def max_over_ranks(x, device="cpu"):
+    """The slowest rank's value (the job ends when the last replica does)."""
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(wl, alg, ws):
+    return {"workload": wl.name, "bs": wl.bs, "hidden": wl.hidden, "experts": wl.num_experts,
+            "topk": wl.topk, "inter": wl.inter, "shared_expert": wl.has_shared,
+            "touched_experts": alg["touched_experts"], "rows": alg["rows"],
+            "l2": "inputs larger than L2 (%.2f GB of touched weights per step vs 0.13 GB L2)" % (alg["step"] / 1e9),
+            "parallelism": "replicas x%d (independent batches, no collective)" % ws}
+
+
+def host_alg(wl):
+    """algorithmic_bytes from the seeded routing, computed on the host."""
+    inp = synth.make_inputs(wl, with_weights=False)
+    act = torch.ones(wl.bs, dtype=torch.bool) if inp.mask is None else inp.mask.bool()
+    ids = inp.expert_ids[act].flatten()
+    ids = ids[(ids >= 0) & (ids < wl.num_experts)]
+    counts = torch.bincount(ids.long(), minlength=wl.num_experts).tolist()
+    return algorithmic_bytes(wl, counts, int(act.sum()))
+
+
+def whole_job_tokens_per_s(bs, world_size, steps, seconds):
+    """Tokens all ranks processed divided by the (max-over-ranks) time."""
+    return bs * world_size * steps / seconds
+
+
 def run_ours(args, wl, ws, rank, local):
     import moe_expert_ffn_dispatch_gb300 as m
 
@@ -218,8 +256,7 @@ def run_ours(args, wl, ws, rank, local):
     if ws > 1:
         torch.distributed.init_process_group("nccl")
     # each rank runs its own batch (seed + rank) through the same replicated weights
-    wl_r = synth.Workload(**{**wl.__dict__, "seed": wl.seed + 7919 * rank})
-    inp = synth.make_inputs(wl_r, with_weights=False)
+    inp = synth.make_inputs(rank_workload(wl, rank), with_weights=False)
     base = synth.make_inputs(wl, with_weights=False)
     weights = {"w1": synth.draw_all_w1(wl, dev), "w1_scale": base.w1_scale.to(dev),
                "w2": synth.draw_all_w2(wl, dev), "w2_scale": base.w2_scale.to(dev)}
@@ -266,10 +303,7 @@ def run_ours(args, wl, ws, rank, local):
     ms_total = e0.elapsed_time(e1)
     if blk.status()["rc"] != 0:
         raise RuntimeError("device status after the timed loop: %s" % blk.status())
-    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
 
     # ---- per-kernel durations: a second pass of the same K forwards with CUDA
     # events around every launch on the launch stream (events between the
@@ -315,10 +349,7 @@ def run_ours(args, wl, ws, rank, local):
         e2e_step()
     t1 = time.perf_counter()
     barrier()
-    te = torch.tensor([t1 - t0], dtype=torch.float64, device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_s = float(te.item())
+    e2e_s = max_over_ranks(t1 - t0, dev)
 
     peaks, peak_kind = measured_peaks()
     # dominant kernel: the GEMM kernel with the most time in the timed region
@@ -331,7 +362,7 @@ def run_ours(args, wl, ws, rank, local):
     tokens = wl.bs * ws
     res = {
         "metric": METRIC,
-        "value": tokens * args.steps / (ms_total / 1e3),
+        "value": whole_job_tokens_per_s(wl.bs, ws, args.steps, ms_total / 1e3),
         "unit": "tokens/s",
         "n_gpus": ws,
         "steps": args.steps,
@@ -343,11 +374,7 @@ def run_ours(args, wl, ws, rank, local):
         "vs_baseline": None,
         "dtype": "int8",
         "data": "synthetic (seeded counter-hash inputs, random-init int8 weights)",
-        "config": {"workload": wl.name, "bs": wl.bs, "hidden": wl.hidden, "experts": wl.num_experts,
-                   "topk": wl.topk, "inter": wl.inter, "shared_expert": wl.has_shared,
-                   "touched_experts": alg["touched_experts"], "rows": alg["rows"],
-                   "l2": "inputs larger than L2 (%.2f GB of touched weights per step vs 0.13 GB L2)" % (alg["step"] / 1e9),
-                   "parallelism": "replicas x%d (independent batches, no collective)" % ws},
+        "config": workload_config(wl, alg, ws),
         "roofline": {**roof, "traffic": traffic, "kernel": dom, "peak_kind": peak_kind,
                      "alg_bytes_per_launch": alg[dom], "int_ops_per_launch": alg["ops"][dom],
                      "avg_launch_us": d_avg_s * 1e6,
@@ -357,7 +384,8 @@ def run_ours(args, wl, ws, rank, local):
                           "alg_bytes": alg["step"], "int_ops": alg["int_ops"]},
         "kernels_us": {k: (v[0] / max(v[1], 1) * 1e3) for k, v in ktimes.items()},
         "gpu_launches": launches,
-        "e2e": {"value": tokens * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_tokens_per_s(wl.bs, ws, e2e_steps, e2e_s), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "clocks": clk.summary(),
     }
@@ -421,7 +449,8 @@ def run_reference(args, wl, ws, rank):
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
-            "data": "synthetic", "config": {"workload": wl.name, "bs": wl.bs},
+            "data": "synthetic (seeded counter-hash inputs, random-init int8 weights)",
+            "config": workload_config(wl, host_alg(wl), ws),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": "one token of %s per step (its %d routed rows + shared row)" % (wl.name, wl.topk)},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
