@@ -78,7 +78,10 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
   take(L.x_scale, bs * 4, moe::kRegXScale);
   take(L.xs_q, c.has_shared ? bs * h : 0, moe::kRegXsq);
   take(L.xs_scale, c.has_shared ? bs * 4 : 0, moe::kRegXsScale);
-  const size_t hbytes = rows * I * 4, ybytes = routed * h * 2;
+  // h rows are 2I floats wide: the tensor-core GEMM1 stores the dequantised
+  // gate and up halves there for the requant kernel, the dp4a GEMM1 stores h
+  // in the first I
+  const size_t hbytes = rows * 2 * I * 4, ybytes = routed * h * 2;
   take(L.hbuf, hbytes > ybytes ? hbytes : ybytes, moe::kRegH);
   take(L.x2, rows * I, moe::kRegX2);
   take(L.s2, rows * 4, moe::kRegS2);

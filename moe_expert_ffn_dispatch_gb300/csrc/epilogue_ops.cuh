@@ -39,7 +39,7 @@ __device__ void requant_rows(const FwdParams& p, int r0, int n, float* s_red, in
   const int lane = ctid & 31, warp = ctid >> 5;
   for (int i = 0; i < n; ++i) {
     const int r = r0 + i;
-    const float4* hr = reinterpret_cast<const float4*>(hbuf + static_cast<size_t>(r) * I);
+    const float4* hr = reinterpret_cast<const float4*>(hbuf + static_cast<size_t>(r) * (2 * I));
     float amax = 0.0f;
     for (int c = ctid; c < n4; c += kConsumers) {
       const float4 v = __ldcg(hr + c);

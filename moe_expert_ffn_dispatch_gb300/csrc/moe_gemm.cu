@@ -353,7 +353,7 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
           const float g = ytile[j * MT + t];
           const float u = ytile[(BN / 2 + j) * MT + t];
           const float d = __fadd_rn(1.0f, expf(-g));
-          hbuf[static_cast<size_t>(info_row[is * MT + t]) * p.I + jt * (BN / 2) + j] =
+          hbuf[static_cast<size_t>(info_row[is * MT + t]) * (2 * p.I) + jt * (BN / 2) + j] =
               __fmul_rn(__fdiv_rn(g, d), u);
         }
       } else {

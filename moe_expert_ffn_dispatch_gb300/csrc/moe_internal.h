@@ -35,7 +35,7 @@ struct WsLayout {
   size_t x_scale;    // [bs_max] f32
   size_t xs_q;       // [bs_max, h] int8 (shared-expert quant)
   size_t xs_scale;   // [bs_max] f32
-  size_t hbuf;       // [rows, I] f32  (aliased by y2)
+  size_t hbuf;       // [rows, 2I] f32: h in [0, I) (dp4a path) or g | u (tensor-core path); aliased by y2
   size_t x2;         // [rows, I] int8
   size_t s2;         // [rows] f32
   size_t y2;         // [bs_max*topk, h] bf16 (== hbuf)

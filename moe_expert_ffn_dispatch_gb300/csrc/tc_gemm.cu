@@ -20,15 +20,15 @@
 // (TMA write + converter read) and the f16 token stage (TMA write + MMA read).  For
 // GEMM1 the 128 rows are 64 gate rows and the 64 matching up rows, laid out
 // so that each 32-lane quadrant of tensor memory holds 16 gate rows in its
-// lanes 0..15 and the 16 matching up rows in lanes 16..31: SwiGLU pairs meet
-// inside one warp and swap halves with a shuffle.
+// lanes 0..15 and the 16 matching up rows in lanes 16..31 (every warp
+// store then covers one 64-byte run of gate and one of up values).
 // The requant of big blocks and the combine of forwards with big blocks run
 // as separate parallel kernels (below): done by the CTA that finishes a block
 // last, they would serialise 128-row blocks and 128-token tiles on a few SMs.
 // Warp roles (one CTA per SM, persistent):
 // A stage is 128 of K: two 64-wide atoms of the 128-byte swizzle per f16 tile.
-//   warp 0      TMA of the int8 weight boxes into a 4-deep staging ring
-//   warp 2      TMA of the f16 token boxes (128-byte swizzle) into a 3-deep
+//   warp 0      TMA of the int8 weight boxes into a 6-deep staging ring
+//   warp 2      TMA of the f16 token boxes (128-byte swizzle) into a 4-deep
 //               ring; 16-row boxes when the block has at most 64 rows
 //   warps 4..7  convert int8 weight stages to f16, one weight row per
 //               thread, into a 4-deep ring in tensor memory (the MMA's A
@@ -37,7 +37,9 @@
 //               K16) into two tensor-memory accumulators, alternating per
 //               1024 of K, and commits to the ring and accumulator barriers
 //   warps 8..15 drain accumulators (tcgen05.ld) into int32, then the
-//               epilogue; two warps per tensor-memory lane quadrant
+//               epilogue (GEMM1: dequantised gate | up values, SwiGLU
+//               being applied by the requant kernel; GEMM2: bf16 dequant);
+//               two warps per tensor-memory lane quadrant
 // All rings are mbarrier full/empty pairs (the FIFO of the Mega-MoE
 // analysis §4); every wait is bounded.
 #include <cuda_fp16.h>
@@ -56,9 +58,9 @@ constexpr int KB = 128;               // K elements per stage
 constexpr int KA = 64;                // K elements per swizzle atom (one 128-byte f16 row)
 constexpr int ATOMS = KB / KA;        // swizzle atoms per f16 stage
 constexpr int CHUNK_KB = 1024 / KB;   // stages per exact accumulation chunk (1024 of K)
-constexpr int S8 = 8;                 // int8 weight staging ring (from HBM)
+constexpr int S8 = 6;                 // int8 weight staging ring (from HBM)
 constexpr int SA = 4;                 // f16 weight ring in tensor memory (converted in the CTA)
-constexpr int SB = 3;                 // f16 token ring (from L2)
+constexpr int SB = 4;                 // f16 token ring (from L2)
 constexpr int kAccCols = 2 * TB;      // two fp32 accumulators of TB columns
 constexpr int kAStageCols = KB / 2;   // one f16 weight stage: 128 lanes x 64 columns of f16 pairs
 constexpr int kTmemCols = 512;        // kAccCols + SA * kAStageCols, rounded to a power of two
@@ -292,15 +294,18 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         if (ok) {
           tc_fence_after();
           const char* src = smem + OFF_A8 + s8 * A8_BYTES + row * KB;
+          // all eight loads first: the tensor-memory stores below are
+          // ordered asm statements that later loads cannot move above
+          uint4 c[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) c[j] = *reinterpret_cast<const uint4*>(src + ((j ^ (row & 7)) << 4));
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t v[32];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-              const int j = 4 * h2 + jj;
-              const uint4 c = *reinterpret_cast<const uint4*>(src + ((j ^ (row & 7)) << 4));
               uint4 lo, hi;
-              int8x16_to_f16(c, lo, hi);
+              int8x16_to_f16(c[4 * h2 + jj], lo, hi);
               v[8 * jj + 0] = lo.x; v[8 * jj + 1] = lo.y; v[8 * jj + 2] = lo.z; v[8 * jj + 3] = lo.w;
               v[8 * jj + 4] = hi.x; v[8 * jj + 5] = hi.y; v[8 * jj + 6] = hi.z; v[8 * jj + 7] = hi.w;
             }
@@ -322,11 +327,16 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     }
   } else if (aligned && warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
-    // Per stage: two waits, eight MMAs and the commits (ring slots and phases
-    // as running counters; the token descriptor advances by addition in its
-    // address field, which counts 16-byte units: +2 per K16 step, +1024 per
-    // 16 KB atom; the weight operand is read from tensor memory, 8 columns
-    // per K16 step).
+    // Two 128-K stages per iteration (one at the end of an odd count): wait
+    // for both stages' operands, then one elected lane issues their sixteen
+    // MMAs and the commits.  The issuing warp's fixed cost per iteration is
+    // several hundred cycles, so pairing stages halves it per unit of tensor
+    // work.  Pairs never straddle a 1024-K chunk (CHUNK_KB is even).  Ring
+    // slots and phases are running counters; the token descriptor advances
+    // by addition in its address field (16-byte units: +2 per K16 step,
+    // +1024 per 16 KB atom); the weight operand is read from tensor memory,
+    // 8 columns per K16 step.
+    static_assert(CHUNK_KB % 2 == 0, "stage pairs must not straddle an accumulation chunk");
     const uint32_t a_tmem0 = tmem + kAccCols;
     const uint64_t b_desc0 = umma_desc_sw128(smem_u32(smem + OFF_B16));
     int sa = 0, sb = 0;
@@ -339,45 +349,81 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       const uint32_t idesc = umma_idesc_f16(BM, (mblk + 15) & ~15);
       uint32_t d_tmem = tmem;
       int kc = 0;  // stage inside the current 1024-K chunk
-      for (int kb = 0; kb < n_kb; ++kb) {
+      for (int kb = 0; kb < n_kb; kb += 2) {
+        const bool pair = kb + 1 < n_kb;
         if (kc == 0) {
           const int buf = static_cast<int>(acc_n & 1);
           d_tmem = tmem + buf * TB;
-          if (acc_n >= 2)
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_empty[buf], ((acc_n >> 1) - 1) & 1, abort_flag,
-                                                           status, site + 5));
-          if (!ok) break;
-          tc_fence_after();
+          if (acc_n >= 2 &&
+              !__all_sync(0xffffffffu, mbar_wait_bounded(&acc_empty[buf], ((acc_n >> 1) - 1) & 1, abort_flag,
+                                                         status, site + 5))) {
+            ok = false;
+            break;
+          }
         }
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a16_full[sa], pa, abort_flag, status, site + 6) &&
-                                         mbar_wait_bounded(&b_full[sb], pb, abort_flag, status, site + 7));
-        if (!ok) break;
+        const int sa1 = sa + 1 == SA ? 0 : sa + 1, sb1 = sb + 1 == SB ? 0 : sb + 1;
+        const uint32_t pa1 = sa + 1 == SA ? pa ^ 1u : pa, pb1 = sb + 1 == SB ? pb ^ 1u : pb;
+        bool w = mbar_wait_bounded(&a16_full[sa], pa, abort_flag, status, site + 6) &&
+                 mbar_wait_bounded(&b_full[sb], pb, abort_flag, status, site + 7);
+        if (pair)
+          w = w && mbar_wait_bounded(&a16_full[sa1], pa1, abort_flag, status, site + 6) &&
+              mbar_wait_bounded(&b_full[sb1], pb1, abort_flag, status, site + 7);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const bool last = (kc == CHUNK_KB - 1 || kb == n_kb - 1);
+        const int nst = pair ? 2 : 1;
+        const bool last = (kc + nst == CHUNK_KB || kb + nst >= n_kb);
         if (elect_one()) {
-          const uint32_t at = a_tmem0 + sa * kAStageCols;
-          const uint64_t bd = b_desc0 + static_cast<uint64_t>(sb * (F16_TILE >> 4));
           constexpr uint64_t kAtom = F16_ATOM >> 4;
-          umma_f16_ts(d_tmem, at, bd, idesc, kc != 0 ? 1u : 0u);
-          umma_f16_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 32, bd + kAtom, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 40, bd + kAtom + 2, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
-          umma_commit(&a16_empty[sa]);
-          umma_commit(&b_empty[sb]);
+          {
+            const uint32_t at = a_tmem0 + sa * kAStageCols;
+            const uint64_t bd = b_desc0 + static_cast<uint64_t>(sb * (F16_TILE >> 4));
+            umma_f16_ts(d_tmem, at, bd, idesc, kc != 0 ? 1u : 0u);
+            umma_f16_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 32, bd + kAtom, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 40, bd + kAtom + 2, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
+            umma_commit(&a16_empty[sa]);
+            umma_commit(&b_empty[sb]);
+          }
+          if (pair) {
+            const uint32_t at = a_tmem0 + sa1 * kAStageCols;
+            const uint64_t bd = b_desc0 + static_cast<uint64_t>(sb1 * (F16_TILE >> 4));
+            umma_f16_ts(d_tmem, at, bd, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 32, bd + kAtom, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 40, bd + kAtom + 2, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
+            umma_commit(&a16_empty[sa1]);
+            umma_commit(&b_empty[sb1]);
+          }
           if (last) umma_commit(&acc_full[acc_n & 1]);
         }
         __syncwarp();
-        if (++sa == SA) { sa = 0; pa ^= 1u; }
-        if (++sb == SB) { sb = 0; pb ^= 1u; }
+        if (pair) {
+          sa = sa1 + 1 == SA ? 0 : sa1 + 1;
+          pa = sa1 + 1 == SA ? pa1 ^ 1u : pa1;
+          sb = sb1 + 1 == SB ? 0 : sb1 + 1;
+          pb = sb1 + 1 == SB ? pb1 ^ 1u : pb1;
+        } else {
+          sa = sa1;
+          pa = pa1;
+          sb = sb1;
+          pb = pb1;
+        }
         if (last) {
           ++acc_n;
           kc = 0;
         } else {
-          ++kc;
+          kc += nst;
         }
       }
     }
@@ -444,23 +490,19 @@ __global__ void __launch_bounds__(kBigThreads, 1)
           if (tok < mblk && ng < NW) raw[static_cast<size_t>(tok_row[tok]) * NW + ng] = acc[j];
         }
       } else if (G1) {
+        // dequantised gate (lanes 0..15) or up (lanes 16..31) value of every
+        // token, into the row's gate | up halves; the requant kernel applies
+        // SwiGLU (a long expf / divide chain that would otherwise hold this
+        // epilogue, and with it the accumulators, for most of an item)
         const float* w1s = x.e >= 0 ? p.w1s + static_cast<size_t>(x.e) * NW : p.sw1s;
-        const float wsg = w1s[col], wsu = w1s[p.I + col];
-        // the gate lane finishes tokens 0..31 of this half, its up partner 32..63
+        const int ncol = gate ? col : p.I + col;
+        const float ws = w1s[ncol];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int send = gate ? acc[32 + j] : acc[j];
-          const int recv = __shfl_xor_sync(0xffffffffu, send, 16);
-          const int gi = gate ? acc[j] : recv;
-          const int ui = gate ? recv : acc[32 + j];
-          const int tok = 64 * half + (gate ? j : 32 + j);
-          if (tok < mblk) {
-            const float ts = tok_scale[tok];
-            const float g = __fmul_rn(__fmul_rn(__int2float_rn(gi), wsg), ts);
-            const float u = __fmul_rn(__fmul_rn(__int2float_rn(ui), wsu), ts);
-            const float d = __fadd_rn(1.0f, expf(-g));
-            hbuf[static_cast<size_t>(tok_row[tok]) * p.I + col] = __fmul_rn(__fdiv_rn(g, d), u);
-          }
+        for (int j = 0; j < 64; ++j) {
+          const int tok = 64 * half + j;
+          if (tok < mblk)
+            hbuf[static_cast<size_t>(tok_row[tok]) * (2 * p.I) + ncol] =
+                __fmul_rn(__fmul_rn(__int2float_rn(acc[j]), ws), tok_scale[tok]);
         }
       } else {
         const float ws = (x.e >= 0 ? p.w2s + static_cast<size_t>(x.e) * NW : p.sw2s)[col];
@@ -544,11 +586,41 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
   }
 }
 
-// Requant of the rows of big blocks (FusedDeepMoE analysis §7.2), one warp
-// per row: amax = max(max|h|, 1e-4), s2 = amax * (1/127),
+// SwiGLU and requant of the rows of big blocks (FusedDeepMoE analysis §6.1
+// and §7.2), one warp per row: h = (g / (1 + exp(-g))) * u from the row's
+// dequantised gate | up halves, amax = max(max|h|, 1e-4), s2 = amax * (1/127),
 // q = RNE((h * 127) * (1/amax)); writes the int8 codes, their f16 copy (the
-// tensor-core GEMM2 operand) and s2.
-__global__ void __launch_bounds__(256) requant_big_kernel(FwdParams p) {
+// tensor-core GEMM2 operand) and s2.  Rows up to I = 2048 keep h in shared
+// memory between the two passes; longer rows recompute it in the second.
+__device__ __forceinline__ float swiglu_1(float g, float u) {
+  const float d = __fadd_rn(1.0f, expf(-g));
+  return __fmul_rn(__fdiv_rn(g, d), u);
+}
+__device__ __forceinline__ float4 swiglu_4(float4 g, float4 u) {
+  return make_float4(swiglu_1(g.x, u.x), swiglu_1(g.y, u.y), swiglu_1(g.z, u.z), swiglu_1(g.w, u.w));
+}
+__device__ __forceinline__ void quant_store4(float4 v, float inv, int c, uint32_t* q4, __half2* h2) {
+  const float f[4] = {v.x, v.y, v.z, v.w};
+  int8_t q[4];
+  uint32_t packed = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    q[j] = f32_to_q(__fmul_rn(__fmul_rn(f[j], 127.0f), inv));
+    packed |= static_cast<uint32_t>(static_cast<uint8_t>(q[j])) << (8 * j);
+  }
+  q4[c] = packed;
+  h2[2 * c] = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
+  h2[2 * c + 1] = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
+}
+__device__ __forceinline__ float amax4(float a, float4 v) {
+  return fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+}
+
+constexpr int kRqWarps = 8;          // rows in flight per CTA (one per warp)
+constexpr int kRqMaxI = 2048;        // rows up to this I keep h in shared memory
+
+__global__ void __launch_bounds__(kRqWarps * 32) requant_big_kernel(FwdParams p) {
+  extern __shared__ float4 rq_smem[];  // [kRqWarps][I / 4] when I <= kRqMaxI
   grid_dependency_wait();
   grid_launch_dependents();
   const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
@@ -560,13 +632,15 @@ __global__ void __launch_bounds__(256) requant_big_kernel(FwdParams p) {
   const int32_t* s_blk = s_rows + st;
   const int n_slots = slots[SlotTable::kNumBig];
   const int I = p.I, n4 = I >> 2;
+  const bool staged = I <= kRqMaxI;
   const float* hbuf = ws_ptr<float>(p, p.L.hbuf);
   int8_t* x2 = ws_ptr<int8_t>(p, p.L.x2);
   __half* x2h = ws_ptr<__half>(p, p.L.x2h);
   float* s2 = ws_ptr<float>(p, p.L.s2);
-  const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int nw = gridDim.x * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  float4* hrow = rq_smem + wid * (kRqMaxI / 4);
+  const int gw = blockIdx.x * kRqWarps + wid;
+  const int nw = gridDim.x * kRqWarps;
   const long nrows = static_cast<long>(total) * TB;  // block-major row slots (some empty)
   for (long g = gw; g < nrows; g += nw) {
     const int b = static_cast<int>(g / TB), i = static_cast<int>(g % TB);
@@ -579,32 +653,43 @@ __global__ void __launch_bounds__(256) requant_big_kernel(FwdParams p) {
     const int tb = b - s_blk[lo];
     if (tb * TB + i >= s_rows[lo]) continue;
     const int r = s_row0[lo] + tb * TB + i;
-    const float4* hr = reinterpret_cast<const float4*>(hbuf + static_cast<size_t>(r) * I);
+    const float4* gr = reinterpret_cast<const float4*>(hbuf + static_cast<size_t>(r) * (2 * I));
+    const float4* ur = gr + n4;
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(x2 + static_cast<size_t>(r) * I);
+    __half2* h2 = reinterpret_cast<__half2*>(x2h + static_cast<size_t>(r) * I);
+    // pass 1: h = SwiGLU(g, u) (into shared memory when the row fits) and amax;
+    // four g / u pairs of loads in flight per lane before any is used
     float amax = 0.0f;
-    for (int c = lane; c < n4; c += 32) {
-      const float4 v = hr[c];
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    for (int c0 = lane; c0 < n4; c0 += 4 * 32) {
+      float4 gv[4], uv[4];
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const int c = c0 + 32 * u4;
+        if (c < n4) {
+          gv[u4] = __ldcs(gr + c);
+          uv[u4] = __ldcs(ur + c);
+        }
+      }
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const int c = c0 + 32 * u4;
+        if (c < n4) {
+          const float4 hv = swiglu_4(gv[u4], uv[u4]);
+          amax = amax4(amax, hv);
+          if (staged) hrow[c] = hv;
+        }
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if (amax < 1e-4f) amax = 1e-4f;
     const float inv = __fdiv_rn(1.0f, amax);
-    uint32_t* q4 = reinterpret_cast<uint32_t*>(x2 + static_cast<size_t>(r) * I);
-    __half2* h2 = reinterpret_cast<__half2*>(x2h + static_cast<size_t>(r) * I);
+    // pass 2: codes (h from shared memory, or recomputed for long rows)
     for (int c = lane; c < n4; c += 32) {
-      const float4 v = hr[c];
-      const float f[4] = {v.x, v.y, v.z, v.w};
-      int8_t q[4];
-      uint32_t packed = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        q[j] = f32_to_q(__fmul_rn(__fmul_rn(f[j], 127.0f), inv));
-        packed |= static_cast<uint32_t>(static_cast<uint8_t>(q[j])) << (8 * j);
-      }
-      q4[c] = packed;
-      h2[2 * c] = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
-      h2[2 * c + 1] = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
+      const float4 hv = staged ? hrow[c] : swiglu_4(gr[c], ur[c]);
+      quant_store4(hv, inv, c, q4, h2);
     }
+    __syncwarp();  // this warp's h row is reused by its next row
     if (lane == 0) s2[r] = __fmul_rn(amax, 1.0f / 127.0f);
   }
 }
@@ -628,7 +713,8 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdParams p) {
 cudaError_t launch_requant_big(const FwdParams& p, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 4), dim3(256), 0, s, attr);
+  const size_t smem = p.I <= kRqMaxI ? static_cast<size_t>(kRqWarps) * kRqMaxI * sizeof(float) : 0;
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 3), dim3(kRqWarps * 32), smem, s, attr);
   return cudaLaunchKernelEx(&cfg, requant_big_kernel, p);
 }
 
@@ -648,7 +734,9 @@ cudaError_t moe_gemm_big_prepare_attributes() {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
   }
-  return cudaSuccess;
+  return cudaFuncSetAttribute(reinterpret_cast<const void*>(requant_big_kernel),
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kRqWarps * kRqMaxI * sizeof(float)));
 }
 
 cudaError_t launch_expand(const FwdParams& p, cudaStream_t s) {

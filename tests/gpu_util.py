@@ -95,6 +95,9 @@ def assert_rel(got: torch.Tensor, ref: torch.Tensor, rel: float, what: str):
         raise AssertionError("%s: element %d got %r want %r" % (what, i, float(g.view(-1)[i]), float(r.view(-1)[i])))
 
 
+SMALL_ROWS = 8  # experts with at most this many rows take the dp4a path (when h, I <= 4096)
+
+
 def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
     """Run one forward on the GPU and check every stage against the oracle.
     Returns (block, oracle result)."""
@@ -139,11 +142,39 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
             assert torch.equal(region(blk, "xs_q", torch.int8, (bs, h))[act], ref["xs_q"][act])
             assert torch.equal(region(blk, "xs_scale", torch.float32, (bs,))[act], ref["xs_scale"][act])
         rows = bs * K + (bs if wl.has_shared else 0)
-        # SwiGLU output h (fp32, exp ulps)
-        hb = staged_h.view(torch.float32)[:rows * I].view(rows, I)
-        assert_rel(hb[:R], ref["h"], H_REL, "h routed")
+        # GEMM1 outputs, rows 2I floats wide.  Rows of experts with at most
+        # SMALL_ROWS rows (dp4a path) hold the SwiGLU output h in [0, I):
+        # fp32 within exp ulps of the oracle.  Rows of the other experts
+        # (tensor-core path) hold the dequantised gate | up values, which must
+        # equal fp32 (float(acc1) * w_scale) * x_scale of the oracle's exact
+        # int32 accumulators bit for bit (SwiGLU is applied by the requant
+        # kernel, whose x2 / s2 are checked below).
+        hb = staged_h.view(torch.float32)[:rows * 2 * I].view(rows, 2 * I)
+        small_ok = h <= 4096 and I <= 4096
+        counts = ref["expert_token_nums"].tolist()
+        big_row = torch.zeros(R, dtype=torch.bool)
+        e_of_row = torch.zeros(R, dtype=torch.long)
+        off = 0
+        for e, c in enumerate(counts):
+            big_row[off:off + c] = (not small_ok) or c > SMALL_ROWS
+            e_of_row[off:off + c] = e
+            off += c
+        t_of_row = ref["tk_of_row"].long() // K
+        if (~big_row).any():
+            assert_rel(hb[:R][~big_row, :I], ref["h"][~big_row], H_REL, "h routed (dp4a rows)")
+        if big_row.any():
+            w1s = inp.w1_scale.to(torch.float32)
+            acc = ref["acc1"][big_row].to(torch.float32)
+            want = (acc * w1s[e_of_row[big_row]]) * ref["x_scale"][t_of_row[big_row]].view(-1, 1)
+            assert torch.equal(hb[:R][big_row], want), "gate | up routed (tensor-core rows)"
         if S:
-            assert_rel(hb[bs * K:bs * K + S], ref["share_h"][act], H_REL, "h shared")
+            if small_ok and S <= SMALL_ROWS:
+                assert_rel(hb[bs * K:bs * K + S, :I], ref["share_h"][act], H_REL, "h shared")
+            else:
+                xs_sh = ref["xs_scale"][act]  # the shared expert's own quant (its smooth vector)
+                acc = ref["share_acc1"][act].to(torch.float32)
+                want = (acc * inp.share_w1_scale.to(torch.float32).view(1, -1)) * xs_sh.view(-1, 1)
+                assert torch.equal(hb[bs * K:bs * K + S], want), "gate | up shared (tensor-core rows)"
         # requant
         x2 = region(blk, "x2", torch.int8, (rows, I))
         s2 = region(blk, "s2", torch.float32, (rows,))
