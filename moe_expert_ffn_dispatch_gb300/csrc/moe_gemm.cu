@@ -328,47 +328,52 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
 
     // lane (rr * MT + t) receives the dot product of row rr of this warp with token t
     const int mine = warp_reduce_scatter32(acc, lane);
-    {
-      const int rr = lane / MT, t = lane % MT;
-      const int nl = kRowsPerWarp * warp + rr;  // row inside the item
-      int ng;
-      if (G1) ng = (nl < BN / 2) ? jt * (BN / 2) + nl : p.I + jt * (BN / 2) + (nl - BN / 2);
-      else ng = jt * BN + nl;
-      if (RAW) {
-        if (t < m) raw[static_cast<size_t>(info_row[is * MT + t]) * NW + ng] = mine;
-      } else {
-        const float* wsc = G1 ? (cur.e >= 0 ? p.w1s + static_cast<size_t>(cur.e) * NW : p.sw1s)
-                              : (cur.e >= 0 ? p.w2s + static_cast<size_t>(cur.e) * NW : p.sw2s);
-        float y = 0.0f;
-        if (t < m) y = __fmul_rn(__fmul_rn(__int2float_rn(mine), wsc[ng]), info_scale[is * MT + t]);
-        ytile[nl * MT + t] = y;
+    const int rr = lane / MT, t = lane % MT;
+    const int nl = kRowsPerWarp * warp + rr;  // row inside the item
+    int ng;
+    if (G1) ng = (nl < BN / 2) ? jt * (BN / 2) + nl : p.I + jt * (BN / 2) + (nl - BN / 2);
+    else ng = jt * BN + nl;
+    // the abort flag is read only right after a CTA-wide barrier, so that
+    // every consumer thread leaves the loop at the same item
+    bool stop = false;
+    if (RAW) {
+      if (t < m) raw[static_cast<size_t>(info_row[is * MT + t]) * NW + ng] = mine;
+      consumer_sync();
+      stop = *abort_flag != 0;
+    } else if (G1) {
+      // gate and up rows of a column sit in different warps: meet in shared memory
+      const float* wsc = cur.e >= 0 ? p.w1s + static_cast<size_t>(cur.e) * NW : p.sw1s;
+      float y = 0.0f;
+      if (t < m) y = __fmul_rn(__fmul_rn(__int2float_rn(mine), wsc[ng]), info_scale[is * MT + t]);
+      ytile[nl * MT + t] = y;
+      consumer_sync();
+      stop = *abort_flag != 0;
+      if (ctid < (BN / 2) * m) {
+        const int tt = ctid / (BN / 2), j = ctid % (BN / 2);
+        const float g = ytile[j * MT + tt];
+        const float u = ytile[(BN / 2 + j) * MT + tt];
+        const float d = __fadd_rn(1.0f, expf(-g));
+        hbuf[static_cast<size_t>(info_row[is * MT + tt]) * (2 * p.I) + jt * (BN / 2) + j] =
+            __fmul_rn(__fdiv_rn(g, d), u);
+      }
+    } else {
+      // GEMM2: each lane owns one (row, token) result and stores it straight
+      // away: no shared-memory staging, no CTA barrier per item
+      if (t < m) {
+        const float* wsc = cur.e >= 0 ? p.w2s + static_cast<size_t>(cur.e) * NW : p.sw2s;
+        const uint16_t b =
+            f32_to_bf16_bits(__fmul_rn(__fmul_rn(__int2float_rn(mine), wsc[ng]), info_scale[is * MT + t]));
+        if (cur.e >= 0) y2[static_cast<size_t>(info_row[is * MT + t]) * p.h + ng] = b;
+        else p.sout[static_cast<size_t>(info_tok[is * MT + t]) * p.h + ng] = b;
       }
     }
-    consumer_sync();
-    const bool stop = *abort_flag != 0;
     if (!RAW) {
-      if (G1) {
-        if (ctid < (BN / 2) * m) {
-          const int t = ctid / (BN / 2), j = ctid % (BN / 2);
-          const float g = ytile[j * MT + t];
-          const float u = ytile[(BN / 2 + j) * MT + t];
-          const float d = __fadd_rn(1.0f, expf(-g));
-          hbuf[static_cast<size_t>(info_row[is * MT + t]) * (2 * p.I) + jt * (BN / 2) + j] =
-              __fmul_rn(__fdiv_rn(g, d), u);
-        }
-      } else {
-        if (ctid < BN * m) {
-          const int t = ctid / BN, j = ctid % BN;
-          const uint16_t b = f32_to_bf16_bits(ytile[j * MT + t]);
-          if (cur.e >= 0) y2[static_cast<size_t>(info_row[is * MT + t]) * p.h + jt * BN + j] = b;
-          else p.sout[static_cast<size_t>(info_tok[is * MT + t]) * p.h + jt * BN + j] = b;
-        }
-      }
       // report once per run of this CTA's items on one expert
       ++run_items;
       if (run_end) {
         __threadfence();
         consumer_sync();
+        if (!G1) stop = *abort_flag != 0;
         if (G1) gemm1_item_done(p, cur.slot, J, run_items, cur.row0, m, s_flag, s_red, ctid, false);
         else if (!has_big) gemm2_item_done(p, cur.e >= 0, m, info_tok + is * MT, BN * run_items, s_tok, ctid);
         run_items = 0;
