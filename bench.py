@@ -135,7 +135,7 @@ class ClockSampler:
 SMALL_ROWS = 8  # experts with at most this many rows run in the weight-streaming kernels
 
 
-def algorithmic_bytes(wl, counts_per_expert, n_active):
+def algorithmic_bytes(wl, counts_per_expert, n_active, unfused=False):
     """Bytes (and int ops) each kernel must handle at least once: the roofline numerator.
 
     Per touched expert (routed experts with >= 1 row, plus the shared expert
@@ -150,11 +150,12 @@ def algorithmic_bytes(wl, counts_per_expert, n_active):
       gemm2_small  W2 + m*(I + 4 in) + 2h per shared row, + 2h*bs out when it combines
       gemm2_big    W2 + m*(I + 4 in + 2h y2 out)
       combine      2h per routed row in + 2h*bs out
-    Experts with at most SMALL_ROWS rows (when h, I <= 4096) run in the
-    *_small kernels, the others in the tensor-core *_big kernels.  The step
+    Experts with at most SMALL_ROWS rows (when h, I <= 4096 and the forward
+    is not the unfused A/B chain) run in the *_small kernels, the others in
+    the tensor-core *_big kernels.  The step
     total counts weights once plus the block's own inputs and outputs."""
     h, I, K, bs = wl.hidden, wl.inter, wl.topk, wl.bs
-    small_ok = h <= 4096 and I <= 4096
+    small_ok = h <= 4096 and I <= 4096 and not unfused
     groups = [(c, True) for c in counts_per_expert if c > 0]
     shared = n_active if (wl.has_shared and n_active > 0) else 0
     if shared:
@@ -271,7 +272,8 @@ def run_ours(args, wl, ws, rank, local):
     if inp.mask is not None:
         di["mask"] = inp.mask.to(dev)
 
-    blk = m.MoeFused(wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter, wl.has_shared, dev)
+    blk = m.MoeFused(wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter, wl.has_shared, dev,
+                     unfused=getattr(args, "unfused", False))
     stream = torch.cuda.current_stream(dev)
     out, sout, nums = blk.forward_inputs(di, weights)
     torch.cuda.synchronize()
@@ -280,7 +282,7 @@ def run_ours(args, wl, ws, rank, local):
         raise RuntimeError("forward status %s" % st)
     counts = nums.cpu().tolist()
     n_active = int(inp.mask.sum()) if inp.mask is not None else wl.bs
-    alg = algorithmic_bytes(wl, counts, n_active)
+    alg = algorithmic_bytes(wl, counts, n_active, unfused=getattr(args, "unfused", False))
 
     def barrier():
         if ws > 1:
@@ -374,7 +376,7 @@ def run_ours(args, wl, ws, rank, local):
         "vs_baseline": None,
         "dtype": "int8",
         "data": "synthetic (seeded counter-hash inputs, random-init int8 weights)",
-        "config": workload_config(wl, alg, ws),
+        "config": {**workload_config(wl, alg, ws), **({"unfused": True} if getattr(args, "unfused", False) else {})},
         "roofline": {**roof, "traffic": traffic, "kernel": dom, "peak_kind": peak_kind,
                      "alg_bytes_per_launch": alg[dom], "int_ops_per_launch": alg["ops"][dom],
                      "avg_launch_us": d_avg_s * 1e6,
@@ -465,6 +467,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="MOE_FLAG_UNFUSED: the unfused chain (tensor-core GEMMs, separate requant and combine) "
+                         "as an A/B baseline")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the workload's expert count (smaller cases for profiler captures)")
     args = ap.parse_args()

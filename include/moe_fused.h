@@ -49,8 +49,17 @@ extern "C" {
 /* Static shape of one block.  Limits: 1 <= hidden, inter <= 16384 and both
  * multiples of 64; 1 <= num_experts <= 1024; 1 <= topk <= min(num_experts, 16);
  * 0 <= bs_max <= 65536.  GEMM1 has N = 2*inter outputs (gate rows 0..inter-1,
- * up rows inter..2*inter-1); GEMM2 maps inter -> hidden.  `flags` is reserved
- * and must be 0.  The pages' supported ranges (§9.4) are not enforced. */
+ * up rows inter..2*inter-1); GEMM2 maps inter -> hidden.  `flags` is 0 or
+ * MOE_FLAG_UNFUSED; other bits are reserved (MOE_ERR_INVALID_ARG).  The
+ * pages' supported ranges (§9.4) are not enforced. */
+
+/* Every expert takes the tensor-core path with separate requant and combine
+ * kernels: the unfused chain (FusedDeepMoE analysis §9.3, the "SmallOps"
+ * sequence of dispatch+quant, GEMM1, requant, GEMM2, combine) kept as an A/B
+ * baseline for the fused weight-streaming path that experts with at most 8
+ * rows take by default.  Results are the same either way (the same
+ * operations in the same order). */
+#define MOE_FLAG_UNFUSED 1
 typedef struct {
   int32_t bs_max;
   int32_t hidden;

@@ -30,6 +30,10 @@ MOE_ERR_DEVICE_TIMEOUT = -5
 MOE_ERR_UNIMPLEMENTED = -6
 MOE_ERR_ALIGNMENT = -7
 
+# config flag: every expert on the tensor-core path with separate requant and
+# combine kernels (the unfused A/B baseline); results are the same
+FLAG_UNFUSED = 1
+
 KERNEL_NAMES = ["dispatch_quant", "expand", "gemm1_small", "gemm1_big", "requant_big", "gemm2_small", "gemm2_big",
                 "combine"]
 KERNEL_ID = {n: i for i, n in enumerate(KERNEL_NAMES)}
@@ -209,13 +213,14 @@ class MoeFused:
     """
 
     def __init__(self, bs_max: int, hidden: int, num_experts: int, topk: int, inter: int,
-                 has_shared: bool, device=None):
+                 has_shared: bool, device=None, unfused: bool = False):
         self.device = torch.device(device if device is not None else "cuda")
         if self.device.type != "cuda":
             raise ValueError("the fused MoE block runs on a CUDA device only")
         if self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
-        self.cfg = Config(bs_max, hidden, num_experts, topk, inter, int(bool(has_shared)), 0)
+        self.cfg = Config(bs_max, hidden, num_experts, topk, inter, int(bool(has_shared)),
+                          FLAG_UNFUSED if unfused else 0)
         with torch.cuda.device(self.device):
             rc, self.handle, self.workspace_bytes = moe_fused_create(self.cfg)
         if rc:

@@ -47,9 +47,9 @@ def device_weights(inp, dev):
     return w
 
 
-def make_block(wl, dev, bs_max=None):
+def make_block(wl, dev, bs_max=None, unfused=False):
     return m.MoeFused(bs_max if bs_max is not None else wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter,
-                      wl.has_shared, dev)
+                      wl.has_shared, dev, unfused=unfused)
 
 
 def region(blk, name, dtype, shape=None):
@@ -150,7 +150,7 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
         # int32 accumulators bit for bit (SwiGLU is applied by the requant
         # kernel, whose x2 / s2 are checked below).
         hb = staged_h.view(torch.float32)[:rows * 2 * I].view(rows, 2 * I)
-        small_ok = h <= 4096 and I <= 4096
+        small_ok = h <= 4096 and I <= 4096 and not (blk.cfg.flags & m.FLAG_UNFUSED)
         counts = ref["expert_token_nums"].tolist()
         big_row = torch.zeros(R, dtype=torch.bool)
         e_of_row = torch.zeros(R, dtype=torch.long)

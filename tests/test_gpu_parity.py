@@ -90,3 +90,17 @@ def test_bs_zero():
     torch.cuda.synchronize()
     assert nums.cpu().tolist() == [0, 0, 0, 0]
     assert blk.status()["dispatched_rows"] == 0
+
+
+UNFUSED_CASES = [CASES[0], CASES[1], CASES[6]]
+
+
+@pytest.mark.parametrize("wl", UNFUSED_CASES, ids=lambda w: w.name)
+def test_unfused_chain_staged_parity(wl):
+    """MOE_FLAG_UNFUSED: every expert (even with 1-8 rows) on the tensor-core
+    GEMMs with the separate requant and combine kernels, against the same
+    oracle and tolerances."""
+    inp = synth.make_inputs(wl)
+    blk = make_block(wl, DEV, unfused=True)
+    blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True, blk=blk)
+    check_raw_accumulators(blk, inp, ref, di, dw, DEV)
