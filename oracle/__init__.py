@@ -47,7 +47,7 @@ class OracleArgs(ctypes.Structure):
                 ("w1", P), ("w1_scale", P), ("w2", P), ("w2_scale", P),
                 ("share_w1", P), ("share_w1_scale", P), ("share_w2", P), ("share_w2_scale", P),
                 ("smooth", P), ("share_smooth", P), ("mask", P), ("token_sample", P),
-                ("threads", I32)]
+                ("threads", I32), ("fold_routing", I32)]
 
 
 class OracleOut(ctypes.Structure):
@@ -189,13 +189,15 @@ def bf16_round(v: float) -> int:
 
 # ------------------------------------------------------------- full block
 def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tensor] = None,
-            threads: Optional[int] = None, expert_weights=None) -> Dict:
+            threads: Optional[int] = None, expert_weights=None, fold_routing: bool = False) -> Dict:
     """Run the whole block on the CPU.
 
     `inp` is a synth.MoeInputs (CPU tensors; weights may be absent, in which
     case the experts that active pairs select are redrawn one by one).
     `token_sample` (bool [bs]) restricts the GEMM work and the outputs to those
-    tokens; dispatch still runs on every token.  Returns a dict of tensors
+    tokens; dispatch still runs on every token.  `fold_routing` selects the
+    mode in which each routed row's routing weight is folded into its GEMM2
+    row scale and the combine is a plain sum.  Returns a dict of tensors
     (bf16 outputs as bf16 tensors).
     """
     wl = inp.wl
@@ -253,7 +255,7 @@ def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tenso
     a = OracleArgs(bs, h, E, K, I, int(shared), _ptr(x), _ptr(ids), _ptr(sc),
                    ctypes.addressof(w1p), _ptr(w1s), ctypes.addressof(w2p), _ptr(w2s),
                    _ptr(sw1), _ptr(sw1s), _ptr(sw2), _ptr(sw2s), _ptr(smooth), _ptr(ssmooth),
-                   _ptr(mask), _ptr(samp), threads)
+                   _ptr(mask), _ptr(samp), threads, int(bool(fold_routing)))
 
     res = {}
     res["output"] = torch.zeros(bs, h, dtype=torch.int16)

@@ -199,6 +199,23 @@ void oracle_combine_token(int H, int topk, const uint16_t* const* rows, const fl
   }
 }
 
+/* Routing weight folded into the GEMM2 row scale (the DeepSeek-V4 decode
+ * case study, §2.3: the per-row dequant scale and the routing weight fused
+ * into one row scale computed once per row).  Row r of pair (t, k) gets
+ * y2'[j] = bf16_rne((float(acc2[j]) * w2s[j]) * (s2 * s_k)), and the combine
+ * is the plain sum: out[c] = bf16_rne(sum_k float(y2'_k[c])), from 0.0f, k
+ * ascending. */
+void oracle_combine_token_folded(int H, int topk, const uint16_t* const* rows, uint16_t* out) {
+  for (int c = 0; c < H; ++c) {
+    float sum = 0.0f;
+    for (int k = 0; k < topk; ++k) {
+      if (!rows[k]) continue;
+      sum = sum + bf16_to_f32(rows[k][c]);
+    }
+    out[c] = f32_to_bf16(sum);
+  }
+}
+
 /* ------------------------------------------------------ whole forward -- */
 typedef struct {
   int32_t bs, hidden, num_experts, topk, inter, has_shared;
@@ -218,6 +235,7 @@ typedef struct {
   const uint8_t* mask;               /* [bs] or NULL */
   const uint8_t* token_sample;       /* [bs] or NULL: compute outputs only where nonzero */
   int32_t threads;
+  int32_t fold_routing;              /* 0: default; 1: routing weight folded into the row scale */
 } oracle_args_t;
 
 typedef struct {
@@ -260,9 +278,12 @@ typedef struct {
   int rc;
 } work_t;
 
-/* one routed or shared row: GEMM1 -> SwiGLU -> requant -> GEMM2 -> dequant */
+/* one routed or shared row: GEMM1 -> SwiGLU -> requant -> GEMM2 -> dequant;
+ * route_scale (non-NULL only for routed rows in the folded mode) multiplies
+ * the requant scale once before the GEMM2 dequant */
 static int expert_row(int h, int I, const int8_t* xrow, float xscale,
                       const int8_t* w1, const float* w1s, const int8_t* w2, const float* w2s,
+                      const float* route_scale,
                       int32_t* acc1_out, float* h_out, int8_t* x2_out, float* s2_out,
                       int32_t* acc2_out, uint16_t* y_out) {
   int32_t* acc1 = (int32_t*)malloc(sizeof(int32_t) * (size_t)(2 * I));
@@ -277,7 +298,7 @@ static int expert_row(int h, int I, const int8_t* xrow, float xscale,
     rc = oracle_gemm_row(h, I, q2, w2, acc2);
   }
   if (rc == 0) {
-    oracle_dequant_bf16_row(h, acc2, w2s, s2, y_out);
+    oracle_dequant_bf16_row(h, acc2, w2s, route_scale ? s2 * (*route_scale) : s2, y_out);
     if (acc1_out) memcpy(acc1_out, acc1, sizeof(int32_t) * (size_t)(2 * I));
     if (h_out) memcpy(h_out, hv, sizeof(float) * (size_t)I);
     if (x2_out) memcpy(x2_out, q2, (size_t)I);
@@ -309,6 +330,7 @@ static void* worker(void* p) {
       if (!a->w1[e] || !a->w2[e]) { w->rc = -2; break; }
       w->rc = expert_row(h, I, w->xq + (size_t)t * h, w->xsc[t],
                          a->w1[e], a->w1_scale + (size_t)e * 2 * I, a->w2[e], a->w2_scale + (size_t)e * h,
+                         a->fold_routing ? a->expert_scales + f : NULL,
                          o->acc1 ? o->acc1 + (size_t)i * 2 * I : NULL,
                          o->h_act ? o->h_act + (size_t)i * I : NULL,
                          o->x2 ? o->x2 + (size_t)i * I : NULL,
@@ -321,7 +343,7 @@ static void* worker(void* p) {
       if (a->token_sample && !a->token_sample[i]) continue;
       if (!active) { memset(so, 0, sizeof(uint16_t) * (size_t)h); continue; }
       w->rc = expert_row(h, I, w->sq + (size_t)i * h, w->ssc[i],
-                         a->share_w1, a->share_w1_scale, a->share_w2, a->share_w2_scale,
+                         a->share_w1, a->share_w1_scale, a->share_w2, a->share_w2_scale, NULL,
                          o->share_acc1 ? o->share_acc1 + (size_t)i * 2 * I : NULL,
                          o->share_h ? o->share_h + (size_t)i * I : NULL,
                          o->share_x2 ? o->share_x2 + (size_t)i * I : NULL,
@@ -338,7 +360,8 @@ static void* worker(void* p) {
         int r = w->row_of[i * K + k];
         rows[k] = r >= 0 ? w->y2 + (size_t)r * h : NULL;
       }
-      oracle_combine_token(h, K, rows, a->expert_scales + (size_t)i * K, out);
+      if (a->fold_routing) oracle_combine_token_folded(h, K, rows, out);
+      else oracle_combine_token(h, K, rows, a->expert_scales + (size_t)i * K, out);
     }
   }
   return NULL;

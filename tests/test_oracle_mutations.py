@@ -32,6 +32,9 @@ MUTANTS = [
     ("dequant_drops_token_scale", "float g = ((float)acc1[j] * w1s[j]) * x_scale;",
      "float g = ((float)acc1[j] * w1s[j]);"),
     ("bf16_truncation", "u += 0x7FFFu + lsb;", "u += 0;"),
+    ("folded_weight_dropped", "route_scale ? s2 * (*route_scale) : s2", "s2"),
+    ("folded_weight_twice", "      sum = sum + bf16_to_f32(rows[k][c]);",
+     "      sum = sum + bf16_to_f32(rows[k][c]) * 0.5f;"),
 ]
 
 

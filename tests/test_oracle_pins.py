@@ -400,3 +400,50 @@ def test_token_sample_matches_full_run():
     part = oracle.forward(inp, token_sample=samp, threads=4)
     assert torch.equal(part["output"].view(torch.int16)[samp], full["output"].view(torch.int16)[samp])
     assert torch.equal(part["share_output"].view(torch.int16)[samp], full["share_output"].view(torch.int16)[samp])
+
+
+# ------------------------------------------------ folded routing weight mode
+# The DeepSeek-V4 decode case study (§2.3) fuses the routing weight into the
+# per-row GEMM2 dequant scale; the combine becomes a plain sum.  Pins: the
+# mode equals the default mode bit for bit whenever every routing weight is a
+# power of two (scaling by 2^j commutes with every rounding step), it matches
+# the float64 dense evaluation within the same bound, and a dropped or
+# doubled weight fails both.
+
+def _with_scales(inp, scales):
+    inp.expert_scales = scales.to(torch.float32)
+    return inp
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_folded_equals_default_for_power_of_two_weights(wl):
+    inp = synth.make_inputs(wl)
+    g = torch.Generator().manual_seed(7)
+    pw = torch.randint(-3, 2, inp.expert_scales.shape, generator=g).to(torch.float32)
+    _with_scales(inp, torch.pow(2.0, pw))
+    a = oracle.forward(inp, threads=4)
+    b = oracle.forward(inp, threads=4, fold_routing=True)
+    assert torch.equal(a["output"].view(torch.int16), b["output"].view(torch.int16))
+    if wl.has_shared:
+        assert torch.equal(a["share_output"].view(torch.int16), b["share_output"].view(torch.int16))
+
+
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_folded_matches_float64_dense(wl):
+    inp = synth.make_inputs(wl)
+    res = oracle.forward(inp, threads=4, fold_routing=True)
+    ref_out, ref_share = dense_reference(inp)
+    rowwise_close(res["output"].float().numpy(), ref_out, 1e-2)
+    if wl.has_shared:
+        rowwise_close(res["share_output"].float().numpy(), ref_share, 1e-2)
+
+
+def test_folded_differs_from_default_for_generic_weights():
+    # the two modes round differently (the weight multiplies before the row's
+    # bf16 rounding); with softmax weights some outputs must differ
+    inp = synth.make_inputs(CASES[0])
+    a = oracle.forward(inp, threads=4)
+    b = oracle.forward(inp, threads=4, fold_routing=True)
+    assert not torch.equal(a["output"].view(torch.int16), b["output"].view(torch.int16))
+    diff = (a["output"].float() - b["output"].float()).abs().max().item()
+    assert diff <= 2e-2 * a["output"].float().abs().max().item()
