@@ -273,7 +273,7 @@ def run_ours(args, wl, ws, rank, local):
         di["mask"] = inp.mask.to(dev)
 
     blk = m.MoeFused(wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter, wl.has_shared, dev,
-                     unfused=getattr(args, "unfused", False))
+                     unfused=getattr(args, "unfused", False), fold_routing=getattr(args, "fold_routing", False))
     stream = torch.cuda.current_stream(dev)
     out, sout, nums = blk.forward_inputs(di, weights)
     torch.cuda.synchronize()
@@ -376,7 +376,8 @@ def run_ours(args, wl, ws, rank, local):
         "vs_baseline": None,
         "dtype": "int8",
         "data": "synthetic (seeded counter-hash inputs, random-init int8 weights)",
-        "config": {**workload_config(wl, alg, ws), **({"unfused": True} if getattr(args, "unfused", False) else {})},
+        "config": {**workload_config(wl, alg, ws), **({"unfused": True} if getattr(args, "unfused", False) else {}),
+                   **({"fold_routing": True} if getattr(args, "fold_routing", False) else {})},
         "roofline": {**roof, "traffic": traffic, "kernel": dom, "peak_kind": peak_kind,
                      "alg_bytes_per_launch": alg[dom], "int_ops_per_launch": alg["ops"][dom],
                      "avg_launch_us": d_avg_s * 1e6,
@@ -470,6 +471,8 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="MOE_FLAG_UNFUSED: the unfused chain (tensor-core GEMMs, separate requant and combine) "
                          "as an A/B baseline")
+    ap.add_argument("--fold-routing", action="store_true",
+                    help="MOE_FLAG_FOLD_ROUTING: routing weight folded into the GEMM2 row scale")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the workload's expert count (smaller cases for profiler captures)")
     args = ap.parse_args()

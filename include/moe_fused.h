@@ -49,9 +49,10 @@ extern "C" {
 /* Static shape of one block.  Limits: 1 <= hidden, inter <= 16384 and both
  * multiples of 64; 1 <= num_experts <= 1024; 1 <= topk <= min(num_experts, 16);
  * 0 <= bs_max <= 65536.  GEMM1 has N = 2*inter outputs (gate rows 0..inter-1,
- * up rows inter..2*inter-1); GEMM2 maps inter -> hidden.  `flags` is 0 or
- * MOE_FLAG_UNFUSED; other bits are reserved (MOE_ERR_INVALID_ARG).  The
- * pages' supported ranges (§9.4) are not enforced. */
+ * up rows inter..2*inter-1); GEMM2 maps inter -> hidden.  `flags` is a
+ * combination of MOE_FLAG_UNFUSED and MOE_FLAG_FOLD_ROUTING; other bits are
+ * reserved (MOE_ERR_INVALID_ARG).  The pages' supported ranges (§9.4) are not
+ * enforced. */
 
 /* Every expert takes the tensor-core path with separate requant and combine
  * kernels: the unfused chain (FusedDeepMoE analysis §9.3, the "SmallOps"
@@ -60,6 +61,15 @@ extern "C" {
  * rows take by default.  Results are the same either way (the same
  * operations in the same order). */
 #define MOE_FLAG_UNFUSED 1
+
+/* The routing weight of pair (t, k) is folded into its row's GEMM2 dequant
+ * scale (DeepSeek-V4 decode case study §2.3: the per-row dequant scale and
+ * the routing weight fused into one row scale computed once per row):
+ *   y2[r][j] = bf16((float(acc2[r][j]) * w2_scale[e][j]) * (s2[r] * expert_scales[t][k]))
+ *   output[t] = bf16(sum over k ascending of float(y2[row(t,k)])), from 0.0f.
+ * The shared expert is unchanged.  This rounds differently from the default
+ * (routing weight applied in the combine after each row's bf16 rounding). */
+#define MOE_FLAG_FOLD_ROUTING 2
 typedef struct {
   int32_t bs_max;
   int32_t hidden;

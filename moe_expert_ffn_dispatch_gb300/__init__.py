@@ -33,6 +33,9 @@ MOE_ERR_ALIGNMENT = -7
 # config flag: every expert on the tensor-core path with separate requant and
 # combine kernels (the unfused A/B baseline); results are the same
 FLAG_UNFUSED = 1
+# config flag: routing weight folded into each row's GEMM2 dequant scale, the
+# combine a plain sum (rounds differently from the default)
+FLAG_FOLD_ROUTING = 2
 
 KERNEL_NAMES = ["dispatch_quant", "expand", "gemm1_small", "gemm1_big", "requant_big", "gemm2_small", "gemm2_big",
                 "combine"]
@@ -213,14 +216,14 @@ class MoeFused:
     """
 
     def __init__(self, bs_max: int, hidden: int, num_experts: int, topk: int, inter: int,
-                 has_shared: bool, device=None, unfused: bool = False):
+                 has_shared: bool, device=None, unfused: bool = False, fold_routing: bool = False):
         self.device = torch.device(device if device is not None else "cuda")
         if self.device.type != "cuda":
             raise ValueError("the fused MoE block runs on a CUDA device only")
         if self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
         self.cfg = Config(bs_max, hidden, num_experts, topk, inter, int(bool(has_shared)),
-                          FLAG_UNFUSED if unfused else 0)
+                          (FLAG_UNFUSED if unfused else 0) | (FLAG_FOLD_ROUTING if fold_routing else 0))
         with torch.cuda.device(self.device):
             rc, self.handle, self.workspace_bytes = moe_fused_create(self.cfg)
         if rc:

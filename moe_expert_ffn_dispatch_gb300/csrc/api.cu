@@ -45,7 +45,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 int check_config(const moe_fused_config_t* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & ~MOE_FLAG_UNFUSED) != 0) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~(MOE_FLAG_UNFUSED | MOE_FLAG_FOLD_ROUTING)) != 0) return MOE_ERR_INVALID_ARG;
   if (c->hidden < 64 || c->hidden > 16384 || c->hidden % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->inter < 64 || c->inter > 16384 || c->inter % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->num_experts < 1 || c->num_experts > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -137,6 +137,7 @@ int build_params(moe_fused_handle* hd, const moe_fused_args_t* a, void* ws, size
   p->I = c.inter;
   p->has_shared = c.has_shared;
   p->share_uses_xq = c.has_shared && (a->expert_smooth_scales == a->share_smooth_scales);
+  p->fold_routing = (c.flags & MOE_FLAG_FOLD_ROUTING) != 0;
   p->with_tickets = 1;
   const bool fused_ok = (c.flags & MOE_FLAG_UNFUSED) == 0 && c.hidden <= moe::kSmallMaxK && c.inter <= moe::kSmallMaxK;
   p->small_rows = fused_ok ? moe::kSmallRows : 0;

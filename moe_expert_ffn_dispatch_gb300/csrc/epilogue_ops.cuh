@@ -107,7 +107,8 @@ __device__ void combine_token(const FwdParams& p, int t, int ctid) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float f = bf16_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
-          acc[j] = __fadd_rn(acc[j], __fmul_rn(f, sc));
+          // folded mode: the rows already carry their routing weight
+          acc[j] = __fadd_rn(acc[j], p.fold_routing ? f : __fmul_rn(f, sc));
         }
       }
     }

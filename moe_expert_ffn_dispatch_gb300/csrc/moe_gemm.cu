@@ -218,11 +218,14 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
     const int8_t* xsq = p.share_uses_xq ? xq : ws_ptr<int8_t>(p, p.L.xs_q);
     const int8_t* x2 = ws_ptr<int8_t>(p, p.L.x2);
     // token info is loaded one item ahead so its latency hides behind the copies
+    const int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
     auto load_info = [&](const SmallItem& x, int& tok, float& sc) {
       if (lane < x.m) {
         const int r = x.row0 + lane;
         tok = row_token[r];
-        sc = G1 ? (x.e >= 0 ? xsc : xssc)[tok] : s2[r];
+        if (G1) sc = (x.e >= 0 ? xsc : xssc)[tok];
+        else if (p.fold_routing && x.e >= 0) sc = __fmul_rn(s2[r], p.scales[tk_of_row[r]]);  // folded row scale
+        else sc = s2[r];
       }
     };
     int nx_tok = 0;

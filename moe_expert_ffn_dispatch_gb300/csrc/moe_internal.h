@@ -87,6 +87,7 @@ constexpr int kTokenBlock = 128;  // token rows per big-phase work item (the MMA
 struct FwdParams {
   int32_t bs, h, E, topk, I, has_shared;
   int32_t share_uses_xq;  // shared quant identical to routed quant (same smooth vector)
+  int32_t fold_routing;   // routing weight folded into the GEMM2 row scale; combine is a plain sum
   int32_t with_tickets;   // dispatch resets the GEMM epilogue counters (forward path)
   int32_t small_rows;     // row count up to which an expert takes the dp4a path (0: never)
   int32_t num_ctas;       // grid of the GEMM launches (<= kMaxCtas)

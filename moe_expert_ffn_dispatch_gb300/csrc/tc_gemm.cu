@@ -438,6 +438,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     const float* xsc = ws_ptr<float>(p, p.L.x_scale);
     const float* xssc = p.share_uses_xq ? xsc : ws_ptr<float>(p, p.L.xs_scale);
     const float* s2 = ws_ptr<float>(p, p.L.s2);
+    const int32_t* tk_of_row_g = ws_ptr<int32_t>(p, p.L.tk_of_row);
     float* hbuf = ws_ptr<float>(p, p.L.hbuf);
     uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
     long acc_n = 0;
@@ -451,7 +452,9 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         const int t = row_token[r];
         tok_row[ctid] = r;
         tok_tok[ctid] = t;
-        tok_scale[ctid] = G1 ? (x.e >= 0 ? xsc : xssc)[t] : s2[r];
+        if (G1) tok_scale[ctid] = (x.e >= 0 ? xsc : xssc)[t];
+        else if (p.fold_routing && x.e >= 0) tok_scale[ctid] = __fmul_rn(s2[r], p.scales[tk_of_row_g[r]]);
+        else tok_scale[ctid] = s2[r];
       }
       consumer_sync();
       int acc[64];

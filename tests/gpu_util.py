@@ -47,9 +47,9 @@ def device_weights(inp, dev):
     return w
 
 
-def make_block(wl, dev, bs_max=None, unfused=False):
+def make_block(wl, dev, bs_max=None, unfused=False, fold_routing=False):
     return m.MoeFused(bs_max if bs_max is not None else wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter,
-                      wl.has_shared, dev, unfused=unfused)
+                      wl.has_shared, dev, unfused=unfused, fold_routing=fold_routing)
 
 
 def region(blk, name, dtype, shape=None):
@@ -116,7 +116,9 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
     torch.cuda.synchronize()
     st = blk.status()
     assert st["rc"] == 0 and st["error_flags"] == 0, st
-    ref = oracle.forward(inp, intermediates=staged, threads=8)
+    # the oracle runs in the mode the block was created in
+    ref = oracle.forward(inp, intermediates=staged, threads=8,
+                         fold_routing=bool(blk.cfg.flags & m.FLAG_FOLD_ROUTING))
     R = ref["R"]
     assert st["dispatched_rows"] == R
     assert st["skipped_pairs"] == ref["skipped"]

@@ -64,10 +64,12 @@ def test_workspace_size_and_config_checks(built):
     assert nb % 256 == 0
     for cfg, code in [(m.Config(8, 100, 4, 2, 64, 0, 0), m.MOE_ERR_UNSUPPORTED_SHAPE),
                       (m.Config(8, 128, 4, 5, 64, 0, 0), m.MOE_ERR_UNSUPPORTED_SHAPE),
-                      (m.Config(8, 128, 4, 2, 64, 0, 3), m.MOE_ERR_INVALID_ARG),
+                      (m.Config(8, 128, 4, 2, 64, 0, 4), m.MOE_ERR_INVALID_ARG),  # reserved flag bit
                       (m.Config(8, 128, 2000, 2, 64, 0, 0), m.MOE_ERR_UNSUPPORTED_SHAPE),
                       (m.Config(8, 128, 4, 2, 64, 2, 0), m.MOE_ERR_INVALID_ARG)]:
         assert m.moe_fused_workspace_size(cfg)[0] == code
+    for flags in (m.FLAG_UNFUSED, m.FLAG_FOLD_ROUTING, m.FLAG_UNFUSED | m.FLAG_FOLD_ROUTING):
+        assert m.moe_fused_workspace_size(m.Config(8, 128, 4, 2, 64, 0, flags))[0] == m.MOE_OK
 
 
 def test_strerror_and_names(built):

@@ -104,3 +104,23 @@ def test_unfused_chain_staged_parity(wl):
     blk = make_block(wl, DEV, unfused=True)
     blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True, blk=blk)
     check_raw_accumulators(blk, inp, ref, di, dw, DEV)
+
+
+FOLD_CASES = [CASES[0], CASES[1], CASES[2], CASES[3]]
+
+
+@pytest.mark.parametrize("wl", FOLD_CASES, ids=lambda w: w.name)
+def test_folded_routing_staged_parity(wl):
+    """MOE_FLAG_FOLD_ROUTING against the oracle's folded mode: y2 rows carry
+    the routing weight, the combine is a plain sum (both GEMM paths: the
+    multi-block case runs experts on the tensor cores)."""
+    inp = synth.make_inputs(wl)
+    blk = make_block(wl, DEV, fold_routing=True)
+    run_and_check(inp, DEV, staged=True, blk=blk)
+
+
+def test_folded_routing_unfused_chain():
+    wl = CASES[1]
+    inp = synth.make_inputs(wl)
+    blk = make_block(wl, DEV, unfused=True, fold_routing=True)
+    run_and_check(inp, DEV, staged=True, blk=blk)
