@@ -530,59 +530,93 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   }
 }
 
-// f16 copies of the token codes of every row in a big block: the GEMM1
-// operand that the tensor-memory path reads with TMA.
-__global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
-  grid_dependency_wait();
-  grid_launch_dependents();
-  const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
-  const int total = slots[SlotTable::kBigBlocks];
-  if (total == 0) return;
+// The big slots' tables (block prefix, first row, row count, expert) staged
+// in shared memory once per CTA, so that kernels working row by row find the
+// slot of a (block, row) pair in a few shared-memory probes instead of a
+// chain of dependent global loads.  Layout: 4 arrays of stride E + 2 ints
+// (at most E + 1 slots), i.e. big_slots_smem_bytes(E).
+__host__ __device__ constexpr size_t big_slots_smem_bytes(int E) { return 4u * (E + 2) * sizeof(int32_t); }
+
+struct BigSlots {
+  const int32_t* pre;
+  const int32_t* row0;
+  const int32_t* rows;
+  const int32_t* exp;
+  int n;
+};
+
+__device__ __forceinline__ BigSlots stage_big_slots(const FwdParams& p, const int32_t* slots, int32_t* t) {
   const int st = SlotTable::stride(p.E);
   const int32_t* s_exp = slots + SlotTable::kHeader;
   const int32_t* s_row0 = s_exp + st;
   const int32_t* s_rows = s_row0 + st;
   const int32_t* s_blk = s_rows + st;
-  const int n_slots = slots[SlotTable::kNumBig];
+  const int n = slots[SlotTable::kNumBig];
+  for (int i = threadIdx.x; i <= n; i += blockDim.x) {
+    t[i] = s_blk[i];
+    if (i < n) {
+      t[st + i] = s_row0[i];
+      t[2 * st + i] = s_rows[i];
+      t[3 * st + i] = s_exp[i];
+    }
+  }
+  __syncthreads();
+  return BigSlots{t, t + st, t + 2 * st, t + 3 * st, n};
+}
+
+// slot of big block b: the last slot whose first block is <= b
+__device__ __forceinline__ int big_slot_of(const BigSlots& t, int b) {
+  int lo = 0, hi = t.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (t.pre[mid] <= b) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// f16 copies of the token codes of every row in a big block: the GEMM1
+// operand that the tensor-memory path reads with TMA.  One warp per row slot
+// (block, row) of the big blocks; slots past a block's last row are skipped.
+__global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
+  extern __shared__ int32_t ex_smem[];  // big_slots_smem_bytes(E)
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
+  const int total = slots[SlotTable::kBigBlocks];
+  if (total == 0) return;
+  const BigSlots tab = stage_big_slots(p, slots, ex_smem);
   const int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
   const int8_t* xq = ws_ptr<int8_t>(p, p.L.x_q);
   const int8_t* xsq = p.share_uses_xq ? xq : ws_ptr<int8_t>(p, p.L.xs_q);
   __half* x1h = ws_ptr<__half>(p, p.L.x1h);
-  __shared__ int s_tok[TB];
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nw = gridDim.x * (blockDim.x >> 5);
   const int n16 = p.h >> 4;
-  for (int b = blockIdx.x; b < total; b += gridDim.x) {
-    int lo = 0, hi = n_slots - 1;  // slot of block b
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_blk[mid] <= b) lo = mid;
-      else hi = mid - 1;
-    }
-    const int tb = b - s_blk[lo];
-    const int r0 = s_row0[lo] + tb * TB;
-    const int n = min(TB, s_rows[lo] - tb * TB);
-    const int8_t* src = s_exp[lo] >= 0 ? xq : xsq;
-    __syncthreads();  // the previous block's readers are done with s_tok
-    if (threadIdx.x < n) s_tok[threadIdx.x] = row_token[r0 + threadIdx.x];
-    __syncthreads();
-    // four independent 16-byte loads in flight per thread
-    const int tasks = n * n16;
-    for (int base = threadIdx.x; base < tasks; base += 4 * blockDim.x) {
+  const long nrows = static_cast<long>(total) * TB;
+  for (long g = gw; g < nrows; g += nw) {
+    const int b = static_cast<int>(g / TB), i = static_cast<int>(g % TB);
+    const int sl = big_slot_of(tab, b);
+    const int tb = b - tab.pre[sl];
+    if (tb * TB + i >= tab.rows[sl]) continue;
+    const int r = tab.row0[sl] + tb * TB + i;
+    const uint4* src = reinterpret_cast<const uint4*>((tab.exp[sl] >= 0 ? xq : xsq) +
+                                                      static_cast<size_t>(row_token[r]) * p.h);
+    uint4* dst = reinterpret_cast<uint4*>(x1h + static_cast<size_t>(r) * p.h);
+    for (int c0 = lane; c0 < n16; c0 += 4 * 32) {
       uint4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int idx = base + u * blockDim.x;
-        if (idx < tasks)
-          v[u] = reinterpret_cast<const uint4*>(src + static_cast<size_t>(s_tok[idx / n16]) * p.h)[idx % n16];
-      }
+      for (int u = 0; u < 4; ++u)
+        if (c0 + 32 * u < n16) v[u] = src[c0 + 32 * u];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int idx = base + u * blockDim.x;
-        if (idx < tasks) {
+        const int c = c0 + 32 * u;
+        if (c < n16) {
           uint4 lo16, hi16;
           int8x16_to_f16(v[u], lo16, hi16);
-          uint4* dst = reinterpret_cast<uint4*>(x1h + static_cast<size_t>(r0 + idx / n16) * p.h) + 2 * (idx % n16);
-          dst[0] = lo16;
-          dst[1] = hi16;
+          dst[2 * c] = lo16;
+          dst[2 * c + 1] = hi16;
         }
       }
     }
@@ -623,19 +657,17 @@ constexpr int kRqWarps = 8;          // rows in flight per CTA (one per warp)
 constexpr int kRqMaxI = 2048;        // rows up to this I keep h in shared memory
 
 __global__ void __launch_bounds__(kRqWarps * 32) requant_big_kernel(FwdParams p) {
-  extern __shared__ float4 rq_smem[];  // [kRqWarps][I / 4] when I <= kRqMaxI
+  // [kRqWarps][kRqMaxI / 4] float4 when I <= kRqMaxI, then big_slots_smem_bytes(E)
+  extern __shared__ float4 rq_smem[];
   grid_dependency_wait();
   grid_launch_dependents();
   const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
   const int total = slots[SlotTable::kBigBlocks];
   if (total == 0) return;
-  const int st = SlotTable::stride(p.E);
-  const int32_t* s_row0 = slots + SlotTable::kHeader + st;
-  const int32_t* s_rows = s_row0 + st;
-  const int32_t* s_blk = s_rows + st;
-  const int n_slots = slots[SlotTable::kNumBig];
   const int I = p.I, n4 = I >> 2;
   const bool staged = I <= kRqMaxI;
+  const BigSlots tab =
+      stage_big_slots(p, slots, reinterpret_cast<int32_t*>(rq_smem + (staged ? kRqWarps * (kRqMaxI / 4) : 0)));
   const float* hbuf = ws_ptr<float>(p, p.L.hbuf);
   int8_t* x2 = ws_ptr<int8_t>(p, p.L.x2);
   __half* x2h = ws_ptr<__half>(p, p.L.x2h);
@@ -647,15 +679,10 @@ __global__ void __launch_bounds__(kRqWarps * 32) requant_big_kernel(FwdParams p)
   const long nrows = static_cast<long>(total) * TB;  // block-major row slots (some empty)
   for (long g = gw; g < nrows; g += nw) {
     const int b = static_cast<int>(g / TB), i = static_cast<int>(g % TB);
-    int lo = 0, hi = n_slots - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_blk[mid] <= b) lo = mid;
-      else hi = mid - 1;
-    }
-    const int tb = b - s_blk[lo];
-    if (tb * TB + i >= s_rows[lo]) continue;
-    const int r = s_row0[lo] + tb * TB + i;
+    const int sl = big_slot_of(tab, b);
+    const int tb = b - tab.pre[sl];
+    if (tb * TB + i >= tab.rows[sl]) continue;
+    const int r = tab.row0[sl] + tb * TB + i;
     const float4* gr = reinterpret_cast<const float4*>(hbuf + static_cast<size_t>(r) * (2 * I));
     const float4* ur = gr + n4;
     uint32_t* q4 = reinterpret_cast<uint32_t*>(x2 + static_cast<size_t>(r) * I);
@@ -716,7 +743,8 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdParams p) {
 cudaError_t launch_requant_big(const FwdParams& p, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
-  const size_t smem = p.I <= kRqMaxI ? static_cast<size_t>(kRqWarps) * kRqMaxI * sizeof(float) : 0;
+  const size_t smem = (p.I <= kRqMaxI ? static_cast<size_t>(kRqWarps) * kRqMaxI * sizeof(float) : 0) +
+                      big_slots_smem_bytes(p.E);
   cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 3), dim3(kRqWarps * 32), smem, s, attr);
   return cudaLaunchKernelEx(&cfg, requant_big_kernel, p);
 }
@@ -739,13 +767,13 @@ cudaError_t moe_gemm_big_prepare_attributes() {
   }
   return cudaFuncSetAttribute(reinterpret_cast<const void*>(requant_big_kernel),
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kRqWarps * kRqMaxI * sizeof(float)));
+                              static_cast<int>(kRqWarps * kRqMaxI * sizeof(float) + big_slots_smem_bytes(1024)));
 }
 
 cudaError_t launch_expand(const FwdParams& p, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 4), dim3(256), 0, s, attr);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 4), dim3(256), big_slots_smem_bytes(p.E), s, attr);
   return cudaLaunchKernelEx(&cfg, expand_kernel, p);
 }
 
