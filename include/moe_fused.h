@@ -204,11 +204,13 @@ int moe_fused_dispatch_noalloc(const int32_t* expert_ids, const uint8_t* x_activ
  * `stream`.  get_timing synchronises the recorded events, writes for each
  * kernel id k < max_kernels the summed milliseconds ms[k] and launch count
  * launches[k] (host arrays), returns the number of kernel ids, and clears the
- * record.  Kernel ids: 0 dispatch + quant, 1 expand (f16 token rows for the
- * tensor-core GEMMs), 2 GEMM1 + SwiGLU (+ requant) for experts with at most
- * 8 rows (dp4a weight streaming), 3 GEMM1 + SwiGLU for the other experts
- * (tcgen05), 4 requant of their rows, 5 GEMM2 + dequant (+ combine when every
- * expert has at most 8 rows), 6 GEMM2 + dequant (tcgen05), 7 combine. */
+ * record.  Kernel ids: 0 dispatch + quant, 1 dispatch finish (multi-CTA
+ * dispatch of batches with bs*topk > 2048; not launched otherwise), 2 expand
+ * (f16 token rows for the tensor-core GEMMs), 3 GEMM1 + SwiGLU (+ requant)
+ * for experts with at most 8 rows (dp4a weight streaming), 4 GEMM1 + dequant
+ * for the other experts (tcgen05), 5 SwiGLU + requant of their rows, 6 GEMM2
+ * + dequant (+ combine when every expert has at most 8 rows), 7 GEMM2 +
+ * dequant (tcgen05), 8 combine. */
 int moe_fused_set_timing(moe_fused_handle_t* handle, int enable);
 int moe_fused_get_timing(moe_fused_handle_t* handle, float* ms, int32_t* launches, int max_kernels);
 const char* moe_fused_kernel_name(int kernel_id);
@@ -219,11 +221,15 @@ const char* moe_fused_kernel_name(int kernel_id);
  *   0 status  1 counts [E]  2 offsets [E+1]  3 row_of [bs*topk]
  *   4 tk_of_row [bs*topk]  5 active tokens [bs]  6 x_q [bs_max,h] int8
  *   7 x_scale [bs_max] f32  8 xs_q [bs_max,h] int8  9 xs_scale [bs_max]
- *   10 h [rows,inter] f32  11 x2 [rows,inter] int8  12 s2 [rows] f32
+ *   10 h [rows,2*inter] f32 (SwiGLU output in the first inter floats of a row
+ *      of the weight-streaming path; dequantised gate | up of the tensor-core
+ *      path)  11 x2 [rows,inter] int8  12 s2 [rows] f32
  *   13 y2 [bs_max*topk,h] bf16 (aliases region 10)  14 slot table
  *   15 row_token [rows] int32  16 shared_row [bs_max] int32
  *   17 row-block counters  18 token counters [bs_max]  19 token totals [bs_max]
  *   20 small-expert item ranges  21 x1h [rows,h] f16  22 x2h [rows,inter] f16
+ *   23 multi-CTA dispatch counts [chunks][E] then skipped ids [chunks]
+ *      (empty when bs_max*topk <= 2048: one CTA dispatches alone)
  * `rows` = bs*topk + bs: routed row r at index r (r < R), the shared expert's
  * i-th active token at index bs*topk + i.  Writes *offset and *bytes. */
 int moe_fused_debug_region(moe_fused_handle_t* handle, int region, size_t* offset, size_t* bytes);

@@ -96,6 +96,8 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
   take(L.ranges, 2 * (moe::kMaxCtas + 1) * 4, moe::kRegRanges);
   take(L.x1h, rows * h * 2, moe::kRegX1h);
   take(L.x2h, rows * I * 2, moe::kRegX2h);
+  const size_t chunks = routed > 4 * moe::kDispChunk ? (routed + moe::kDispChunk - 1) / moe::kDispChunk : 1;
+  take(L.dcnt, chunks > 1 ? (chunks * E + chunks) * 4 : 0, moe::kRegDcnt);
   L.total = off;
   return L;
 }
@@ -138,6 +140,9 @@ int build_params(moe_fused_handle* hd, const moe_fused_args_t* a, void* ws, size
   p->has_shared = c.has_shared;
   p->share_uses_xq = c.has_shared && (a->expert_smooth_scales == a->share_smooth_scales);
   p->fold_routing = (c.flags & MOE_FLAG_FOLD_ROUTING) != 0;
+  // the second launch of the multi-CTA dispatch pays off above a few chunks
+  const int nf = a->bs * c.topk;
+  p->disp_chunks = nf > 4 * moe::kDispChunk ? (nf + moe::kDispChunk - 1) / moe::kDispChunk : 1;
   p->with_tickets = 1;
   const bool fused_ok = (c.flags & MOE_FLAG_UNFUSED) == 0 && c.hidden <= moe::kSmallMaxK && c.inter <= moe::kSmallMaxK;
   p->small_rows = fused_ok ? moe::kSmallRows : 0;
@@ -324,6 +329,7 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
   auto run = [&](int k) -> cudaError_t {
     switch (k) {
       case moe::kKDispatchQuant: return moe::launch_dispatch_quant(p, s);
+      case moe::kKDispatchFinish: return moe::launch_dispatch_finish(p, s);
       case moe::kKExpand: return moe::launch_expand(p, s);
       case moe::kKGemm1Small: return moe::launch_moe_gemm_small(p, moe::kGemm1SwiGLU, nullptr, sms, s);
       case moe::kKGemm1Big: return moe::launch_moe_gemm_big(p, maps, moe::kGemm1SwiGLU, nullptr, sms, s);
@@ -334,7 +340,10 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
     }
   };
   e = cudaSuccess;
-  for (int k = 0; k <= last_kernel && e == cudaSuccess; ++k) e = timed(hd, k, s, [&] { return run(k); });
+  for (int k = 0; k <= last_kernel && e == cudaSuccess; ++k) {
+    if (k == moe::kKDispatchFinish && p.disp_chunks <= 1) continue;  // one-CTA dispatch: nothing to launch
+    e = timed(hd, k, s, [&] { return run(k); });
+  }
   return cuda_fail(e);
 }
 
@@ -412,8 +421,8 @@ int moe_fused_get_timing(moe_fused_handle_t* hd, float* ms, int32_t* launches, i
 }
 
 const char* moe_fused_kernel_name(int k) {
-  static const char* names[] = {"dispatch_quant", "expand",      "gemm1_small", "gemm1_big",
-                                "requant_big",    "gemm2_small", "gemm2_big",   "combine"};
+  static const char* names[] = {"dispatch_quant", "dispatch_finish", "expand",    "gemm1_small", "gemm1_big",
+                                "requant_big",    "gemm2_small",     "gemm2_big", "combine"};
   return (k >= 0 && k < moe::kNumKernels) ? names[k] : "unknown";
 }
 
@@ -429,7 +438,7 @@ int moe_fused_debug_region(moe_fused_handle_t* hd, int region, size_t* offset, s
   const size_t offs[moe::kNumRegions] = {L.status, L.counts, L.offsets, L.row_of, L.tk_of_row, L.active, L.x_q,
                                          L.x_scale, L.xs_q, L.xs_scale, L.hbuf, L.x2, L.s2, L.y2, L.slots,
                                          L.row_token, L.shared_row, L.blk_ticket, L.tok_ticket, L.tok_expect,
-                                         L.ranges, L.x1h, L.x2h};
+                                         L.ranges, L.x1h, L.x2h, L.dcnt};
   if (region < 0 || region >= moe::kNumRegions) return MOE_ERR_INVALID_ARG;
   *offset = offs[region];
   *bytes = L.sizes[region];

@@ -72,71 +72,55 @@ __device__ __forceinline__ unsigned warp_peers(int key, int nbits) {
   return m;
 }
 
-// Dispatch by one 1024-thread CTA.  dsm: dynamic shared memory of
-// dispatch_smem_bytes(E).
-__device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
-  __shared__ int s_warp[32];
-  __shared__ unsigned long long s_warp64[32];
-  __shared__ int s_skipped;
-  const int E = p.E, K = p.topk, bs = p.bs;
+// Step 1 of the dispatch over the flat pairs [f_lo, f_hi) by one 1024-thread
+// CTA: warp w ranks the contiguous segment [f_lo + w seg, f_lo + (w+1) seg)
+// 32 pairs at a time (equal experts inside a step found by one ballot per
+// expert-id bit; wcnt[w][e] keeps the warp's running count).  On return
+// (after a CTA barrier): row_of[f] = rank of pair f inside (its warp's
+// segment, its expert), or -1 for a pair that is not routed; wcnt[w][e] =
+// rows of expert e in the segments of warps before w; running[e] (e < E) =
+// rows of expert e in the range; [seg_lo, seg_hi) = this warp's segment.
+__device__ void rank_range(const FwdParams& p, int32_t* running, int32_t* wcnt, int f_lo, int f_hi,
+                           int* s_skipped, int& seg_lo, int& seg_hi) {
+  const int E = p.E, K = p.topk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int32_t* running = dsm;    // [E]: rows per expert so far, later the offsets
-  int32_t* wcnt = dsm + E;   // [32][E]: rows per (warp, expert) in this chunk
   int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
-  int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
-  int32_t* counts = ws_ptr<int32_t>(p, p.L.counts);
-  int32_t* offsets = ws_ptr<int32_t>(p, p.L.offsets);
-  int32_t* active = ws_ptr<int32_t>(p, p.L.active);
-  int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
-  int32_t* status = ws_ptr<int32_t>(p, p.L.status);
-  int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
-  int32_t* shared_row = ws_ptr<int32_t>(p, p.L.shared_row);
-
-  for (int e = tid; e < E; e += kDispatchThreads) running[e] = 0;
-  if (tid == 0) s_skipped = 0;
-  __syncthreads();
-
-  // 1. rank of every active, valid pair inside its expert group, stable in
-  //    the flat order: warp w ranks the contiguous segment [w seg, (w+1) seg)
-  //    of the flat (t, k) index 32 pairs at a time (match_any groups equal
-  //    experts; wcnt[w][e] keeps the warp's running count), then the
-  //    per-expert exclusive prefix over the warps turns (warp, rank) into the
-  //    rank inside the expert group.
-  const int nf = bs * K;
-  const int seg = ((nf + 31) / 32 + 31) & ~31;  // pairs per warp, a multiple of 32
+  const int nfr = f_hi - f_lo;
+  const int seg = ((nfr + 31) / 32 + 31) & ~31;  // pairs per warp, a multiple of 32
   const int key_bits = 32 - __clz(E);            // keys 0..E (E = not routed)
-  const int f_begin = warp * seg, f_end = min(nf, (warp + 1) * seg);
+  seg_lo = min(f_hi, f_lo + warp * seg);
+  seg_hi = min(f_hi, f_lo + (warp + 1) * seg);
   for (int i = tid; i < 32 * E; i += kDispatchThreads) wcnt[i] = 0;
   __syncthreads();
   {
     int32_t* mycnt = wcnt + warp * E;
-    for (int f0 = f_begin; f0 < f_end; f0 += 32 * 8) {
+    for (int f0 = seg_lo; f0 < seg_hi; f0 += 32 * 8) {
       int ev[8];  // the ids of 8 steps are loaded before any is ranked
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int f = f0 + 32 * u + lane;
         int e = E;
-        if (f < f_end) {
+        if (f < seg_hi) {
           const int t = f / K;
           const bool act = (p.mask == nullptr) || (p.mask[t] != 0);
           const int id = p.ids[f];
           if (act) {
             if (id >= 0 && id < E) e = id;
-            else atomicAdd(&s_skipped, 1);
+            else atomicAdd(s_skipped, 1);
           }
         }
         ev[u] = e;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        if (f0 + 32 * u >= f_end) break;  // warp-uniform
+        if (f0 + 32 * u >= seg_hi) break;  // warp-uniform
         const int f = f0 + 32 * u + lane;
         const int e = ev[u];
         const unsigned peers = warp_peers(e, key_bits);
         const int rank_w = __popc(peers & ((1u << lane) - 1u));
         const int before = (e < E) ? mycnt[e] : 0;
         __syncwarp();
-        if (f < f_end) row_of[f] = (e < E) ? before + rank_w : -1;
+        if (f < seg_hi) row_of[f] = (e < E) ? before + rank_w : -1;
         if (e < E && rank_w == 0) mycnt[e] = before + __popc(peers);
         __syncwarp();
       }
@@ -153,47 +137,32 @@ __device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
     running[tid] = run;
   }
   __syncthreads();
+}
 
-  // 2. counts -> exclusive offsets (E <= 1024: one expert per thread)
-  const int c = tid < E ? running[tid] : 0;
-  int R = 0;
-  const int off = block_exclusive_scan(c, &R, s_warp);
+// Everything after the rows are placed, by one CTA: counts, offsets and
+// expert_token_nums; the active-token list and shared rows; the slot tables;
+// the status words; the small-phase item ranges and the per-forward ticket
+// reset.  Thread tid < E holds its expert's count c and first row off; R is
+// the number of routed rows.  dsm: at least E + 2 ints of scratch.
+__device__ void dispatch_tail(const FwdParams& p, int32_t* dsm, int c, int off, int R, int skipped) {
+  __shared__ int s_warp[32];
+  __shared__ unsigned long long s_warp64[32];
+  const int E = p.E, K = p.topk, bs = p.bs;
+  const int tid = threadIdx.x;
+  int32_t* counts = ws_ptr<int32_t>(p, p.L.counts);
+  int32_t* offsets = ws_ptr<int32_t>(p, p.L.offsets);
+  int32_t* active = ws_ptr<int32_t>(p, p.L.active);
+  int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
+  int32_t* status = ws_ptr<int32_t>(p, p.L.status);
+  int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
+  int32_t* shared_row = ws_ptr<int32_t>(p, p.L.shared_row);
+  const int s_skipped = skipped;
   if (tid < E) {
     counts[tid] = c;
     offsets[tid] = off;
     p.token_nums[tid] = c;
-    running[tid] = off;
   }
   if (tid == 0) offsets[E] = R;
-  __syncthreads();
-
-  // 3. final row index and its inverse: each warp walks its own segment
-  //    again (its ranks were written by the same lanes), 8 steps of loads at
-  //    a time before the writes.
-  {
-    const int32_t* mypre = wcnt + warp * E;
-    for (int f0 = f_begin; f0 < f_end; f0 += 32 * 8) {
-      int rk[8], ev[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int f = f0 + 32 * u + lane;
-        rk[u] = (f < f_end) ? row_of[f] : -1;
-        ev[u] = (f < f_end) ? p.ids[f] : 0;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (rk[u] >= 0) {
-          const int f = f0 + 32 * u + lane;
-          const int e = ev[u];
-          const int r = running[e] + mypre[e] + rk[u];
-          row_of[f] = r;
-          tk_of_row[r] = f;
-          row_token[r] = f / K;
-        }
-      }
-    }
-  }
-  __syncthreads();
 
   // 4. active tokens in ascending order (rows of the shared expert)
   int S = 0;
@@ -337,6 +306,91 @@ __device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
   }
 }
 
+// Dispatch of the whole batch by one 1024-thread CTA.  dsm: dynamic shared
+// memory of dispatch_smem_bytes(E).
+__device__ void dispatch_block(const FwdParams& p, int32_t* dsm) {
+  __shared__ int s_warp1[32];
+  __shared__ int s_skipped;
+  const int E = p.E, K = p.topk, bs = p.bs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t* running = dsm;    // [E]: rows per expert, later the offsets
+  int32_t* wcnt = dsm + E;   // [32][E]: rows per (warp, expert)
+  int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
+  int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
+  int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
+  if (tid == 0) s_skipped = 0;
+  __syncthreads();
+
+  // 1. ranks inside (warp segment, expert)
+  int seg_lo, seg_hi;
+  rank_range(p, running, wcnt, 0, bs * K, &s_skipped, seg_lo, seg_hi);
+
+  // 2. counts -> exclusive offsets (E <= 1024: one expert per thread)
+  const int c = tid < E ? running[tid] : 0;
+  int R = 0;
+  const int off = block_exclusive_scan(c, &R, s_warp1);
+  if (tid < E) running[tid] = off;
+  __syncthreads();
+
+  // 3. final row index and its inverse: each warp walks its own segment
+  //    again (its ranks were written by the same lanes), 8 steps of loads at
+  //    a time before the writes.
+  {
+    const int32_t* mypre = wcnt + warp * E;
+    for (int f0 = seg_lo; f0 < seg_hi; f0 += 32 * 8) {
+      int rk[8], ev[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int f = f0 + 32 * u + lane;
+        rk[u] = (f < seg_hi) ? row_of[f] : -1;
+        ev[u] = (f < seg_hi) ? p.ids[f] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (rk[u] >= 0) {
+          const int f = f0 + 32 * u + lane;
+          const int e = ev[u];
+          const int r = running[e] + mypre[e] + rk[u];
+          row_of[f] = r;
+          tk_of_row[r] = f;
+          row_token[r] = f / K;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  dispatch_tail(p, dsm, c, off, R, s_skipped);
+}
+
+// Multi-CTA dispatch, first phase: CTA g ranks chunk g of the flat pairs
+// (kDispChunk pairs) and leaves each routed pair's rank inside (chunk,
+// expert) in row_of, its per-expert totals in dcnt[g][0..E) and its count of
+// skipped ids in dcnt[G E + g].
+__device__ void dispatch_chunk(const FwdParams& p, int32_t* dsm, int g) {
+  __shared__ int s_skipped;
+  const int E = p.E, nf = p.bs * p.topk;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t* running = dsm;
+  int32_t* wcnt = dsm + E;
+  int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
+  int32_t* dcnt = ws_ptr<int32_t>(p, p.L.dcnt);
+  const int G = p.disp_chunks;
+  if (tid == 0) s_skipped = 0;
+  __syncthreads();
+  int seg_lo, seg_hi;
+  const int f_lo = g * kDispChunk, f_hi = min(nf, f_lo + kDispChunk);
+  rank_range(p, running, wcnt, f_lo, f_hi, &s_skipped, seg_lo, seg_hi);
+  {
+    const int32_t* mypre = wcnt + warp * E;
+    for (int f = seg_lo + lane; f < seg_hi; f += 32) {
+      const int rk = row_of[f];
+      if (rk >= 0) row_of[f] = mypre[p.ids[f]] + rk;
+    }
+  }
+  if (tid < E) dcnt[static_cast<size_t>(g) * E + tid] = running[tid];
+  if (tid == 0) dcnt[static_cast<size_t>(G) * E + g] = s_skipped;
+}
+
 __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(FwdParams p) {
   extern __shared__ int32_t dsm[];
   dispatch_block(p, dsm);
@@ -428,22 +482,83 @@ __device__ void quant_token(const FwdParams& p, int t, float* s_red, int group) 
   }
 }
 
-// CTA 0 dispatches; CTA b >= 1 quantises tokens 4(b-1) .. 4(b-1)+3, one per
-// 256-thread group.  The two halves are independent: nothing the quant
-// writes depends on the dispatch.
+// The first CTA (or the first disp_chunks CTAs, for large batches) dispatch;
+// the others quantise tokens, one per 256-thread group at a time.  The two
+// halves are independent: nothing the quant writes depends on the dispatch.
 __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(FwdParams p) {
   extern __shared__ int32_t dsm[];
   __shared__ float s_red[kQuantGroups][8];
   // the previous forward's GEMM2 may still read the workspace and write outputs
   grid_dependency_wait();
   grid_launch_dependents();
-  if (blockIdx.x == 0) {
-    dispatch_block(p, dsm);
+  const int nd = p.disp_chunks > 1 ? p.disp_chunks : 1;  // dispatch CTAs
+  if (blockIdx.x < nd) {
+    if (nd == 1) dispatch_block(p, dsm);
+    else dispatch_chunk(p, dsm, blockIdx.x);
     return;
   }
+  // quant CTAs loop over tokens (at most two CTAs per SM), one token per
+  // 256-thread group at a time
   const int group = threadIdx.x / kQuantThreads;
-  const int t = (blockIdx.x - 1) * kQuantGroups + group;
-  if (t < p.bs) quant_token(p, t, s_red[group], group);
+  const int stride = (gridDim.x - nd) * kQuantGroups;
+  for (int t = (blockIdx.x - nd) * kQuantGroups + group; t < p.bs; t += stride)
+    quant_token(p, t, s_red[group], group);
+}
+
+// Multi-CTA dispatch, second phase, one CTA per chunk: CTA g places the
+// routed pairs of chunk g -- expert e's rows of chunk g start at
+// offsets[e] + (rows of e in the chunks before g) -- and CTA 0 then runs the
+// tail (counts, offsets, active list, slot tables, status, tickets).
+__global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_finish_kernel(FwdParams p) {
+  extern __shared__ int32_t dsm[];
+  __shared__ int s_warp1[32];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int E = p.E, K = p.topk, nf = p.bs * K, G = p.disp_chunks;
+  const int tid = threadIdx.x, g = blockIdx.x;
+  const int32_t* dcnt = ws_ptr<int32_t>(p, p.L.dcnt);
+  int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
+  int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
+  int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
+  int pre = 0, tot = 0;
+  if (tid < E) {
+    for (int j = 0; j < G; ++j) {
+      const int v = dcnt[static_cast<size_t>(j) * E + tid];
+      if (j < g) pre += v;
+      tot += v;
+    }
+  }
+  int R = 0;
+  const int off = block_exclusive_scan(tot, &R, s_warp1);
+  if (tid < E) dsm[tid] = off + pre;
+  __syncthreads();
+  const int f_lo = g * kDispChunk, f_hi = min(nf, f_lo + kDispChunk);
+  for (int f0 = f_lo + tid; f0 < f_hi; f0 += 4 * kDispatchThreads) {
+    int rk[4], ev[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int f = f0 + u * kDispatchThreads;
+      rk[u] = f < f_hi ? row_of[f] : -1;
+      ev[u] = f < f_hi ? p.ids[f] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (rk[u] >= 0) {
+        const int f = f0 + u * kDispatchThreads;
+        const int r = dsm[ev[u]] + rk[u];
+        row_of[f] = r;
+        tk_of_row[r] = f;
+        row_token[r] = f / K;
+      }
+    }
+  }
+  if (g == 0) {
+    int skipped = 0;
+    if (tid == 0)
+      for (int j = 0; j < G; ++j) skipped += dcnt[static_cast<size_t>(G) * E + j];
+    __syncthreads();  // every placement of chunk 0 has read dsm
+    dispatch_tail(p, dsm, tot, off, R, skipped);
+  }
 }
 
 }  // namespace
@@ -451,17 +566,30 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(Fwd
 size_t dispatch_smem_bytes(int E) { return sizeof(int32_t) * static_cast<size_t>(33 * E); }
 
 cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s) {
-  const int blocks = 1 + (p.bs + kQuantGroups - 1) / kQuantGroups;
+  const int nd = p.disp_chunks > 1 ? p.disp_chunks : 1;
+  const int qblocks = (p.bs + kQuantGroups - 1) / kQuantGroups;
+  const int blocks = nd + (qblocks < 2 * p.num_ctas ? qblocks : 2 * p.num_ctas);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(blocks), dim3(kDispatchThreads), dispatch_smem_bytes(p.E), s, attr);
   return cudaLaunchKernelEx(&cfg, dispatch_quant_kernel, p);
+}
+
+cudaError_t launch_dispatch_finish(const FwdParams& p, cudaStream_t s) {
+  if (p.bs == 0 || p.disp_chunks <= 1) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg =
+      pdl_config(dim3(p.disp_chunks), dim3(kDispatchThreads), dispatch_smem_bytes(p.E), s, attr);
+  return cudaLaunchKernelEx(&cfg, dispatch_finish_kernel, p);
 }
 
 cudaError_t dispatch_prepare_attributes(int E) {
   cudaError_t e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(dispatch_smem_bytes(E)));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(dispatch_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(dispatch_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(dispatch_smem_bytes(E)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(dispatch_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(dispatch_smem_bytes(E)));
 }
 

@@ -48,15 +48,16 @@ struct WsLayout {
   size_t ranges;     // [2][kMaxCtas + 1] int32: small-phase item range of each CTA (GEMM1, GEMM2)
   size_t x1h;        // [rows, h] f16: GEMM1 token operand of the rows in big blocks (codes as f16)
   size_t x2h;        // [rows, I] f16: GEMM2 token operand of the rows in big blocks
+  size_t dcnt;       // multi-CTA dispatch: [chunks][E] rows per (chunk, expert), then [chunks] skipped ids
   size_t total;
-  size_t sizes[24];  // bytes per region id (debug_region)
+  size_t sizes[32];  // bytes per region id (debug_region)
 };
 
 // Region ids (moe_fused_debug_region); the order of WsLayout's fields.
 enum Region : int {
   kRegStatus = 0, kRegCounts, kRegOffsets, kRegRowOf, kRegTkOfRow, kRegActive, kRegXq, kRegXScale,
   kRegXsq, kRegXsScale, kRegH, kRegX2, kRegS2, kRegY2, kRegSlots, kRegRowToken, kRegSharedRow,
-  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kRegRanges, kRegX1h, kRegX2h, kNumRegions
+  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kRegRanges, kRegX1h, kRegX2h, kRegDcnt, kNumRegions
 };
 
 constexpr int kMaxCtas = 1023;  // persistent grid size limit (one CTA per SM)
@@ -82,12 +83,14 @@ struct SlotTable {
 constexpr int kSmallRows = 8;     // experts with <= this many rows take the dp4a path ...
 constexpr int kSmallMaxK = 4096;  // ... when both contraction lengths are at most this
 constexpr int kTokenBlock = 128;  // token rows per big-phase work item (the MMA's N)
+constexpr int kDispChunk = 2048;  // flat (t, k) pairs per CTA of the multi-CTA dispatch
 
 // ---------------------------------------------------------------- params
 struct FwdParams {
   int32_t bs, h, E, topk, I, has_shared;
   int32_t share_uses_xq;  // shared quant identical to routed quant (same smooth vector)
   int32_t fold_routing;   // routing weight folded into the GEMM2 row scale; combine is a plain sum
+  int32_t disp_chunks;    // dispatch chunks of kDispChunk pairs; <= 1: one CTA dispatches alone
   int32_t with_tickets;   // dispatch resets the GEMM epilogue counters (forward path)
   int32_t small_rows;     // row count up to which an expert takes the dp4a path (0: never)
   int32_t num_ctas;       // grid of the GEMM launches (<= kMaxCtas)
@@ -120,14 +123,15 @@ __host__ __device__ inline T* ws_ptr(const FwdParams& p, size_t off) {
 // kernel ids (timing / status sites)
 enum KernelId : int {
   kKDispatchQuant = 0,
-  kKExpand = 1,
-  kKGemm1Small = 2,
-  kKGemm1Big = 3,
-  kKRequantBig = 4,
-  kKGemm2Small = 5,
-  kKGemm2Big = 6,
-  kKCombine = 7,
-  kNumKernels = 8
+  kKDispatchFinish = 1,
+  kKExpand = 2,
+  kKGemm1Small = 3,
+  kKGemm1Big = 4,
+  kKRequantBig = 5,
+  kKGemm2Small = 6,
+  kKGemm2Big = 7,
+  kKCombine = 8,
+  kNumKernels = 9
 };
 
 // TMA descriptors of the big-phase operands (built on the host per forward).
@@ -164,6 +168,7 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStr
 size_t dispatch_smem_bytes(int E);
 cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_expand(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_dispatch_finish(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_requant_big(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_combine(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_moe_gemm_small(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);

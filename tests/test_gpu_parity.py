@@ -124,3 +124,18 @@ def test_folded_routing_unfused_chain():
     inp = synth.make_inputs(wl)
     blk = make_block(wl, DEV, unfused=True, fold_routing=True)
     run_and_check(inp, DEV, staged=True, blk=blk)
+
+
+def test_multi_cta_dispatch_with_masks_and_skipped_ids():
+    """bs*topk = 4 * 2048 + 12: five dispatch chunks (the multi-CTA dispatch
+    and its finish kernel), masked tokens, skipped ids in different chunks,
+    experts spanning chunk boundaries, and experts of both GEMM paths."""
+    wl = synth.custom("multi_chunk", bs=2051, hidden=128, num_experts=12, topk=4, inter=64, has_shared=True,
+                      masked_fraction=0.1, smooth=True, seed=27)
+    inp = synth.make_inputs(wl)
+    inp.expert_ids[3, 1] = -1
+    inp.expert_ids[600, 0] = 12
+    inp.expert_ids[2050, 3] = 1 << 29
+    inp.expert_ids[1400, :] = -3
+    blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True)
+    check_raw_accumulators(blk, inp, ref, di, dw, DEV)
