@@ -593,7 +593,6 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int nw = gridDim.x * (blockDim.x >> 5);
-  const int n16 = p.h >> 4;
   const long nrows = static_cast<long>(total) * TB;
   for (long g = gw; g < nrows; g += nw) {
     const int b = static_cast<int>(g / TB), i = static_cast<int>(g % TB);
@@ -601,22 +600,24 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
     const int tb = b - tab.pre[sl];
     if (tb * TB + i >= tab.rows[sl]) continue;
     const int r = tab.row0[sl] + tb * TB + i;
-    const uint4* src = reinterpret_cast<const uint4*>((tab.exp[sl] >= 0 ? xq : xsq) +
+    // lane l converts codes 8 c .. 8 c + 7 for c = l, l + 32, ...: every warp
+    // store covers 512 contiguous bytes of the f16 row
+    const uint2* src = reinterpret_cast<const uint2*>((tab.exp[sl] >= 0 ? xq : xsq) +
                                                       static_cast<size_t>(row_token[r]) * p.h);
     uint4* dst = reinterpret_cast<uint4*>(x1h + static_cast<size_t>(r) * p.h);
-    for (int c0 = lane; c0 < n16; c0 += 4 * 32) {
-      uint4 v[4];
+    const int n8 = p.h >> 3;
+    for (int c0 = lane; c0 < n8; c0 += 4 * 32) {
+      uint2 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (c0 + 32 * u < n16) v[u] = src[c0 + 32 * u];
+        if (c0 + 32 * u < n8) v[u] = src[c0 + 32 * u];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int c = c0 + 32 * u;
-        if (c < n16) {
+        if (c < n8) {
           uint4 lo16, hi16;
-          int8x16_to_f16(v[u], lo16, hi16);
-          dst[2 * c] = lo16;
-          dst[2 * c + 1] = hi16;
+          int8x16_to_f16(make_uint4(v[u].x, v[u].y, 0u, 0u), lo16, hi16);
+          dst[c] = lo16;
         }
       }
     }
@@ -626,8 +627,8 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
 // SwiGLU and requant of the rows of big blocks (FusedDeepMoE analysis §6.1
 // and §7.2), one warp per row: h = (g / (1 + exp(-g))) * u from the row's
 // dequantised gate | up halves, amax = max(max|h|, 1e-4), s2 = amax * (1/127),
-// q = RNE((h * 127) * (1/amax)); writes the int8 codes, their f16 copy (the
-// tensor-core GEMM2 operand) and s2.  Rows up to I = 2048 keep h in shared
+// q = RNE((h * 127) * (1/amax)); writes the codes as f16 (the tensor-core
+// GEMM2 operand, exact) and s2.  Rows up to I = 2048 keep h in shared
 // memory between the two passes; longer rows recompute it in the second.
 __device__ __forceinline__ float swiglu_1(float g, float u) {
   const float d = __fadd_rn(1.0f, expf(-g));
@@ -636,16 +637,13 @@ __device__ __forceinline__ float swiglu_1(float g, float u) {
 __device__ __forceinline__ float4 swiglu_4(float4 g, float4 u) {
   return make_float4(swiglu_1(g.x, u.x), swiglu_1(g.y, u.y), swiglu_1(g.z, u.z), swiglu_1(g.w, u.w));
 }
-__device__ __forceinline__ void quant_store4(float4 v, float inv, int c, uint32_t* q4, __half2* h2) {
+// the codes of big rows are stored only as f16 (exact): the tensor-core GEMM2
+// reads nothing else
+__device__ __forceinline__ void quant_store4(float4 v, float inv, int c, __half2* h2) {
   const float f[4] = {v.x, v.y, v.z, v.w};
   int8_t q[4];
-  uint32_t packed = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    q[j] = f32_to_q(__fmul_rn(__fmul_rn(f[j], 127.0f), inv));
-    packed |= static_cast<uint32_t>(static_cast<uint8_t>(q[j])) << (8 * j);
-  }
-  q4[c] = packed;
+  for (int j = 0; j < 4; ++j) q[j] = f32_to_q(__fmul_rn(__fmul_rn(f[j], 127.0f), inv));
   h2[2 * c] = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
   h2[2 * c + 1] = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
 }
@@ -669,7 +667,6 @@ __global__ void __launch_bounds__(kRqWarps * 32) requant_big_kernel(FwdParams p)
   const BigSlots tab =
       stage_big_slots(p, slots, reinterpret_cast<int32_t*>(rq_smem + (staged ? kRqWarps * (kRqMaxI / 4) : 0)));
   const float* hbuf = ws_ptr<float>(p, p.L.hbuf);
-  int8_t* x2 = ws_ptr<int8_t>(p, p.L.x2);
   __half* x2h = ws_ptr<__half>(p, p.L.x2h);
   float* s2 = ws_ptr<float>(p, p.L.s2);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -685,7 +682,6 @@ __global__ void __launch_bounds__(kRqWarps * 32) requant_big_kernel(FwdParams p)
     const int r = tab.row0[sl] + tb * TB + i;
     const float4* gr = reinterpret_cast<const float4*>(hbuf + static_cast<size_t>(r) * (2 * I));
     const float4* ur = gr + n4;
-    uint32_t* q4 = reinterpret_cast<uint32_t*>(x2 + static_cast<size_t>(r) * I);
     __half2* h2 = reinterpret_cast<__half2*>(x2h + static_cast<size_t>(r) * I);
     // pass 1: h = SwiGLU(g, u) (into shared memory when the row fits) and amax;
     // four g / u pairs of loads in flight per lane before any is used
@@ -717,7 +713,7 @@ __global__ void __launch_bounds__(kRqWarps * 32) requant_big_kernel(FwdParams p)
     // pass 2: codes (h from shared memory, or recomputed for long rows)
     for (int c = lane; c < n4; c += 32) {
       const float4 hv = staged ? hrow[c] : swiglu_4(gr[c], ur[c]);
-      quant_store4(hv, inv, c, q4, h2);
+      quant_store4(hv, inv, c, h2);
     }
     __syncwarp();  // this warp's h row is reused by its next row
     if (lane == 0) s2[r] = __fmul_rn(amax, 1.0f / 127.0f);

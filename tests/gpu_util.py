@@ -177,8 +177,16 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
                 acc = ref["share_acc1"][act].to(torch.float32)
                 want = (acc * inp.share_w1_scale.to(torch.float32).view(1, -1)) * xs_sh.view(-1, 1)
                 assert torch.equal(hb[bs * K:bs * K + S], want), "gate | up shared (tensor-core rows)"
-        # requant
-        x2 = region(blk, "x2", torch.int8, (rows, I))
+        # requant: dp4a rows keep int8 codes (x2); tensor-core rows keep them
+        # only as exact f16 values (x2h, the tensor-core GEMM2 operand)
+        x2 = region(blk, "x2", torch.int8, (rows, I)).clone()
+        x2h = region(blk, "x2h", torch.int16, (rows, I)).view(torch.float16).to(torch.int8)
+        shared_big = bool(S) and not (small_ok and S <= SMALL_ROWS)
+        row_big = torch.zeros(rows, dtype=torch.bool)
+        row_big[:R] = big_row
+        if shared_big:
+            row_big[bs * K:bs * K + S] = True
+        x2[row_big] = x2h[row_big]
         s2 = region(blk, "s2", torch.float32, (rows,))
         assert_codes_close(x2[:R], ref["x2"], "x2 routed")
         assert_rel(s2[:R], ref["s2"], H_REL, "s2 routed")
