@@ -153,6 +153,20 @@ __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddep
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+// Named barrier that also returns the OR of a predicate over its threads,
+// so that a decision taken after it (stop on an error) is uniform.
+__device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
 
 // ------------------------------------------------------------ TMA tensor
 // 2-D tiled bulk tensor copy global -> shared, completing bytes on `bar`.

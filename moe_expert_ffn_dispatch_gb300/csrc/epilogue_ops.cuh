@@ -20,6 +20,7 @@ constexpr float kAmaxEps = 1e-4f;
 constexpr float kInv127 = 1.0f / 127.0f;  // the fp32 nearest to 1/127
 
 __device__ __forceinline__ void consumer_sync() { named_barrier_sync(1, kConsumers); }
+__device__ __forceinline__ bool consumer_sync_or(bool pred) { return named_barrier_or(1, kConsumers, pred); }
 
 __device__ __forceinline__ void mbar_inval(uint64_t* bar) {
   asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");

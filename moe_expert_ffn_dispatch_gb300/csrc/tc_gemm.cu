@@ -30,6 +30,9 @@
 //   warp 0      TMA of the int8 weight boxes into a 6-deep staging ring
 //   warp 2      TMA of the f16 token boxes (128-byte swizzle) into a 4-deep
 //               ring; 16-row boxes when the block has at most 64 rows
+//   warp 3      item scheduler: decodes the CTA's work items (slot-table
+//               search, a chain of dependent global loads) into a 4-deep
+//               shared-memory ring that the other roles read
 //   warps 4..7  convert int8 weight stages to f16, one weight row per
 //               thread, into a 4-deep ring in tensor memory (the MMA's A
 //               operand), which keeps the f16 weights off shared memory
@@ -61,6 +64,7 @@ constexpr int CHUNK_KB = 1024 / KB;   // stages per exact accumulation chunk (10
 constexpr int S8 = 6;                 // int8 weight staging ring (from HBM)
 constexpr int SA = 4;                 // f16 weight ring in tensor memory (converted in the CTA)
 constexpr int SB = 4;                 // f16 token ring (from L2)
+constexpr int SI = 4;                 // decoded work-item ring (item scheduler -> the other roles)
 constexpr int kAccCols = 2 * TB;      // two fp32 accumulators of TB columns
 constexpr int kAStageCols = KB / 2;   // one f16 weight stage: 128 lanes x 64 columns of f16 pairs
 constexpr int kTmemCols = 512;        // kAccCols + SA * kAStageCols, rounded to a power of two
@@ -69,7 +73,7 @@ constexpr int kSmallBox = 16;         // rows of the narrow token box
 
 constexpr int kBigWarps = 16;
 constexpr int kBigThreads = kBigWarps * 32;
-constexpr int kWarpA = 0, kWarpMma = 1, kWarpB = 2;
+constexpr int kWarpA = 0, kWarpMma = 1, kWarpB = 2, kWarpSched = 3;
 constexpr int kConvWarp0 = 4, kConvWarps = 4;
 constexpr int kEpiWarp0 = 8;          // epilogue warps 8..15 = the 256 "consumer" threads
 
@@ -79,17 +83,19 @@ constexpr int F16_TILE = ATOMS * F16_ATOM;           // 32 KB
 constexpr int OFF_B16 = 0;                           // SB x ATOMS x [128][64] f16, swizzled (TMA)
 constexpr int OFF_A8 = OFF_B16 + SB * F16_TILE;      // S8 x [128][128] int8, swizzled (TMA)
 constexpr int OFF_BAR = OFF_A8 + S8 * A8_BYTES;
-constexpr int NBAR = 2 * S8 + 2 * SA + 2 * SB + 4;
+constexpr int NBAR = 2 * S8 + 2 * SA + 2 * SB + 4 + 2 * SI;
 constexpr int OFF_INFO = OFF_BAR + NBAR * 8;         // tok_scale, tok_row, tok_tok [TB]
-constexpr int OFF_MISC = OFF_INFO + 3 * TB * 4;      // tmem slot, abort flag
+constexpr int OFF_ITEM = OFF_INFO + 3 * TB * 4;      // SI decoded items, 8 ints each
+constexpr int OFF_MISC = OFF_ITEM + SI * 8 * 4;      // tmem slot, abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 16;
+constexpr int kItemReaders = 4;                      // weight TMA, token TMA, MMA, epilogue
 static_assert(KB == 128 && KA == 64, "the MMA loop issues two atoms of four K16 steps per stage");
 static_assert(OFF_B16 % 1024 == 0 && OFF_A8 % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
 
 struct BigItem {
-  int slot, e, row0, rows, tb, jt;
+  int slot, e, row0, rows, tb, jt, mblk;
 };
 
 __device__ __forceinline__ BigItem decode_item(long it, int J, const int32_t* slots, int E) {
@@ -114,6 +120,22 @@ __device__ __forceinline__ BigItem decode_item(long it, int J, const int32_t* sl
   x.rows = s_rows[lo];
   x.jt = static_cast<int>(local / T);
   x.tb = static_cast<int>(local % T);
+  x.mblk = min(TB, x.rows - x.tb * TB);
+  return x;
+}
+
+// Decoded items pass from the scheduler warp to the other roles through a
+// shared-memory ring (one 8-int entry per item): the decode's chain of
+// dependent global loads then runs ahead of the pipeline instead of stalling
+// every role at each item boundary.
+__device__ __forceinline__ void put_item(int32_t* ent, const BigItem& x) {
+  ent[0] = x.slot; ent[1] = x.e; ent[2] = x.row0; ent[3] = x.rows;
+  ent[4] = x.tb; ent[5] = x.jt; ent[6] = x.mblk;
+}
+__device__ __forceinline__ BigItem get_item(const volatile int32_t* ent) {
+  BigItem x;
+  x.slot = ent[0]; x.e = ent[1]; x.row0 = ent[2]; x.rows = ent[3];
+  x.tb = ent[4]; x.jt = ent[5]; x.mblk = ent[6];
   return x;
 }
 
@@ -150,6 +172,9 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   uint64_t* b_empty = b_full + SB;
   uint64_t* acc_full = b_empty + SB;
   uint64_t* acc_empty = acc_full + 2;
+  uint64_t* it_full = acc_empty + 2;
+  uint64_t* it_empty = it_full + SI;
+  volatile int32_t* items = reinterpret_cast<volatile int32_t*>(smem + OFF_ITEM);
   float* tok_scale = reinterpret_cast<float*>(smem + OFF_INFO);
   int32_t* tok_row = reinterpret_cast<int32_t*>(smem + OFF_INFO) + TB;
   int32_t* tok_tok = tok_row + TB;
@@ -189,6 +214,10 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], kBigWarps - kEpiWarp0);
     }
+    for (int s = 0; s < SI; ++s) {
+      mbar_init(&it_full[s], 1);
+      mbar_init(&it_empty[s], kItemReaders);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -201,18 +230,39 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   // The single-issuer roles (the two TMA producers and the MMA issuer) run
   // their loops on the whole warp, so every address and descriptor is
   // warp-uniform; one elected lane issues the copies and tensor-core work.
-  if (aligned && warp == kWarpA) {
+  // Every role walks the same item sequence (blockIdx.x, + gridDim.x, ...)
+  // and takes each item's decoded form from the scheduler's ring.
+  int si = 0;
+  uint32_t pi = 0;
+  if (aligned && warp == kWarpSched) {
+    // ------------------------------------------------------- item scheduler
+    bool wrapped = false;
+    for (long it = blockIdx.x; it < total; it += gridDim.x) {
+      const BigItem x = decode_item(it, J, slots, p.E);
+      if (wrapped &&
+          !__all_sync(0xffffffffu, mbar_wait_bounded(&it_empty[si], pi ^ 1u, abort_flag, status, site + 9, false)))
+        break;
+      if (lane == 0) {
+        put_item(const_cast<int32_t*>(items) + 8 * si, x);
+        mbar_arrive(&it_full[si]);
+      }
+      __syncwarp();
+      if (++si == SI) { si = 0; pi ^= 1u; wrapped = true; }
+    }
+  } else if (aligned && warp == kWarpA) {
     // ---------------------------------------------------- weight TMA (int8)
-    const void* map = G1 ? &maps.a1 : &maps.a2;
-    const void* map_s = G1 ? &maps.a1s : &maps.a2s;
     int s = 0;
     uint32_t ph = 0;
     bool wrapped = false;
     for (long it = blockIdx.x; it < total; it += gridDim.x) {
-      const BigItem x = decode_item(it, J, slots, p.E);
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&it_full[si], pi, abort_flag, status, site + 10))) goto done_a;
+      const BigItem x = get_item(items + 8 * si);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[si]);
+      if (++si == SI) { si = 0; pi ^= 1u; }
       const bool sh = x.e < 0;
       const int rbase = sh ? 0 : x.e * NW;
-      const void* mp = sh ? map_s : map;
+      const void* mp = sh ? (G1 ? &maps.a1s : &maps.a2s) : (G1 ? &maps.a1 : &maps.a2);
       for (int kb = 0; kb < n_kb; ++kb) {
         if (wrapped &&
             !__all_sync(0xffffffffu, mbar_wait_bounded(&a8_empty[s], ph ^ 1u, abort_flag, status, site + 1, false)))
@@ -239,18 +289,22 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   done_a:;
   } else if (aligned && warp == kWarpB) {
     // ---------------------------------------------------- token TMA (f16)
-    const void* map = G1 ? &maps.b1 : &maps.b2;
-    const void* map_n = G1 ? &maps.b1n : &maps.b2n;
     int s = 0;
     uint32_t ph = 0;
     bool wrapped = false;
     for (long it = blockIdx.x; it < total; it += gridDim.x) {
-      const BigItem x = decode_item(it, J, slots, p.E);
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&it_full[si], pi, abort_flag, status, site + 10))) goto done_b;
+      const BigItem x = get_item(items + 8 * si);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[si]);
+      if (++si == SI) { si = 0; pi ^= 1u; }
       const int r0 = x.row0 + x.tb * TB;
-      const int mblk = min(TB, x.rows - x.tb * TB);
+      const int mblk = x.mblk;
       // narrow boxes for short blocks: the MMA reads only the first mblk rows
       const int nbox = mblk > 64 ? 1 : (mblk + kSmallBox - 1) / kSmallBox;
       const uint32_t bytes = ATOMS * (mblk > 64 ? F16_ATOM : nbox * kSmallBox * KA * 2);
+      const void* map = G1 ? &maps.b1 : &maps.b2;
+      const void* map_n = G1 ? &maps.b1n : &maps.b2n;
       for (int kb = 0; kb < n_kb; ++kb) {
         if (wrapped &&
             !__all_sync(0xffffffffu, mbar_wait_bounded(&b_empty[s], ph ^ 1u, abort_flag, status, site + 2, false)))
@@ -289,8 +343,9 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     bool ok = true;
     for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
       for (int kb = 0; kb < n_kb; ++kb) {
-        ok = mbar_wait_bounded(&a8_full[s8], p8, abort_flag, status, site + 3);
-        if (ok && wrapped) ok = mbar_wait_bounded(&a16_empty[sa], pa ^ 1u, abort_flag, status, site + 4);
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a8_full[s8], p8, abort_flag, status, site + 3));
+        if (ok && wrapped)
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a16_empty[sa], pa ^ 1u, abort_flag, status, site + 4));
         if (ok) {
           tc_fence_after();
           const char* src = smem + OFF_A8 + s8 * A8_BYTES + row * KB;
@@ -344,8 +399,11 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     long acc_n = 0;
     bool ok = true;
     for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
-      const BigItem x = decode_item(it, J, slots, p.E);
-      const int mblk = min(TB, x.rows - x.tb * TB);
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&it_full[si], pi, abort_flag, status, site + 10))) break;
+      const int mblk = items[8 * si + 6];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[si]);
+      if (++si == SI) { si = 0; pi ^= 1u; }
       const uint32_t idesc = umma_idesc_f16(BM, (mblk + 15) & ~15);
       uint32_t d_tmem = tmem;
       int kc = 0;  // stage inside the current 1024-K chunk
@@ -442,11 +500,17 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     float* hbuf = ws_ptr<float>(p, p.L.hbuf);
     uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
     long acc_n = 0;
-    for (long it = blockIdx.x; it < total; it += gridDim.x) {
-      const BigItem x = decode_item(it, J, slots, p.E);
+    for (long it = blockIdx.x; it < total && aligned; it += gridDim.x) {
+      const bool got = mbar_wait_bounded(&it_full[si], pi, abort_flag, status, site + 10);
+      const BigItem x = get_item(items + 8 * si);
+      // the previous item's epilogue is done with the token info, and every
+      // thread has read the ring entry
+      const bool failed = consumer_sync_or(!got || *abort_flag != 0);
+      if (ctid == 0) mbar_arrive(&it_empty[si]);
+      if (++si == SI) { si = 0; pi ^= 1u; }
+      if (failed) break;
       const int tok0 = x.tb * TB;
-      const int mblk = min(TB, x.rows - tok0);
-      consumer_sync();  // the previous item's epilogue is done with the token info
+      const int mblk = x.mblk;
       if (ctid < mblk) {
         const int r = x.row0 + tok0 + ctid;
         const int t = row_token[r];
@@ -461,10 +525,10 @@ __global__ void __launch_bounds__(kBigThreads, 1)
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = 0;
       const int n_chunks = (n_kb + CHUNK_KB - 1) / CHUNK_KB;
-      bool ok = aligned;
+      bool ok = true;
       for (int c = 0; c < n_chunks && ok; ++c, ++acc_n) {
         const int buf = static_cast<int>(acc_n & 1);
-        ok = mbar_wait_bounded(&acc_full[buf], (acc_n >> 1) & 1, abort_flag, status, site + 8);
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[buf], (acc_n >> 1) & 1, abort_flag, status, site + 8));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -480,9 +544,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
       }
-      consumer_sync();
-      const bool stop = *abort_flag != 0;  // a failed wait raised it before this barrier
-      if (!aligned) break;
+      const bool stop = consumer_sync_or(*abort_flag != 0);  // uniform over the epilogue threads
       // GEMM1: output column of this lane's gate / up pair; GEMM2: output column
       const int col = G1 ? x.jt * 64 + 16 * q + (lane & 15) : x.jt * BM + m;
       if (RAW) {
