@@ -37,8 +37,9 @@
 //               thread, into a 4-deep ring in tensor memory (the MMA's A
 //               operand), which keeps the f16 weights off shared memory
 //   warp 1      one thread issues tcgen05.mma (M128, N = rows rounded to 16,
-//               K16) into two tensor-memory accumulators, alternating per
-//               1024 of K, and commits to the ring and accumulator barriers
+//               K16) stage by stage into two tensor-memory accumulators,
+//               alternating per 1024 of K, and commits to the ring and
+//               accumulator barriers
 //   warps 8..15 drain accumulators (tcgen05.ld) into int32, then the
 //               epilogue (GEMM1: dequantised gate | up values, SwiGLU
 //               being applied by the requant kernel; GEMM2: bf16 dequant);
@@ -382,16 +383,15 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     }
   } else if (aligned && warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
-    // Two 128-K stages per iteration (one at the end of an odd count): wait
-    // for both stages' operands, then one elected lane issues their sixteen
-    // MMAs and the commits.  The issuing warp's fixed cost per iteration is
-    // several hundred cycles, so pairing stages halves it per unit of tensor
-    // work.  Pairs never straddle a 1024-K chunk (CHUNK_KB is even).  Ring
-    // slots and phases are running counters; the token descriptor advances
-    // by addition in its address field (16-byte units: +2 per K16 step,
-    // +1024 per 16 KB atom); the weight operand is read from tensor memory,
-    // 8 columns per K16 step.
-    static_assert(CHUNK_KB % 2 == 0, "stage pairs must not straddle an accumulation chunk");
+    // One 128-K stage per iteration: wait for its weight slot (tensor
+    // memory) and token stage (shared memory), then one elected lane issues
+    // its eight K16 MMAs and commits the slot, the stage and, at the end of
+    // a 1024-K chunk, the accumulator.  Issuing stage by stage releases each
+    // weight slot as early as possible, which keeps the converters ahead.
+    // Ring slots and phases are running counters; the token descriptor
+    // advances by addition in its address field (16-byte units: +2 per K16
+    // step, +1024 per 16 KB atom); the weight operand is read from tensor
+    // memory, 8 columns per K16 step.
     const uint32_t a_tmem0 = tmem + kAccCols;
     const uint64_t b_desc0 = umma_desc_sw128(smem_u32(smem + OFF_B16));
     int sa = 0, sb = 0;
@@ -407,8 +407,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       const uint32_t idesc = umma_idesc_f16(BM, (mblk + 15) & ~15);
       uint32_t d_tmem = tmem;
       int kc = 0;  // stage inside the current 1024-K chunk
-      for (int kb = 0; kb < n_kb; kb += 2) {
-        const bool pair = kb + 1 < n_kb;
+      for (int kb = 0; kb < n_kb; ++kb) {
         if (kc == 0) {
           const int buf = static_cast<int>(acc_n & 1);
           d_tmem = tmem + buf * TB;
@@ -419,69 +418,38 @@ __global__ void __launch_bounds__(kBigThreads, 1)
             break;
           }
         }
-        const int sa1 = sa + 1 == SA ? 0 : sa + 1, sb1 = sb + 1 == SB ? 0 : sb + 1;
-        const uint32_t pa1 = sa + 1 == SA ? pa ^ 1u : pa, pb1 = sb + 1 == SB ? pb ^ 1u : pb;
-        bool w = mbar_wait_bounded(&a16_full[sa], pa, abort_flag, status, site + 6) &&
-                 mbar_wait_bounded(&b_full[sb], pb, abort_flag, status, site + 7);
-        if (pair)
-          w = w && mbar_wait_bounded(&a16_full[sa1], pa1, abort_flag, status, site + 6) &&
-              mbar_wait_bounded(&b_full[sb1], pb1, abort_flag, status, site + 7);
+        const bool w = mbar_wait_bounded(&a16_full[sa], pa, abort_flag, status, site + 6) &&
+                       mbar_wait_bounded(&b_full[sb], pb, abort_flag, status, site + 7);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int nst = pair ? 2 : 1;
-        const bool last = (kc + nst == CHUNK_KB || kb + nst >= n_kb);
+        const bool last = (kc + 1 == CHUNK_KB || kb + 1 == n_kb);
         if (elect_one()) {
           constexpr uint64_t kAtom = F16_ATOM >> 4;
-          {
-            const uint32_t at = a_tmem0 + sa * kAStageCols;
-            const uint64_t bd = b_desc0 + static_cast<uint64_t>(sb * (F16_TILE >> 4));
-            umma_f16_ts(d_tmem, at, bd, idesc, kc != 0 ? 1u : 0u);
-            umma_f16_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 32, bd + kAtom, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 40, bd + kAtom + 2, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
-            umma_commit(&a16_empty[sa]);
-            umma_commit(&b_empty[sb]);
-          }
-          if (pair) {
-            const uint32_t at = a_tmem0 + sa1 * kAStageCols;
-            const uint64_t bd = b_desc0 + static_cast<uint64_t>(sb1 * (F16_TILE >> 4));
-            umma_f16_ts(d_tmem, at, bd, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 32, bd + kAtom, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 40, bd + kAtom + 2, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
-            umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
-            umma_commit(&a16_empty[sa1]);
-            umma_commit(&b_empty[sb1]);
-          }
+          const uint32_t at = a_tmem0 + sa * kAStageCols;
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>(sb * (F16_TILE >> 4));
+          umma_f16_ts(d_tmem, at, bd, idesc, kc != 0 ? 1u : 0u);
+          umma_f16_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 32, bd + kAtom, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 40, bd + kAtom + 2, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
+          umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
+          umma_commit(&a16_empty[sa]);
+          umma_commit(&b_empty[sb]);
           if (last) umma_commit(&acc_full[acc_n & 1]);
         }
         __syncwarp();
-        if (pair) {
-          sa = sa1 + 1 == SA ? 0 : sa1 + 1;
-          pa = sa1 + 1 == SA ? pa1 ^ 1u : pa1;
-          sb = sb1 + 1 == SB ? 0 : sb1 + 1;
-          pb = sb1 + 1 == SB ? pb1 ^ 1u : pb1;
-        } else {
-          sa = sa1;
-          pa = pa1;
-          sb = sb1;
-          pb = pb1;
-        }
+        if (++sa == SA) { sa = 0; pa ^= 1u; }
+        if (++sb == SB) { sb = 0; pb ^= 1u; }
         if (last) {
           ++acc_n;
           kc = 0;
         } else {
-          kc += nst;
+          ++kc;
         }
       }
     }
