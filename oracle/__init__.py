@@ -47,7 +47,8 @@ class OracleArgs(ctypes.Structure):
                 ("w1", P), ("w1_scale", P), ("w2", P), ("w2_scale", P),
                 ("share_w1", P), ("share_w1_scale", P), ("share_w2", P), ("share_w2_scale", P),
                 ("smooth", P), ("share_smooth", P), ("mask", P), ("token_sample", P),
-                ("threads", I32), ("fold_routing", I32)]
+                ("threads", I32), ("fold_routing", I32),
+                ("act_fp16", I32), ("scale_dtype", I32), ("smooth_per_expert", I32)]
 
 
 class OracleOut(ctypes.Structure):
@@ -83,6 +84,10 @@ def lib():
         L.oracle_bf16_to_f32.restype = ctypes.c_float
         L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
         L.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        L.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+        L.oracle_f16_to_f32.restype = ctypes.c_float
+        L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_f16.restype = ctypes.c_uint16
         L.oracle_sizeof_args.restype = ctypes.c_int
         L.oracle_sizeof_out.restype = ctypes.c_int
         assert L.oracle_sizeof_args() == ctypes.sizeof(OracleArgs)
@@ -99,12 +104,25 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 
 def _bits(x: torch.Tensor) -> torch.Tensor:
-    """bf16 tensor -> its raw 16-bit patterns (int16 view), contiguous CPU."""
+    """bf16 / fp16 tensor -> its raw 16-bit patterns (int16 view), contiguous CPU."""
     return x.detach().to("cpu").contiguous().view(torch.int16)
 
 
 def _bf16(bits: torch.Tensor) -> torch.Tensor:
     return bits.view(torch.bfloat16)
+
+
+def _act(bits: torch.Tensor, fp16: bool) -> torch.Tensor:
+    return bits.view(torch.float16 if fp16 else torch.bfloat16)
+
+
+_SCALE_DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+
+
+def _scales(t: torch.Tensor) -> torch.Tensor:
+    """Weight scales as stored: fp32 values, or the raw bits of bf16 / fp16."""
+    t = t.detach().to("cpu").contiguous()
+    return t if t.dtype == torch.float32 else t.view(torch.int16)
 
 
 # ----------------------------------------------------------- step functions
@@ -187,6 +205,15 @@ def bf16_round(v: float) -> int:
     return int(lib().oracle_f32_to_bf16(v)) & 0xFFFF
 
 
+def f16_round(v: float) -> int:
+    """fp16 code of v (round to nearest, ties to even)."""
+    return int(lib().oracle_f32_to_f16(v)) & 0xFFFF
+
+
+def f16_value(code: int) -> float:
+    return float(lib().oracle_f16_to_f32(code & 0xFFFF))
+
+
 # ------------------------------------------------------------- full block
 def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tensor] = None,
             threads: Optional[int] = None, expert_weights=None, fold_routing: bool = False) -> Dict:
@@ -197,8 +224,11 @@ def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tenso
     `token_sample` (bool [bs]) restricts the GEMM work and the outputs to those
     tokens; dispatch still runs on every token.  `fold_routing` selects the
     mode in which each routed row's routing weight is folded into its GEMM2
-    row scale and the combine is a plain sum.  Returns a dict of tensors
-    (bf16 outputs as bf16 tensors).
+    row scale and the combine is a plain sum.  The signature variants follow
+    the inputs' own dtypes and shapes: fp16 x gives fp16 y2 and outputs,
+    bf16 / fp16 routed weight scales are widened exactly, and a [E, h]
+    smooth tensor makes the routed quant per row.  Returns a dict of tensors
+    (outputs in x's dtype).
     """
     wl = inp.wl
     bs, h, E, K, I = wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter
@@ -206,6 +236,11 @@ def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tenso
     if threads is None:
         threads = int(os.environ.get("ORACLE_THREADS", os.cpu_count() or 1))
     x = _bits(inp.x)
+    fp16 = inp.x.dtype == torch.float16
+    if inp.w1_scale.dtype != inp.w2_scale.dtype:
+        raise ValueError("routed weight scales must share one dtype")
+    scale_dtype = _SCALE_DTYPES[inp.w1_scale.dtype]
+    per_expert = inp.smooth is not None and inp.smooth.dim() == 2
     ids = inp.expert_ids.to(torch.int32).contiguous()
     sc = inp.expert_scales.to(torch.float32).contiguous()
     mask = None if inp.mask is None else inp.mask.to(torch.uint8).contiguous()
@@ -241,8 +276,8 @@ def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tenso
         keep += [a, b]
         w1p[e] = a.data_ptr(); w2p[e] = b.data_ptr()
 
-    w1s = inp.w1_scale.to(torch.float32).contiguous()
-    w2s = inp.w2_scale.to(torch.float32).contiguous()
+    w1s = _scales(inp.w1_scale)
+    w2s = _scales(inp.w2_scale)
     sw1 = sw2 = sw1s = sw2s = None
     if shared:
         sw1, sw2 = host_weights(E)
@@ -255,7 +290,8 @@ def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tenso
     a = OracleArgs(bs, h, E, K, I, int(shared), _ptr(x), _ptr(ids), _ptr(sc),
                    ctypes.addressof(w1p), _ptr(w1s), ctypes.addressof(w2p), _ptr(w2s),
                    _ptr(sw1), _ptr(sw1s), _ptr(sw2), _ptr(sw2s), _ptr(smooth), _ptr(ssmooth),
-                   _ptr(mask), _ptr(samp), threads, int(bool(fold_routing)))
+                   _ptr(mask), _ptr(samp), threads, int(bool(fold_routing)),
+                   int(fp16), scale_dtype, int(per_expert))
 
     res = {}
     res["output"] = torch.zeros(bs, h, dtype=torch.int16)
@@ -269,8 +305,9 @@ def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tenso
         res["offsets"] = torch.zeros(E + 1, dtype=torch.int32)
         res["row_of"] = torch.full((bs, K), -1, dtype=torch.int32)
         res["tk_of_row"] = torch.full((max(nrows, 1),), -1, dtype=torch.int32)
-        res["x_q"] = torch.zeros(bs, h, dtype=torch.int8)
-        res["x_scale"] = torch.zeros(bs, dtype=torch.float32)
+        nq = nrows if per_expert else bs   # per routed row with [E, h] smooth scales
+        res["x_q"] = torch.zeros(max(nq, 1), h, dtype=torch.int8)
+        res["x_scale"] = torch.zeros(max(nq, 1), dtype=torch.float32)
         res["acc1"] = torch.zeros(nrows, 2 * I, dtype=torch.int32)
         res["h"] = torch.zeros(nrows, I, dtype=torch.float32)
         res["x2"] = torch.zeros(nrows, I, dtype=torch.int8)
@@ -297,12 +334,15 @@ def forward(inp, intermediates: bool = False, token_sample: Optional[torch.Tenso
     R = o.R
     res["R"] = R
     res["skipped"] = o.skipped
-    res["output"] = _bf16(res["output"])
+    res["output"] = _act(res["output"], fp16)
     if shared:
-        res["share_output"] = _bf16(res["share_output"])
+        res["share_output"] = _act(res["share_output"], fp16)
     if intermediates:
         res["tk_of_row"] = res["tk_of_row"][:R]
         for name in ("acc1", "h", "x2", "s2", "acc2"):
             res[name] = res[name][:R]
-        res["y2"] = _bf16(res["y2"][:R])
+        if per_expert:
+            res["x_q"] = res["x_q"][:R]
+            res["x_scale"] = res["x_scale"][:R]
+        res["y2"] = _act(res["y2"][:R], fp16)
     return res

@@ -134,6 +134,9 @@ class Workload:
     smooth: bool = False              # expert_smooth_scales U(0.8, 1.2)
     share_smooth: bool = False        # share_smooth_scales U(0.8, 1.2)
     seed: int = 1000
+    act_dtype: str = "bf16"           # x (and the outputs): bf16 | fp16
+    scale_dtype: str = "f32"          # routed weight scales: f32 | bf16 | fp16
+    smooth_per_expert: bool = False   # expert_smooth_scales [E, h] instead of [h]
 
 
 WORKLOADS: Dict[str, Workload] = {
@@ -153,7 +156,9 @@ class MoeInputs:
     x [bs,h] bf16, expert_ids [bs,k] int32, expert_scales [bs,k] f32,
     w1 [E,2I,h] int8 (rows 0..I-1 gate, I..2I-1 up), w1_scale [E,2I] f32,
     w2 [E,h,I] int8, w2_scale [E,h] f32, shared weights without the E axis,
-    smooth scales [h] f32, x_active_mask [bs] bool."""
+    smooth scales [h] f32, x_active_mask [bs] bool.  Signature variants: x
+    fp16; routed weight scales bf16 / fp16 (the f32 draw cast once);
+    expert smooth scales [E, h]."""
     wl: Workload
     x: torch.Tensor
     expert_ids: torch.Tensor
@@ -247,7 +252,8 @@ def make_inputs(wl: Workload, weight_device="cpu", with_weights: bool = True) ->
     """Draw every input of `wl`.  With with_weights=False the big INT8 weight tensors
     are left out (w1 = w2 = None); redraw them per expert with draw_w1/draw_w2."""
     seed, bs, h, E, k, I = wl.seed, wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter
-    x = normal(seed, S_X1, S_X2, 0, bs * h).view(bs, h).to(torch.bfloat16)
+    act = {"bf16": torch.bfloat16, "fp16": torch.float16}[wl.act_dtype]
+    x = normal(seed, S_X1, S_X2, 0, bs * h).view(bs, h).to(act)
 
     if wl.routing == "uniform":
         ids = _route_uniform(wl)
@@ -261,8 +267,9 @@ def make_inputs(wl: Workload, weight_device="cpu", with_weights: bool = True) ->
     logits = normal(seed, S_LOGITS1, S_LOGITS2, 0, bs * k).view(bs, k)
     scales = torch.softmax(logits, dim=1).to(torch.float32).contiguous()
 
-    w1s = _channel_scales(seed, S_W1S, E, 2 * I, h)
-    w2s = _channel_scales(seed, S_W2S, E, h, I)
+    sdt = {"f32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[wl.scale_dtype]
+    w1s = _channel_scales(seed, S_W1S, E, 2 * I, h).to(sdt)
+    w2s = _channel_scales(seed, S_W2S, E, h, I).to(sdt)
     w1 = draw_all_w1(wl, weight_device) if with_weights else None
     w2 = draw_all_w2(wl, weight_device) if with_weights else None
 
@@ -273,7 +280,9 @@ def make_inputs(wl: Workload, weight_device="cpu", with_weights: bool = True) ->
         inp.share_w1_scale = _channel_scales(seed, S_W1S, 1, 2 * I, h, start=E * 2 * I).view(2 * I)
         inp.share_w2_scale = _channel_scales(seed, S_W2S, 1, h, I, start=E * h).view(h)
     if wl.smooth:
-        inp.smooth = (0.8 + 0.4 * uniform01(seed, S_SMOOTH, 0, h)).to(torch.float32)
+        n = E * h if wl.smooth_per_expert else h
+        sm = (0.8 + 0.4 * uniform01(seed, S_SMOOTH, 0, n)).to(torch.float32)
+        inp.smooth = sm.view(E, h) if wl.smooth_per_expert else sm
     if wl.share_smooth:
         inp.share_smooth = (0.8 + 0.4 * uniform01(seed, S_SSMOOTH, 0, h)).to(torch.float32)
     if wl.masked_fraction > 0:
@@ -286,10 +295,12 @@ def make_inputs(wl: Workload, weight_device="cpu", with_weights: bool = True) ->
 
 
 def custom(name="custom", bs=8, hidden=256, num_experts=8, topk=2, inter=128, has_shared=False,
-           routing="uniform", masked_fraction=0.0, smooth=False, share_smooth=False, seed=7) -> Workload:
+           routing="uniform", masked_fraction=0.0, smooth=False, share_smooth=False, seed=7,
+           act_dtype="bf16", scale_dtype="f32", smooth_per_expert=False) -> Workload:
     """A workload with arbitrary shapes (tests use these for ragged and edge cases)."""
     return Workload(name, bs, hidden, num_experts, topk, inter, has_shared, routing,
-                    masked_fraction, smooth, share_smooth, seed)
+                    masked_fraction, smooth, share_smooth, seed, act_dtype, scale_dtype,
+                    smooth_per_expert)
 
 
 def touched_experts(ids: torch.Tensor, num_experts: int, mask: Optional[torch.Tensor] = None):

@@ -27,14 +27,24 @@ MUTANTS = [
      "for (int k = 0; k < topk - 1; ++k) {\n      if (!rows[k]) continue;"),
     ("unstable_dispatch", "int r = fill[e]++;", "int r = offsets[e + 1] - 1 - (fill[e]++ - offsets[e]);"),
     ("requant_scale", "*scale2 = amax * inv127;", "*scale2 = amax;"),
-    ("shared_uses_expert_smooth", "oracle_quant_row(h, a->x + (size_t)i * h, a->share_smooth,",
-     "oracle_quant_row(h, a->x + (size_t)i * h, a->smooth,"),
+    ("shared_uses_expert_smooth", "quant_row(h, xt, a->act_fp16, a->share_smooth,",
+     "quant_row(h, xt, a->act_fp16, a->smooth,"),
     ("dequant_drops_token_scale", "float g = ((float)acc1[j] * w1s[j]) * x_scale;",
      "float g = ((float)acc1[j] * w1s[j]);"),
     ("bf16_truncation", "u += 0x7FFFu + lsb;", "u += 0;"),
     ("folded_weight_dropped", "route_scale ? s2 * (*route_scale) : s2", "s2"),
-    ("folded_weight_twice", "      sum = sum + bf16_to_f32(rows[k][c]);",
-     "      sum = sum + bf16_to_f32(rows[k][c]) * 0.5f;"),
+    ("folded_weight_twice", "      sum = sum + act_to_f32(rows[k][c], fp16);",
+     "      sum = sum + act_to_f32(rows[k][c], fp16) * 0.5f;"),
+    # signature variants
+    ("f16_truncation", "uint32_t q = (uint32_t)rintf(ldexpf(a, 10 - e));",
+     "uint32_t q = (uint32_t)truncf(ldexpf(a, 10 - e));"),
+    ("f16_subnormal_scale", "f = ldexpf((float)m, -24);", "f = ldexpf((float)m, -25);"),
+    ("fp16_x_read_as_bf16", "float v = act_to_f32(x[c], fp16);", "float v = act_to_f32(x[c], 0);"),
+    ("fp16_y2_written_as_bf16", "y[j] = f32_to_act(((float)acc2[j] * w2s[j]) * scale2, fp16);",
+     "y[j] = f32_to_act(((float)acc2[j] * w2s[j]) * scale2, 0);"),
+    ("bf16_scale_decoded_as_f16", "else if (dtype == 1) dst[i] = bf16_to_f32(",
+     "else if (dtype == 1) dst[i] = f16_to_f32("),
+    ("expert_smooth_wrong_row", "a->smooth + (size_t)e * h, q,", "a->smooth, q,"),
 ]
 
 

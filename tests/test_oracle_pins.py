@@ -263,15 +263,17 @@ def dense_reference(inp):
 
     out = np.zeros((bs, h))
     share = np.zeros((bs, h))
+    sm = None if inp.smooth is None else inp.smooth.double().numpy()
     for t in range(bs):
         if not mask[t]:
             continue
-        xs = x[t] * (1.0 if inp.smooth is None else inp.smooth.double().numpy())
-        xq, xsc = quant(xs)
+        xq, xsc = quant(x[t] * (1.0 if sm is None or sm.ndim == 2 else sm))
         for k in range(K):
             e = int(ids[t, k])
             if not 0 <= e < E:
                 continue
+            if sm is not None and sm.ndim == 2:    # per-expert smooth: the row's own quant
+                xq, xsc = quant(x[t] * sm[e])
             out[t] += sc[t, k] * ffn(xq, xsc, W1[e], w1s[e], W2[e], w2s[e])
         if wl.has_shared:
             xs2 = x[t] * (1.0 if inp.share_smooth is None else inp.share_smooth.double().numpy())
@@ -447,3 +449,120 @@ def test_folded_differs_from_default_for_generic_weights():
     assert not torch.equal(a["output"].view(torch.int16), b["output"].view(torch.int16))
     diff = (a["output"].float() - b["output"].float()).abs().max().item()
     assert diff <= 2e-2 * a["output"].float().abs().max().item()
+
+
+# ------------------------------------------------------ signature variants
+# The pages' input table lists x as bf16 or fp16 and the routed weight scales
+# as fp32, bf16 or fp16; the smooth scales' shape is not given ([E, h] per
+# expert is the variant).  Pins: the fp16 conversions against numpy's IEEE
+# float16 casts (all 65536 codes one way, edge and random values the other);
+# fp16 mode equal to bf16 mode through every integer stage when x is exact in
+# both formats; 16-bit scales equal to their exact fp32 widening; [E, h]
+# smooth equal to the [h] mode when all rows agree, and with a distinct power
+# of two per expert each routed row's scale names the expert whose row it
+# used; and every variant within the float64 dense bound.
+
+def test_f16_to_f32_all_codes_match_numpy():
+    codes = np.arange(65536, dtype=np.uint16)
+    ref = codes.view(np.float16).astype(np.float32)
+    got = np.array([oracle.f16_value(int(c)) for c in codes], dtype=np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))   # signed zeros too
+
+
+def test_f32_to_f16_matches_numpy_rne():
+    rng = np.random.default_rng(5)
+    vals = [0.0, -0.0, 1.0, -1.0, 65504.0, 65519.99, 65520.0, 65536.0, 1e9, -1e9, 2.0 ** -24, 2.0 ** -25,
+            3 * 2.0 ** -26, 2.0 ** -25 * 1.0000001, 2.0 ** -14, 2.0 ** -14 * (1 - 2.0 ** -12), 1e-30,
+            float("inf"), -float("inf"), 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 2049.0, 2051.0, 4097.0]
+    # every f16 midpoint in a few binades (ties go to the even code)
+    base = np.arange(0x3C00, 0x3C40, dtype=np.uint16).view(np.float16).astype(np.float64)
+    vals += list((base[:-1] + base[1:]) / 2)
+    vals += list(np.ldexp(rng.uniform(-1, 1, 4000), rng.integers(-30, 18, 4000)))
+    v32 = np.array(vals, dtype=np.float32)
+    ref = v32.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f16_round(float(v)) for v in v32], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def _variant(wl, **kw):
+    return synth.Workload(**{**wl.__dict__, **kw})
+
+
+def test_fp16_x_equals_bf16_x_through_the_integer_stages():
+    wl = CASES[1]
+    inp = synth.make_inputs(wl)
+    # x values with 8 significant bits and a moderate exponent: exact in both formats
+    inp.x = (torch.round(inp.x.float() * 64) / 64).clamp(-3.9, 3.9).to(torch.bfloat16)
+    a = oracle.forward(inp, intermediates=True, threads=4)
+    inp.x = inp.x.float().to(torch.float16)
+    b = oracle.forward(inp, intermediates=True, threads=4)
+    for name in ("x_q", "x_scale", "acc1", "h", "x2", "s2", "acc2", "xs_q", "xs_scale", "share_acc2"):
+        assert torch.equal(a[name], b[name]), name
+    assert b["output"].dtype == torch.float16 and b["y2"].dtype == torch.float16
+    # y2 and the outputs: one rounding of the same fp32 values, to bf16 or to fp16
+    yb, yf = a["y2"].float(), b["y2"].float()
+    assert ((yb - yf).abs() <= yf.abs() * 2.0 ** -8 + 1e-30).all()
+    # the outputs sum topk such terms (cancellation allowed): bound by the row's largest value
+    ob, of = a["output"].float(), b["output"].float()
+    assert ((ob - of).abs() <= of.abs().amax(dim=1, keepdim=True) * 2.0 ** -7).all()
+
+
+@pytest.mark.parametrize("sdt", ["bf16", "fp16"])
+def test_16_bit_weight_scales_equal_their_fp32_widening(sdt):
+    inp = synth.make_inputs(_variant(CASES[1], scale_dtype=sdt))
+    assert inp.w1_scale.dtype == {"bf16": torch.bfloat16, "fp16": torch.float16}[sdt]
+    a = oracle.forward(inp, threads=4)
+    inp.w1_scale = inp.w1_scale.float()
+    inp.w2_scale = inp.w2_scale.float()
+    b = oracle.forward(inp, threads=4)
+    assert torch.equal(a["output"].view(torch.int16), b["output"].view(torch.int16))
+    assert torch.equal(a["share_output"].view(torch.int16), b["share_output"].view(torch.int16))
+
+
+def test_per_expert_smooth_with_equal_rows_equals_vector_mode():
+    wl = CASES[1]
+    inp = synth.make_inputs(wl)
+    a = oracle.forward(inp, threads=4)
+    inp.smooth = inp.smooth.view(1, -1).repeat(wl.num_experts, 1).contiguous()
+    b = oracle.forward(inp, intermediates=True, threads=4)
+    assert torch.equal(a["output"].view(torch.int16), b["output"].view(torch.int16))
+    assert torch.equal(a["share_output"].view(torch.int16), b["share_output"].view(torch.int16))
+    assert b["x_q"].shape[0] == b["R"]
+
+
+def test_per_expert_smooth_row_uses_its_own_expert():
+    wl = CASES[2]
+    inp = synth.make_inputs(wl)
+    E, h, K = wl.num_experts, wl.hidden, wl.topk
+    inp.smooth = None
+    plain = oracle.forward(inp, intermediates=True, threads=4)
+    j = torch.arange(E) % 5 - 2                      # expert e scales x by 2^j[e]
+    inp.smooth = torch.pow(2.0, j.float()).view(E, 1).repeat(1, h).contiguous()
+    res = oracle.forward(inp, intermediates=True, threads=4)
+    for r in range(res["R"]):
+        f = int(res["tk_of_row"][r])
+        t, e = f // K, int(inp.expert_ids.view(-1)[f])
+        assert torch.equal(res["x_q"][r], plain["x_q"][t])               # quant invariant to 2^j
+        assert res["x_scale"][r].item() == plain["x_scale"][t].item() * 2.0 ** int(j[e])
+    # same codes, so the GEMM1 accumulators equal the plain run's (the 2^j
+    # stays in the row's dequant scale: smoothing is not undone later)
+    assert torch.equal(res["acc1"], plain["acc1"])
+
+
+VARIANT_CASES = [
+    _variant(CASES[1], act_dtype="fp16", name="ragged_fp16"),
+    _variant(CASES[2], scale_dtype="bf16", smooth_per_expert=True, name="zipf_bf16scale_expert_smooth"),
+    _variant(CASES[1], act_dtype="fp16", scale_dtype="fp16", smooth_per_expert=True, name="ragged_all"),
+]
+
+
+@pytest.mark.parametrize("wl", VARIANT_CASES, ids=lambda w: w.name)
+def test_variants_match_float64_dense(wl):
+    inp = synth.make_inputs(wl)
+    res = oracle.forward(inp, threads=4)
+    ref_out, ref_share = dense_reference(inp)
+    rowwise_close(res["output"].float().numpy(), ref_out, 1e-2)
+    if wl.has_shared:
+        rowwise_close(res["share_output"].float().numpy(), ref_share, 1e-2)
