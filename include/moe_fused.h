@@ -50,8 +50,9 @@ extern "C" {
  * multiples of 64; 1 <= num_experts <= 1024; 1 <= topk <= min(num_experts, 16);
  * 0 <= bs_max <= 65536.  GEMM1 has N = 2*inter outputs (gate rows 0..inter-1,
  * up rows inter..2*inter-1); GEMM2 maps inter -> hidden.  `flags` is a
- * combination of MOE_FLAG_UNFUSED and MOE_FLAG_FOLD_ROUTING; other bits are
- * reserved (MOE_ERR_INVALID_ARG).  The pages' supported ranges (§9.4) are not
+ * combination of the MOE_FLAG_* bits below (MOE_FLAG_SCALE_BF16 and
+ * MOE_FLAG_SCALE_FP16 exclude each other); other bits are reserved
+ * (MOE_ERR_INVALID_ARG).  The pages' supported ranges (§9.4) are not
  * enforced. */
 
 /* Every expert takes the tensor-core path with separate requant and combine
@@ -70,6 +71,23 @@ extern "C" {
  * The shared expert is unchanged.  This rounds differently from the default
  * (routing weight applied in the combine after each row's bf16 rounding). */
 #define MOE_FLAG_FOLD_ROUTING 2
+
+/* Signature variants of the operator's input table (§1.2: x bf16 or fp16;
+ * routed weight scales fp32, bf16 or fp16; smooth scales optional, shape not
+ * given).
+ * MOE_FLAG_FP16_ACT: x is fp16, and y2, output and share_output are fp16
+ *   (round to nearest even, IEEE overflow to infinity) instead of bf16.
+ * MOE_FLAG_SCALE_BF16 / MOE_FLAG_SCALE_FP16: gmm1_weight_scale and
+ *   gmm2_weight_scale hold bf16 / fp16 values, widened exactly to fp32 before
+ *   the same arithmetic.  The shared expert's scales stay fp32.
+ * MOE_FLAG_EXPERT_SMOOTH: expert_smooth_scales is [num_experts, hidden]; the
+ *   routed row of pair (t, k) with expert e is quantised from
+ *   x[t] * expert_smooth_scales[e] (a per-row quant: the workspace holds one
+ *   int8 row per routed pair).  The shared expert keeps its [hidden] vector. */
+#define MOE_FLAG_FP16_ACT 4
+#define MOE_FLAG_SCALE_BF16 8
+#define MOE_FLAG_SCALE_FP16 16
+#define MOE_FLAG_EXPERT_SMOOTH 32
 typedef struct {
   int32_t bs_max;
   int32_t hidden;
@@ -81,25 +99,27 @@ typedef struct {
 } moe_fused_config_t;
 
 /* Per-call tensors, following the operator signature (§1.2):
- *   x                  [bs, hidden] bf16
+ *   x                  [bs, hidden] bf16 (fp16 with MOE_FLAG_FP16_ACT)
  *   expert_ids         [bs, topk] int32; a pair whose id is outside
  *                      [0, num_experts) is skipped (not counted, adds nothing)
  *   expert_scales      [bs, topk] fp32 routing weights
  *   gmm1_weight        [num_experts, 2*inter, hidden] int8, K (hidden) contiguous
- *   gmm1_weight_scale  [num_experts, 2*inter] fp32 per output channel
+ *   gmm1_weight_scale  [num_experts, 2*inter] fp32 per output channel (bf16 / fp16
+ *                      with MOE_FLAG_SCALE_BF16 / MOE_FLAG_SCALE_FP16)
  *   gmm2_weight        [num_experts, hidden, inter] int8, K (inter) contiguous
- *   gmm2_weight_scale  [num_experts, hidden] fp32
+ *   gmm2_weight_scale  [num_experts, hidden] fp32 (or as gmm1_weight_scale)
  *   share_gmm1_weight / _scale   [2*inter, hidden] / [2*inter]  (has_shared)
  *   share_gmm2_weight / _scale   [hidden, inter] / [hidden]     (has_shared)
  *   expert_smooth_scales  [hidden] fp32 or NULL: multiplies x per channel
- *                      before the routed experts' quant
+ *                      before the routed experts' quant ([num_experts, hidden]
+ *                      with MOE_FLAG_EXPERT_SMOOTH: expert e's own row)
  *   share_smooth_scales   [hidden] fp32 or NULL: same for the shared expert
  *   x_active_mask      [bs] bool (one byte, 0 = inactive) or NULL (all active);
  *                      inactive tokens are not dispatched and get zero rows in
  *                      output and share_output
  * Outputs:
- *   output             [bs, hidden] bf16
- *   share_output       [bs, hidden] bf16, required iff has_shared, else NULL
+ *   output             [bs, hidden] bf16 (x's dtype)
+ *   share_output       [bs, hidden] bf16 (x's dtype), required iff has_shared, else NULL
  *   expert_token_nums  [num_experts] int32: rows each expert received (counts,
  *                      not a prefix sum)
  * bs: 0 <= bs <= bs_max.  bs == 0 zeroes expert_token_nums and leaves the other
@@ -109,9 +129,9 @@ typedef struct {
   const int32_t* expert_ids;
   const float* expert_scales;
   const int8_t* gmm1_weight;
-  const float* gmm1_weight_scale;
+  const void* gmm1_weight_scale;   /* fp32, or bf16 / fp16 bits (flags) */
   const int8_t* gmm2_weight;
-  const float* gmm2_weight_scale;
+  const void* gmm2_weight_scale;
   const int8_t* share_gmm1_weight;
   const float* share_gmm1_weight_scale;
   const int8_t* share_gmm2_weight;

@@ -36,6 +36,13 @@ FLAG_UNFUSED = 1
 # config flag: routing weight folded into each row's GEMM2 dequant scale, the
 # combine a plain sum (rounds differently from the default)
 FLAG_FOLD_ROUTING = 2
+# config flags, signature variants: x / output / share_output fp16; routed
+# weight scales bf16 or fp16 (widened exactly); expert smooth scales [E, h]
+FLAG_FP16_ACT = 4
+FLAG_SCALE_BF16 = 8
+FLAG_SCALE_FP16 = 16
+FLAG_EXPERT_SMOOTH = 32
+_SCALE_FLAGS = {torch.float32: 0, torch.bfloat16: FLAG_SCALE_BF16, torch.float16: FLAG_SCALE_FP16}
 
 KERNEL_NAMES = ["dispatch_quant", "dispatch_finish", "expand", "gemm1_small", "gemm1_big", "requant_big",
                 "gemm2_small", "gemm2_big", "combine"]
@@ -216,14 +223,25 @@ class MoeFused:
     """
 
     def __init__(self, bs_max: int, hidden: int, num_experts: int, topk: int, inter: int,
-                 has_shared: bool, device=None, unfused: bool = False, fold_routing: bool = False):
+                 has_shared: bool, device=None, unfused: bool = False, fold_routing: bool = False,
+                 act_dtype=torch.bfloat16, scale_dtype=torch.float32, expert_smooth: bool = False):
+        """act_dtype: dtype of x and of the outputs (bf16 or fp16); scale_dtype:
+        dtype of the routed experts' weight scales (fp32, bf16 or fp16);
+        expert_smooth: expert_smooth_scales are [num_experts, hidden]."""
         self.device = torch.device(device if device is not None else "cuda")
         if self.device.type != "cuda":
             raise ValueError("the fused MoE block runs on a CUDA device only")
         if self.device.index is None:
             self.device = torch.device("cuda", torch.cuda.current_device())
-        self.cfg = Config(bs_max, hidden, num_experts, topk, inter, int(bool(has_shared)),
-                          (FLAG_UNFUSED if unfused else 0) | (FLAG_FOLD_ROUTING if fold_routing else 0))
+        if act_dtype not in (torch.bfloat16, torch.float16):
+            raise TypeError("act_dtype must be bfloat16 or float16")
+        if scale_dtype not in _SCALE_FLAGS:
+            raise TypeError("scale_dtype must be float32, bfloat16 or float16")
+        self.act_dtype, self.scale_dtype, self.expert_smooth = act_dtype, scale_dtype, bool(expert_smooth)
+        flags = ((FLAG_UNFUSED if unfused else 0) | (FLAG_FOLD_ROUTING if fold_routing else 0) |
+                 (FLAG_FP16_ACT if act_dtype == torch.float16 else 0) | _SCALE_FLAGS[scale_dtype] |
+                 (FLAG_EXPERT_SMOOTH if expert_smooth else 0))
+        self.cfg = Config(bs_max, hidden, num_experts, topk, inter, int(bool(has_shared)), flags)
         with torch.cuda.device(self.device):
             rc, self.handle, self.workspace_bytes = moe_fused_create(self.cfg)
         if rc:
@@ -253,32 +271,34 @@ class MoeFused:
         c, dev = self.cfg, self.device
         bs = x.shape[0]
         h, E, K, I = c.hidden, c.num_experts, c.topk, c.inter
+        act, sdt = self.act_dtype, self.scale_dtype
         if out is None:
-            out = torch.empty(bs, h, dtype=torch.bfloat16, device=dev)
+            out = torch.empty(bs, h, dtype=act, device=dev)
         if share_out is None and c.has_shared:
-            share_out = torch.empty(bs, h, dtype=torch.bfloat16, device=dev)
+            share_out = torch.empty(bs, h, dtype=act, device=dev)
         if token_nums is None:
             token_nums = torch.empty(E, dtype=torch.int32, device=dev)
         a = Args()
-        a.x = _check(x, "x", torch.bfloat16, (bs, h), dev)
+        a.x = _check(x, "x", act, (bs, h), dev)
         a.expert_ids = _check(expert_ids, "expert_ids", torch.int32, (bs, K), dev)
         a.expert_scales = _check(expert_scales, "expert_scales", torch.float32, (bs, K), dev)
         a.gmm1_weight = _check(w1, "gmm1_weight", torch.int8, (E, 2 * I, h), dev)
-        a.gmm1_weight_scale = _check(w1_scale, "gmm1_weight_scale", torch.float32, (E, 2 * I), dev)
+        a.gmm1_weight_scale = _check(w1_scale, "gmm1_weight_scale", sdt, (E, 2 * I), dev)
         a.gmm2_weight = _check(w2, "gmm2_weight", torch.int8, (E, h, I), dev)
-        a.gmm2_weight_scale = _check(w2_scale, "gmm2_weight_scale", torch.float32, (E, h), dev)
+        a.gmm2_weight_scale = _check(w2_scale, "gmm2_weight_scale", sdt, (E, h), dev)
         opt = not c.has_shared
         a.share_gmm1_weight = _check(share_w1, "share_gmm1_weight", torch.int8, (2 * I, h), dev, opt)
         a.share_gmm1_weight_scale = _check(share_w1_scale, "share_gmm1_weight_scale", torch.float32, (2 * I,), dev, opt)
         a.share_gmm2_weight = _check(share_w2, "share_gmm2_weight", torch.int8, (h, I), dev, opt)
         a.share_gmm2_weight_scale = _check(share_w2_scale, "share_gmm2_weight_scale", torch.float32, (h,), dev, opt)
-        a.expert_smooth_scales = _check(smooth, "expert_smooth_scales", torch.float32, (h,), dev, True)
+        a.expert_smooth_scales = _check(smooth, "expert_smooth_scales", torch.float32,
+                                        (E, h) if self.expert_smooth else (h,), dev, True)
         a.share_smooth_scales = _check(share_smooth, "share_smooth_scales", torch.float32, (h,), dev, True)
         if mask is not None and mask.dtype == torch.bool:
             mask = mask.view(torch.uint8)
         a.x_active_mask = _check(mask, "x_active_mask", torch.uint8, (bs,), dev, True)
-        a.output = _check(out, "output", torch.bfloat16, (bs, h), dev)
-        a.share_output = _check(share_out, "share_output", torch.bfloat16, (bs, h), dev, True)
+        a.output = _check(out, "output", act, (bs, h), dev)
+        a.share_output = _check(share_out, "share_output", act, (bs, h), dev, True)
         a.expert_token_nums = _check(token_nums, "expert_token_nums", torch.int32, (E,), dev)
         a.bs = bs
         keep = (x, expert_ids, expert_scales, w1, w1_scale, w2, w2_scale, share_w1, share_w1_scale, share_w2,

@@ -45,7 +45,10 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 int check_config(const moe_fused_config_t* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & ~(MOE_FLAG_UNFUSED | MOE_FLAG_FOLD_ROUTING)) != 0) return MOE_ERR_INVALID_ARG;
+  const int32_t known = MOE_FLAG_UNFUSED | MOE_FLAG_FOLD_ROUTING | MOE_FLAG_FP16_ACT | MOE_FLAG_SCALE_BF16 |
+                        MOE_FLAG_SCALE_FP16 | MOE_FLAG_EXPERT_SMOOTH;
+  if ((c->flags & ~known) != 0) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & MOE_FLAG_SCALE_BF16) && (c->flags & MOE_FLAG_SCALE_FP16)) return MOE_ERR_INVALID_ARG;
   if (c->hidden < 64 || c->hidden > 16384 || c->hidden % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->inter < 64 || c->inter > 16384 || c->inter % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->num_experts < 1 || c->num_experts > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -74,8 +77,10 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
   take(L.row_of, routed * 4, moe::kRegRowOf);
   take(L.tk_of_row, routed * 4, moe::kRegTkOfRow);
   take(L.active, bs * 4, moe::kRegActive);
-  take(L.x_q, bs * h, moe::kRegXq);
-  take(L.x_scale, bs * 4, moe::kRegXScale);
+  // per-expert smooth scales quantise every routed row on its own
+  const size_t xq_rows = (c.flags & MOE_FLAG_EXPERT_SMOOTH) ? routed : bs;
+  take(L.x_q, xq_rows * h, moe::kRegXq);
+  take(L.x_scale, xq_rows * 4, moe::kRegXScale);
   take(L.xs_q, c.has_shared ? bs * h : 0, moe::kRegXsq);
   take(L.xs_scale, c.has_shared ? bs * 4 : 0, moe::kRegXsScale);
   // h rows are 2I floats wide: the tensor-core GEMM1 stores the dequantised
@@ -138,7 +143,11 @@ int build_params(moe_fused_handle* hd, const moe_fused_args_t* a, void* ws, size
   p->topk = c.topk;
   p->I = c.inter;
   p->has_shared = c.has_shared;
-  p->share_uses_xq = c.has_shared && (a->expert_smooth_scales == a->share_smooth_scales);
+  // [E, h] smooth scales (when given) make the routed quant per row
+  p->xq_per_row = (c.flags & MOE_FLAG_EXPERT_SMOOTH) != 0 && a->expert_smooth_scales != nullptr;
+  p->share_uses_xq = c.has_shared && !p->xq_per_row && (a->expert_smooth_scales == a->share_smooth_scales);
+  p->act_fp16 = (c.flags & MOE_FLAG_FP16_ACT) != 0;
+  p->scale_dtype = (c.flags & MOE_FLAG_SCALE_BF16) ? 1 : (c.flags & MOE_FLAG_SCALE_FP16) ? 2 : 0;
   p->fold_routing = (c.flags & MOE_FLAG_FOLD_ROUTING) != 0;
   // the second launch of the multi-CTA dispatch pays off above a few chunks
   const int nf = a->bs * c.topk;

@@ -7,6 +7,7 @@
 // caller unwinds.  Nothing traps.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -289,6 +290,23 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   uint16_t r;
   asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
   return r;
+}
+
+// Activation elements (x, y2, the outputs) are bf16, or fp16 when `fp16`.
+__device__ __forceinline__ float act_bits_to_f32(uint16_t b, bool fp16) {
+  return fp16 ? __half2float(__ushort_as_half(b)) : bf16_bits_to_f32(b);
+}
+// fp32 -> activation bits, round half to even (fp16: IEEE, overflow to infinity)
+__device__ __forceinline__ uint16_t f32_to_act_bits(float f, bool fp16) {
+  return fp16 ? __half_as_ushort(__float2half_rn(f)) : f32_to_bf16_bits(f);
+}
+
+// Element i of a routed weight-scale array of dtype code dt (0 fp32, 1 bf16,
+// 2 fp16), widened exactly to fp32.
+__device__ __forceinline__ float wscale_at(const void* base, size_t i, int dt) {
+  if (dt == 0) return static_cast<const float*>(base)[i];
+  const uint16_t b = static_cast<const uint16_t*>(base)[i];
+  return dt == 1 ? bf16_bits_to_f32(b) : __half2float(__ushort_as_half(b));
 }
 
 }  // namespace moe

@@ -413,9 +413,9 @@ __device__ __forceinline__ float group_max(float v, float* s_red, int group) {
   return r;
 }
 
-// Quantise one bf16 row (h multiple of 64) with optional smooth scales, by
-// the 256 threads of one group.
-__device__ void quant_row(const uint16_t* __restrict__ x, const float* __restrict__ smooth, int h,
+// Quantise one bf16 (fp16 when `fp16`) row (h multiple of 64) with optional
+// smooth scales, by the 256 threads of one group.
+__device__ void quant_row(const uint16_t* __restrict__ x, bool fp16, const float* __restrict__ smooth, int h,
                           int8_t* __restrict__ q, float* __restrict__ scale_out, float* s_red, int group) {
   const int gt = threadIdx.x & (kQuantThreads - 1);
   const int n8 = h >> 3;
@@ -425,7 +425,7 @@ __device__ void quant_row(const uint16_t* __restrict__ x, const float* __restric
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      float f = bf16_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
+      float f = act_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu), fp16);
       if (smooth) f = __fmul_rn(f, smooth[i * 8 + j]);
       amax = fmaxf(amax, fabsf(f));
     }
@@ -439,7 +439,7 @@ __device__ void quant_row(const uint16_t* __restrict__ x, const float* __restric
     uint32_t packed[2] = {0u, 0u};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      float f = bf16_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
+      float f = act_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu), fp16);
       if (smooth) f = __fmul_rn(f, smooth[i * 8 + j]);
       const uint32_t b = static_cast<uint8_t>(f32_to_q(__fmul_rn(f, m)));
       packed[j >> 2] |= b << ((j & 3) * 8);
@@ -474,10 +474,13 @@ __device__ void quant_token(const FwdParams& p, int t, float* s_red, int group) 
     return;
   }
   const uint16_t* xr = p.x + static_cast<size_t>(t) * p.h;
-  quant_row(xr, p.smooth, p.h, ws_ptr<int8_t>(p, p.L.x_q) + static_cast<size_t>(t) * p.h,
-            ws_ptr<float>(p, p.L.x_scale) + t, s_red, group);
+  // per-expert smooth scales: the routed rows are quantised one by one after
+  // the dispatch (expand kernel); only the shared expert's quant runs here
+  if (!p.xq_per_row)
+    quant_row(xr, p.act_fp16, p.smooth, p.h, ws_ptr<int8_t>(p, p.L.x_q) + static_cast<size_t>(t) * p.h,
+              ws_ptr<float>(p, p.L.x_scale) + t, s_red, group);
   if (p.has_shared && !p.share_uses_xq) {
-    quant_row(xr, p.ssmooth, p.h, ws_ptr<int8_t>(p, p.L.xs_q) + static_cast<size_t>(t) * p.h,
+    quant_row(xr, p.act_fp16, p.ssmooth, p.h, ws_ptr<int8_t>(p, p.L.xs_q) + static_cast<size_t>(t) * p.h,
               ws_ptr<float>(p, p.L.xs_scale) + t, s_red, group);
   }
 }

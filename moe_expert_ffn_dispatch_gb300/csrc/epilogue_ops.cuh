@@ -107,7 +107,7 @@ __device__ void combine_token(const FwdParams& p, int t, int ctid) {
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float f = bf16_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu));
+          const float f = act_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu), p.act_fp16);
           // folded mode: the rows already carry their routing weight
           acc[j] = __fadd_rn(acc[j], p.fold_routing ? f : __fmul_rn(f, sc));
         }
@@ -116,8 +116,8 @@ __device__ void combine_token(const FwdParams& p, int t, int ctid) {
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      o[j] = static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * j])) |
-             (static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * j + 1])) << 16);
+      o[j] = static_cast<uint32_t>(f32_to_act_bits(acc[2 * j], p.act_fp16)) |
+             (static_cast<uint32_t>(f32_to_act_bits(acc[2 * j + 1], p.act_fp16)) << 16);
     out[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }

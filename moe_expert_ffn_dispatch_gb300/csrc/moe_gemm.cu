@@ -223,7 +223,8 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       if (lane < x.m) {
         const int r = x.row0 + lane;
         tok = row_token[r];
-        if (G1) sc = (x.e >= 0 ? xsc : xssc)[tok];
+        // routed x_scale is per token, or per row with per-expert smooth scales
+        if (G1) sc = x.e >= 0 ? xsc[p.xq_per_row ? r : tok] : xssc[tok];
         else if (p.fold_routing && x.e >= 0) sc = __fmul_rn(s2[r], p.scales[tk_of_row[r]]);  // folded row scale
         else sc = s2[r];
       }
@@ -255,8 +256,10 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
         if (lane == 0) mbar_arrive_expect_tx(tok_full, static_cast<uint32_t>(cur.m * K));
         __syncwarp();
         if (lane < cur.m) {
-          const int8_t* trow = G1 ? (cur.e >= 0 ? xq : xsq) + static_cast<size_t>(cur_tok) * p.h
-                                  : x2 + static_cast<size_t>(cur.row0 + lane) * p.I;
+          const int8_t* trow =
+              !G1 ? x2 + static_cast<size_t>(cur.row0 + lane) * p.I
+              : cur.e < 0 ? xsq + static_cast<size_t>(cur_tok) * p.h
+                          : xq + static_cast<size_t>(p.xq_per_row ? cur.row0 + lane : cur_tok) * p.h;
           bulk_g2s(smem + OFF_T + lane * K, trow, static_cast<uint32_t>(K), tok_full, pol_t);
         }
         run_slot = cur.slot;
@@ -345,9 +348,10 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       stop = *abort_flag != 0;
     } else if (G1) {
       // gate and up rows of a column sit in different warps: meet in shared memory
-      const float* wsc = cur.e >= 0 ? p.w1s + static_cast<size_t>(cur.e) * NW : p.sw1s;
+      const float ws = cur.e >= 0 ? wscale_at(p.w1s, static_cast<size_t>(cur.e) * NW + ng, p.scale_dtype)
+                                  : p.sw1s[ng];
       float y = 0.0f;
-      if (t < m) y = __fmul_rn(__fmul_rn(__int2float_rn(mine), wsc[ng]), info_scale[is * MT + t]);
+      if (t < m) y = __fmul_rn(__fmul_rn(__int2float_rn(mine), ws), info_scale[is * MT + t]);
       ytile[nl * MT + t] = y;
       consumer_sync();
       stop = *abort_flag != 0;
@@ -363,9 +367,10 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       // GEMM2: each lane owns one (row, token) result and stores it straight
       // away: no shared-memory staging, no CTA barrier per item
       if (t < m) {
-        const float* wsc = cur.e >= 0 ? p.w2s + static_cast<size_t>(cur.e) * NW : p.sw2s;
+        const float ws = cur.e >= 0 ? wscale_at(p.w2s, static_cast<size_t>(cur.e) * NW + ng, p.scale_dtype)
+                                    : p.sw2s[ng];
         const uint16_t b =
-            f32_to_bf16_bits(__fmul_rn(__fmul_rn(__int2float_rn(mine), wsc[ng]), info_scale[is * MT + t]));
+            f32_to_act_bits(__fmul_rn(__fmul_rn(__int2float_rn(mine), ws), info_scale[is * MT + t]), p.act_fp16);
         if (cur.e >= 0) y2[static_cast<size_t>(info_row[is * MT + t]) * p.h + ng] = b;
         else p.sout[static_cast<size_t>(info_tok[is * MT + t]) * p.h + ng] = b;
       }

@@ -94,13 +94,16 @@ struct FwdParams {
   int32_t with_tickets;   // dispatch resets the GEMM epilogue counters (forward path)
   int32_t small_rows;     // row count up to which an expert takes the dp4a path (0: never)
   int32_t num_ctas;       // grid of the GEMM launches (<= kMaxCtas)
+  int32_t act_fp16;       // x, y2 and the outputs are fp16 (else bf16)
+  int32_t scale_dtype;    // routed weight scales: 0 fp32, 1 bf16, 2 fp16
+  int32_t xq_per_row;     // per-expert smooth: routed x_q / x_scale are indexed by row, not token
   const uint16_t* x;
   const int32_t* ids;
   const float* scales;
   const int8_t* w1;
-  const float* w1s;
+  const void* w1s;        // dtype scale_dtype
   const int8_t* w2;
-  const float* w2s;
+  const void* w2s;        // dtype scale_dtype
   const int8_t* sw1;
   const float* sw1s;
   const int8_t* sw2;

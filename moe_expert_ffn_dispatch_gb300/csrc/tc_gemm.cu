@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         const int t = row_token[r];
         tok_row[ctid] = r;
         tok_tok[ctid] = t;
-        if (G1) tok_scale[ctid] = (x.e >= 0 ? xsc : xssc)[t];
+        if (G1) tok_scale[ctid] = x.e >= 0 ? xsc[p.xq_per_row ? r : t] : xssc[t];
         else if (p.fold_routing && x.e >= 0) tok_scale[ctid] = __fmul_rn(s2[r], p.scales[tk_of_row_g[r]]);
         else tok_scale[ctid] = s2[r];
       }
@@ -527,9 +527,9 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         // token, into the row's gate | up halves; the requant kernel applies
         // SwiGLU (a long expf / divide chain that would otherwise hold this
         // epilogue, and with it the accumulators, for most of an item)
-        const float* w1s = x.e >= 0 ? p.w1s + static_cast<size_t>(x.e) * NW : p.sw1s;
         const int ncol = gate ? col : p.I + col;
-        const float ws = w1s[ncol];
+        const float ws = x.e >= 0 ? wscale_at(p.w1s, static_cast<size_t>(x.e) * NW + ncol, p.scale_dtype)
+                                  : p.sw1s[ncol];
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
           const int tok = 64 * half + j;
@@ -538,13 +538,16 @@ __global__ void __launch_bounds__(kBigThreads, 1)
                 __fmul_rn(__fmul_rn(__int2float_rn(acc[j]), ws), tok_scale[tok]);
         }
       } else {
-        const float ws = (x.e >= 0 ? p.w2s + static_cast<size_t>(x.e) * NW : p.sw2s)[col];
         const bool valid_n = col < p.h;
+        const float ws = !valid_n ? 0.0f
+                         : x.e >= 0 ? wscale_at(p.w2s, static_cast<size_t>(x.e) * NW + col, p.scale_dtype)
+                                    : p.sw2s[col];
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
           const int tok = 64 * half + j;
           if (tok < mblk && valid_n) {
-            const uint16_t b = f32_to_bf16_bits(__fmul_rn(__fmul_rn(__int2float_rn(acc[j]), ws), tok_scale[tok]));
+            const uint16_t b =
+                f32_to_act_bits(__fmul_rn(__fmul_rn(__int2float_rn(acc[j]), ws), tok_scale[tok]), p.act_fp16);
             if (x.e >= 0) y2[static_cast<size_t>(tok_row[tok]) * p.h + col] = b;
             else p.sout[static_cast<size_t>(tok_tok[tok]) * p.h + col] = b;
           }
@@ -605,15 +608,81 @@ __device__ __forceinline__ int big_slot_of(const BigSlots& t, int b) {
   return lo;
 }
 
+// Per-row quant of routed row r with per-expert smooth scales (the operator
+// input table's smooth scales read as [E, h]): the same steps as the token
+// quant (xs = x[t] * smooth[e], amax floored at 1e-4, m = 127 / amax,
+// q = RNE(xs * m), scale = 1 / m), by one warp; rows of big blocks also get
+// their f16 copy for the tensor-core GEMM1.
+__device__ __forceinline__ void quant_routed_row(const FwdParams& p, int r, int lane, const int32_t* tk_of_row,
+                                                 const int32_t* counts, int8_t* xq, float* xsc, __half* x1h) {
+  const int f = tk_of_row[r];
+  const int t = f / p.topk, e = p.ids[f];
+  const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * p.h);
+  const float4* sm = reinterpret_cast<const float4*>(p.smooth + static_cast<size_t>(e) * p.h);
+  const int n8 = p.h >> 3;
+  const bool fp16 = p.act_fp16 != 0;
+  auto load8 = [&](int c, float (&v)[8]) {
+    const uint4 w4 = xr[c];
+    const float4 s0 = sm[2 * c], s1 = sm[2 * c + 1];
+    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+    const float s8[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      v[j] = __fmul_rn(act_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu), fp16), s8[j]);
+  };
+  float amax = 0.0f;
+  for (int c = lane; c < n8; c += 32) {
+    float v[8];
+    load8(c, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (amax < kAmaxEps) amax = kAmaxEps;
+  const float m = __fdiv_rn(127.0f, amax);
+  const bool big = counts[e] > p.small_rows;
+  uint2* qrow = reinterpret_cast<uint2*>(xq + static_cast<size_t>(r) * p.h);
+  uint4* hrow = reinterpret_cast<uint4*>(x1h + static_cast<size_t>(r) * p.h);
+  for (int c = lane; c < n8; c += 32) {
+    float v[8];
+    load8(c, v);
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      packed[j >> 2] |= static_cast<uint32_t>(static_cast<uint8_t>(f32_to_q(__fmul_rn(v[j], m)))) << ((j & 3) * 8);
+    qrow[c] = make_uint2(packed[0], packed[1]);
+    if (big) {
+      uint4 lo16, hi16;
+      int8x16_to_f16(make_uint4(packed[0], packed[1], 0u, 0u), lo16, hi16);
+      hrow[c] = lo16;
+    }
+  }
+  if (lane == 0) xsc[r] = __fdiv_rn(1.0f, m);
+}
+
 // f16 copies of the token codes of every row in a big block: the GEMM1
 // operand that the tensor-memory path reads with TMA.  One warp per row slot
 // (block, row) of the big blocks; slots past a block's last row are skipped.
+// With per-expert smooth scales the routed rows are quantised here first
+// (every routed row, one warp each, their f16 copies included), and the slot
+// loop then copies only the shared expert's rows.
 __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
   extern __shared__ int32_t ex_smem[];  // big_slots_smem_bytes(E)
   grid_dependency_wait();
   grid_launch_dependents();
   const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
+  if (p.xq_per_row) {
+    const int R = slots[SlotTable::kRows];
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    for (int r = gw; r < R; r += nw)
+      quant_routed_row(p, r, lane, ws_ptr<int32_t>(p, p.L.tk_of_row), ws_ptr<int32_t>(p, p.L.counts),
+                       ws_ptr<int8_t>(p, p.L.x_q), ws_ptr<float>(p, p.L.x_scale), ws_ptr<__half>(p, p.L.x1h));
+  }
   const int total = slots[SlotTable::kBigBlocks];
+
   if (total == 0) return;
   const BigSlots tab = stage_big_slots(p, slots, ex_smem);
   const int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
@@ -629,6 +698,7 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
     const int sl = big_slot_of(tab, b);
     const int tb = b - tab.pre[sl];
     if (tb * TB + i >= tab.rows[sl]) continue;
+    if (p.xq_per_row && tab.exp[sl] >= 0) continue;  // quantised and copied above
     const int r = tab.row0[sl] + tb * TB + i;
     // lane l converts codes 8 c .. 8 c + 7 for c = l, l + 32, ...: every warp
     // store covers 512 contiguous bytes of the f16 row

@@ -10,8 +10,10 @@ Tolerances (the block's accuracy contract):
     each within a few ulp);
   * requantised x2: at most 1 LSB apart on at most 0.1 % of the elements
     (an exp ulp can move a value across a rounding boundary), s2 within 2e-6;
-  * bf16 y2 / output / share_output: per row, max |gpu - oracle| <= 2e-2 *
-    max |oracle row|; masked rows exactly zero.
+  * bf16 (or fp16) y2 / output / share_output: per row, max |gpu - oracle| <=
+    2e-2 * max |oracle row|; masked rows exactly zero.
+The block is created in the workload's signature variant (x dtype, weight
+scale dtype, per-expert smooth scales), the oracle reads the same inputs.
 """
 from __future__ import annotations
 
@@ -47,9 +49,14 @@ def device_weights(inp, dev):
     return w
 
 
+_DT = {"bf16": torch.bfloat16, "fp16": torch.float16, "f32": torch.float32}
+
+
 def make_block(wl, dev, bs_max=None, unfused=False, fold_routing=False):
     return m.MoeFused(bs_max if bs_max is not None else wl.bs, wl.hidden, wl.num_experts, wl.topk, wl.inter,
-                      wl.has_shared, dev, unfused=unfused, fold_routing=fold_routing)
+                      wl.has_shared, dev, unfused=unfused, fold_routing=fold_routing,
+                      act_dtype=_DT[wl.act_dtype], scale_dtype=_DT[wl.scale_dtype],
+                      expert_smooth=wl.smooth_per_expert)
 
 
 def region(blk, name, dtype, shape=None):
@@ -135,11 +142,18 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
         assert torch.equal(region(blk, "tk_of_row", torch.int32, (R,)), ref["tk_of_row"])
         if wl.has_shared:
             assert torch.equal(region(blk, "active", torch.int32, (S,)), act.to(torch.int32))
-        # quant (bit-exact on active tokens)
-        xq = region(blk, "x_q", torch.int8, (bs, h))
-        xs = region(blk, "x_scale", torch.float32, (bs,))
-        assert torch.equal(xq[act], ref["x_q"][act]), "x_q differs"
-        assert torch.equal(xs[act], ref["x_scale"][act]), "x_scale differs"
+        # quant (bit-exact on active tokens; per routed row with [E, h] smooth scales)
+        per_row = inp.smooth is not None and inp.smooth.dim() == 2
+        if per_row:
+            xq = region(blk, "x_q", torch.int8, (R, h))
+            xs = region(blk, "x_scale", torch.float32, (R,))
+            assert torch.equal(xq, ref["x_q"]), "x_q (per row) differs"
+            assert torch.equal(xs, ref["x_scale"]), "x_scale (per row) differs"
+        else:
+            xq = region(blk, "x_q", torch.int8, (bs, h))
+            xs = region(blk, "x_scale", torch.float32, (bs,))
+            assert torch.equal(xq[act], ref["x_q"][act]), "x_q differs"
+            assert torch.equal(xs[act], ref["x_scale"][act]), "x_scale differs"
         if wl.has_shared and (inp.smooth is not None or inp.share_smooth is not None):
             assert torch.equal(region(blk, "xs_q", torch.int8, (bs, h))[act], ref["xs_q"][act])
             assert torch.equal(region(blk, "xs_scale", torch.float32, (bs,))[act], ref["xs_scale"][act])
@@ -167,7 +181,8 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
         if big_row.any():
             w1s = inp.w1_scale.to(torch.float32)
             acc = ref["acc1"][big_row].to(torch.float32)
-            want = (acc * w1s[e_of_row[big_row]]) * ref["x_scale"][t_of_row[big_row]].view(-1, 1)
+            xsc_row = ref["x_scale"][:R][big_row] if per_row else ref["x_scale"][t_of_row[big_row]]
+            want = (acc * w1s[e_of_row[big_row]]) * xsc_row.view(-1, 1)
             assert torch.equal(hb[:R][big_row], want), "gate | up routed (tensor-core rows)"
         if S:
             if small_ok and S <= SMALL_ROWS:
@@ -193,10 +208,11 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
         if S:
             assert_codes_close(x2[bs * K:bs * K + S], ref["share_x2"][act], "x2 shared")
             assert_rel(s2[bs * K:bs * K + S], ref["share_s2"][act], H_REL, "s2 shared")
-        # y2 (bf16) of routed rows
-        y2 = region(blk, "y2", torch.int16, (max(R, 1), h))[:R].view(torch.bfloat16)
+        # y2 (x's dtype) of routed rows
+        y2 = region(blk, "y2", torch.int16, (max(R, 1), h))[:R].view(inp.x.dtype)
         assert_rows_close(y2, ref["y2"], OUT_REL, "y2")
     if bs > 0:
+        assert out.dtype == inp.x.dtype and (sout is None or sout.dtype == inp.x.dtype)
         assert_rows_close(out, ref["output"], OUT_REL, "output")
         if wl.has_shared:
             assert_rows_close(sout, ref["share_output"], OUT_REL, "share_output")

@@ -64,12 +64,19 @@ def test_workspace_size_and_config_checks(built):
     assert nb % 256 == 0
     for cfg, code in [(m.Config(8, 100, 4, 2, 64, 0, 0), m.MOE_ERR_UNSUPPORTED_SHAPE),
                       (m.Config(8, 128, 4, 5, 64, 0, 0), m.MOE_ERR_UNSUPPORTED_SHAPE),
-                      (m.Config(8, 128, 4, 2, 64, 0, 4), m.MOE_ERR_INVALID_ARG),  # reserved flag bit
+                      (m.Config(8, 128, 4, 2, 64, 0, 64), m.MOE_ERR_INVALID_ARG),  # reserved flag bit
+                      (m.Config(8, 128, 4, 2, 64, 0, m.FLAG_SCALE_BF16 | m.FLAG_SCALE_FP16),
+                       m.MOE_ERR_INVALID_ARG),  # two scale dtypes
                       (m.Config(8, 128, 2000, 2, 64, 0, 0), m.MOE_ERR_UNSUPPORTED_SHAPE),
                       (m.Config(8, 128, 4, 2, 64, 2, 0), m.MOE_ERR_INVALID_ARG)]:
         assert m.moe_fused_workspace_size(cfg)[0] == code
-    for flags in (m.FLAG_UNFUSED, m.FLAG_FOLD_ROUTING, m.FLAG_UNFUSED | m.FLAG_FOLD_ROUTING):
+    for flags in (m.FLAG_UNFUSED, m.FLAG_FOLD_ROUTING, m.FLAG_UNFUSED | m.FLAG_FOLD_ROUTING, m.FLAG_FP16_ACT,
+                  m.FLAG_SCALE_BF16, m.FLAG_SCALE_FP16 | m.FLAG_EXPERT_SMOOTH, 63 & ~m.FLAG_SCALE_FP16):
         assert m.moe_fused_workspace_size(m.Config(8, 128, 4, 2, 64, 0, flags))[0] == m.MOE_OK
+    # per-expert smooth scales quantise every routed pair on its own: x_q grows to bs * topk rows
+    base = m.moe_fused_workspace_size(m.Config(64, 4096, 256, 8, 2048, 1, 0))[1]
+    per_row = m.moe_fused_workspace_size(m.Config(64, 4096, 256, 8, 2048, 1, m.FLAG_EXPERT_SMOOTH))[1]
+    assert per_row - base >= 64 * 7 * 4096
 
 
 def test_strerror_and_names(built):

@@ -56,7 +56,8 @@ def test_error_codes_leave_outputs_untouched():
 
 def test_create_rejects_bad_config():
     bad = [m.Config(8, 100, 4, 2, 64, 0, 0), m.Config(8, 128, 4, 5, 64, 0, 0), m.Config(8, 128, 0, 1, 64, 0, 0),
-           m.Config(8, 128, 4, 2, 64, 0, 4), m.Config(-1, 128, 4, 2, 64, 0, 0)]  # flags bit 2 is reserved
+           m.Config(8, 128, 4, 2, 64, 0, 64), m.Config(-1, 128, 4, 2, 64, 0, 0),
+           m.Config(8, 128, 4, 2, 64, 0, m.FLAG_SCALE_BF16 | m.FLAG_SCALE_FP16)]  # bit 6 reserved; one scale dtype
     for cfg in bad:
         rc, h, _ = m.moe_fused_create(cfg)
         assert rc < 0 and h == 0

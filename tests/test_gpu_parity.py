@@ -139,3 +139,34 @@ def test_multi_cta_dispatch_with_masks_and_skipped_ids():
     inp.expert_ids[1400, :] = -3
     blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True)
     check_raw_accumulators(blk, inp, ref, di, dw, DEV)
+
+
+# Signature variants (the operator's input table: x bf16 or fp16; routed
+# weight scales fp32, bf16 or fp16; smooth scales, here per expert [E, h]):
+# both GEMM paths, masks, the shared expert and a multi-block expert.
+VARIANT_CASES = [
+    synth.custom("fp16_bf16scale_multiblock", bs=100, hidden=320, num_experts=3, topk=2, inter=64,
+                 has_shared=True, act_dtype="fp16", scale_dtype="bf16", seed=51),
+    synth.custom("expert_smooth_fp16scale", bs=37, hidden=192, num_experts=5, topk=3, inter=128,
+                 has_shared=True, masked_fraction=0.2, smooth=True, share_smooth=True, scale_dtype="fp16",
+                 smooth_per_expert=True, seed=52),
+    synth.custom("all_variants_zipf", bs=64, hidden=512, num_experts=32, topk=4, inter=256, has_shared=True,
+                 routing="zipf", masked_fraction=0.25, smooth=True, act_dtype="fp16", scale_dtype="bf16",
+                 smooth_per_expert=True, seed=53),
+    synth.custom("expert_smooth_big_blocks", bs=300, hidden=256, num_experts=4, topk=2, inter=128,
+                 has_shared=True, smooth=True, smooth_per_expert=True, seed=54),
+]
+
+
+@pytest.mark.parametrize("wl", VARIANT_CASES, ids=lambda w: w.name)
+def test_signature_variants_staged_parity(wl):
+    inp = synth.make_inputs(wl)
+    blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True)
+    check_raw_accumulators(blk, inp, ref, di, dw, DEV)
+
+
+def test_signature_variants_unfused_and_folded():
+    wl = VARIANT_CASES[2]
+    inp = synth.make_inputs(wl)
+    run_and_check(inp, DEV, staged=True, blk=make_block(wl, DEV, unfused=True))
+    run_and_check(inp, DEV, staged=True, blk=make_block(wl, DEV, fold_routing=True))
