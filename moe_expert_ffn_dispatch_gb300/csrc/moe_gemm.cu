@@ -65,22 +65,50 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
   return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
 }
 
-// Butterfly reduce-scatter over the warp: on entry every lane holds 32 partial
-// sums v[0..31]; on exit lane L holds the full sum of index L (31 shuffles,
-// exact int32 adds).
-__device__ __forceinline__ int warp_reduce_scatter32(int (&v)[32], int lane) {
+// Butterfly reduce-scatter over the warp of the 4 * MP partial sums a lane
+// holds: its warp's 4 weight rows x the first MP token slots (MP a power of
+// two >= the item's token rows; the slots past them hold zeros).  The
+// log2(4 MP) highest lane bits scatter the values and the remaining bits sum
+// them, so lane L ends with the full sum of index L >> (5 - log2(4 MP)) =
+// rr * MP + t: 4 MP - 1 + 5 - log2(4 MP) shuffles (6 for one token row, 31
+// for eight), exact int32 adds.
+template <int MP>
+__device__ __forceinline__ int warp_reduce_scatter(const int (&acc)[kRowsPerWarp * MT], int lane) {
+  constexpr int N = kRowsPerWarp * MP;
+  constexpr int LG = N == 4 ? 2 : N == 8 ? 3 : N == 16 ? 4 : 5;
+  int v[N];
 #pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool upper = (lane & half) != 0;
+  for (int rr = 0; rr < kRowsPerWarp; ++rr)
 #pragma unroll
-    for (int k = 0; k < half; ++k) {
-      const int send = upper ? v[k] : v[k + half];
-      const int keep = upper ? v[k + half] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+    for (int t = 0; t < MP; ++t) v[rr * MP + t] = acc[rr * MT + t];
+#pragma unroll
+  for (int lv = 0; lv < LG; ++lv) {
+    const int hv = N >> (lv + 1), bit = 16 >> lv;
+    const bool upper = (lane & bit) != 0;
+#pragma unroll
+    for (int k = 0; k < hv; ++k) {
+      const int send = upper ? v[k] : v[k + hv];
+      const int keep = upper ? v[k + hv] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
     }
   }
+#pragma unroll
+  for (int bit = 16 >> LG; bit >= 1; bit >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], bit);
   return v[0];
 }
+
+// log2 of the token slots an item of m rows reduces over (1, 2, 4 or 8 slots)
+__device__ __forceinline__ int slot_log2(int m) { return m <= 1 ? 0 : m <= 2 ? 1 : m <= 4 ? 2 : 3; }
+
+__device__ __forceinline__ int reduce_item(int lgmp, const int (&acc)[kRowsPerWarp * MT], int lane) {
+  switch (lgmp) {
+    case 0: return warp_reduce_scatter<1>(acc, lane);
+    case 1: return warp_reduce_scatter<2>(acc, lane);
+    case 2: return warp_reduce_scatter<4>(acc, lane);
+    default: return warp_reduce_scatter<MT>(acc, lane);
+  }
+}
+static_assert(MT == 8, "reduce_item covers 1, 2, 4 and 8 token slots");
 
 // One stage of dot products for a warp: kRowsPerWarp weight rows (at Ws,
 // stride KC) against M token rows (at Ts, stride KC), lane-strided 16-byte
@@ -288,7 +316,8 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       // next item's token info: its dependent loads run while this item's copies fly
       if (it + 1 < it_end) {
         nx = item_at(it + 1);
-        load_info(nx, nx_tok, nx_scale);
+        // the items of one run share the expert's token rows, and so their info
+        if (nx.slot != cur.slot) load_info(nx, nx_tok, nx_scale);
       }
     }
     return;
@@ -304,6 +333,22 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
     const SmallItem cur = item_at(it);
     const int m = cur.m, jt = cur.jt;
     const int is = item_no % kInfoSlots;
+    // after the reduce, lane L holds (row rr of this warp, token t) with
+    // rr * mp + t = L >> sh; one owner lane per pair writes it
+    const int lgmp = slot_log2(m), sh = 3 - lgmp;
+    const int idx = lane >> sh;
+    const int rr = idx >> lgmp, t = idx & ((1 << lgmp) - 1);
+    const bool owner = (lane & ((1 << sh) - 1)) == 0 && t < m;
+    const int nl = kRowsPerWarp * warp + rr;  // row inside the item
+    int ng;
+    if (G1) ng = (nl < BN / 2) ? jt * (BN / 2) + nl : p.I + jt * (BN / 2) + (nl - BN / 2);
+    else ng = jt * BN + nl;
+    // this lane's weight scale, loaded now and used after the dot products
+    float ws = 0.0f;
+    if (!RAW) {
+      if (cur.e >= 0) ws = wscale_at(G1 ? p.w1s : p.w2s, static_cast<size_t>(cur.e) * NW + ng, p.scale_dtype);
+      else ws = (G1 ? p.sw1s : p.sw2s)[ng];
+    }
     const bool run_end = (it + 1 == it_end) || ((it + 1) / J != cur.slot);
     if (cur.slot != run_slot) {
       tok_ok = mbar_wait_bounded(tok_full, run_no & 1, abort_flag, status, site + 4);
@@ -332,27 +377,17 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
     }
     if (run_end && lane == 0) mbar_arrive(tok_empty);  // this run's token rows are no longer read
 
-    // lane (rr * MT + t) receives the dot product of row rr of this warp with token t
-    const int mine = warp_reduce_scatter32(acc, lane);
-    const int rr = lane / MT, t = lane % MT;
-    const int nl = kRowsPerWarp * warp + rr;  // row inside the item
-    int ng;
-    if (G1) ng = (nl < BN / 2) ? jt * (BN / 2) + nl : p.I + jt * (BN / 2) + (nl - BN / 2);
-    else ng = jt * BN + nl;
+    const int mine = reduce_item(lgmp, acc, lane);
     // the abort flag is read only right after a CTA-wide barrier, so that
     // every consumer thread leaves the loop at the same item
     bool stop = false;
     if (RAW) {
-      if (t < m) raw[static_cast<size_t>(info_row[is * MT + t]) * NW + ng] = mine;
+      if (owner) raw[static_cast<size_t>(info_row[is * MT + t]) * NW + ng] = mine;
       consumer_sync();
       stop = *abort_flag != 0;
     } else if (G1) {
       // gate and up rows of a column sit in different warps: meet in shared memory
-      const float ws = cur.e >= 0 ? wscale_at(p.w1s, static_cast<size_t>(cur.e) * NW + ng, p.scale_dtype)
-                                  : p.sw1s[ng];
-      float y = 0.0f;
-      if (t < m) y = __fmul_rn(__fmul_rn(__int2float_rn(mine), ws), info_scale[is * MT + t]);
-      ytile[nl * MT + t] = y;
+      if (owner) ytile[nl * MT + t] = __fmul_rn(__fmul_rn(__int2float_rn(mine), ws), info_scale[is * MT + t]);
       consumer_sync();
       stop = *abort_flag != 0;
       if (ctid < (BN / 2) * m) {
@@ -366,9 +401,7 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
     } else {
       // GEMM2: each lane owns one (row, token) result and stores it straight
       // away: no shared-memory staging, no CTA barrier per item
-      if (t < m) {
-        const float ws = cur.e >= 0 ? wscale_at(p.w2s, static_cast<size_t>(cur.e) * NW + ng, p.scale_dtype)
-                                    : p.sw2s[ng];
+      if (owner) {
         const uint16_t b =
             f32_to_act_bits(__fmul_rn(__fmul_rn(__int2float_rn(mine), ws), info_scale[is * MT + t]), p.act_fp16);
         if (cur.e >= 0) y2[static_cast<size_t>(info_row[is * MT + t]) * p.h + ng] = b;
