@@ -216,10 +216,13 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
   }
   __syncthreads();
   const bool cached = n_cached <= kSlotCache;
-  auto item_at = [&](long it) {
+  // items are walked as (slot, tile) pairs advanced one by one: no 64-bit
+  // division by J per item
+  const int jt_first = static_cast<int>(it_begin - static_cast<long>(slot_first) * J);
+  auto item_of = [&](int slot, int jt) {
     SmallItem x;
-    x.slot = static_cast<int>(it / J);
-    x.jt = static_cast<int>(it % J);
+    x.slot = slot;
+    x.jt = jt;
     if (cached) {
       const int c = x.slot - slot_first;
       x.e = slot_cache[3 * c];
@@ -260,8 +263,9 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
     int nx_tok = 0;
     float nx_scale = 0.0f;
     SmallItem nx{};
+    int ps = slot_first, pj = jt_first;  // position of nx
     if (it_begin < it_end) {
-      nx = item_at(it_begin);
+      nx = item_of(ps, pj);
       load_info(nx, nx_tok, nx_scale);
     }
     int stage_it = 0, item_no = 0, run_slot = -1, run_no = 0;
@@ -315,7 +319,11 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       }
       // next item's token info: its dependent loads run while this item's copies fly
       if (it + 1 < it_end) {
-        nx = item_at(it + 1);
+        if (++pj == J) {
+          pj = 0;
+          ++ps;
+        }
+        nx = item_of(ps, pj);
         // the items of one run share the expert's token rows, and so their info
         if (nx.slot != cur.slot) load_info(nx, nx_tok, nx_scale);
       }
@@ -329,8 +337,14 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
   uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
   int stage_it = 0, item_no = 0, run_items = 0, run_slot = -1, run_no = 0;
   bool tok_ok = true;
+  int cs = slot_first, cj = jt_first;  // position of the current item
   for (long it = it_begin; it < it_end; ++it, ++item_no) {
-    const SmallItem cur = item_at(it);
+    const SmallItem cur = item_of(cs, cj);
+    const bool run_end = (it + 1 == it_end) || (cj + 1 == J);
+    if (++cj == J) {
+      cj = 0;
+      ++cs;
+    }
     const int m = cur.m, jt = cur.jt;
     const int is = item_no % kInfoSlots;
     // after the reduce, lane L holds (row rr of this warp, token t) with
@@ -349,7 +363,6 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
       if (cur.e >= 0) ws = wscale_at(G1 ? p.w1s : p.w2s, static_cast<size_t>(cur.e) * NW + ng, p.scale_dtype);
       else ws = (G1 ? p.sw1s : p.sw2s)[ng];
     }
-    const bool run_end = (it + 1 == it_end) || ((it + 1) / J != cur.slot);
     if (cur.slot != run_slot) {
       tok_ok = mbar_wait_bounded(tok_full, run_no & 1, abort_flag, status, site + 4);
       run_slot = cur.slot;
