@@ -628,22 +628,25 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   }
 }
 
-// The big slots' tables (block prefix, first row, row count, expert) staged
-// in shared memory once per CTA, so that kernels working row by row find the
-// slot of a (block, row) pair in a few shared-memory probes instead of a
-// chain of dependent global loads.  Layout: 4 arrays of stride E + 2 ints
-// (at most E + 1 slots), i.e. big_slots_smem_bytes(E).
-__host__ __device__ constexpr size_t big_slots_smem_bytes(int E) { return 4u * (E + 2) * sizeof(int32_t); }
+// The big slots' tables (block prefix, first row, row count, expert, and a
+// prefix of their row counts) staged in shared memory once per CTA, so that
+// kernels working row by row find the slot of a row in a few shared-memory
+// probes instead of a chain of dependent global loads.  Layout: 5 arrays of
+// stride E + 2 ints (at most E + 1 slots), i.e. big_slots_smem_bytes(E).
+__host__ __device__ constexpr size_t big_slots_smem_bytes(int E) { return 5u * (E + 2) * sizeof(int32_t); }
 
 struct BigSlots {
-  const int32_t* pre;
+  const int32_t* pre;   // first block of each slot (n + 1 entries)
   const int32_t* row0;
   const int32_t* rows;
   const int32_t* exp;
+  const int32_t* rpre;  // rows of the slots before each slot (n + 1 entries: rpre[n] = all big rows)
   int n;
 };
 
+// Called by every thread of the block (blockDim a multiple of 32, <= 1024).
 __device__ __forceinline__ BigSlots stage_big_slots(const FwdParams& p, const int32_t* slots, int32_t* t) {
+  __shared__ int s_wsum[32];
   const int st = SlotTable::stride(p.E);
   const int32_t* s_exp = slots + SlotTable::kHeader;
   const int32_t* s_row0 = s_exp + st;
@@ -659,15 +662,49 @@ __device__ __forceinline__ BigSlots stage_big_slots(const FwdParams& p, const in
     }
   }
   __syncthreads();
-  return BigSlots{t, t + st, t + 2 * st, t + 3 * st, n};
+  // row prefix: each thread sums a contiguous chunk of slots, the chunk sums
+  // are scanned across the block, then each thread writes its chunk's prefixes
+  int32_t* rpre = t + 4 * st;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nwarp = blockDim.x >> 5;
+  const int chunk = (n + blockDim.x - 1) / blockDim.x;
+  const int c0 = min(n, tid * chunk), c1 = min(n, c0 + chunk);
+  int sum = 0;
+  for (int i = c0; i < c1; ++i) sum += t[2 * st + i];
+  int x = sum;  // inclusive scan over the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_wsum[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = lane < nwarp ? s_wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nwarp) s_wsum[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = x - sum + (wid > 0 ? s_wsum[wid - 1] : 0);
+  for (int i = c0; i < c1; ++i) {
+    rpre[i] = run;
+    run += t[2 * st + i];
+  }
+  if (tid == 0) rpre[n] = s_wsum[nwarp - 1];
+  __syncthreads();
+  return BigSlots{t, t + st, t + 2 * st, t + 3 * st, rpre, n};
 }
 
-// slot of big block b: the last slot whose first block is <= b
-__device__ __forceinline__ int big_slot_of(const BigSlots& t, int b) {
+// slot of big row g (0 <= g < rpre[n], counting only real rows of big slots):
+// the last slot whose first row index is <= g
+__device__ __forceinline__ int big_row_slot(const BigSlots& t, int g) {
   int lo = 0, hi = t.n - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (t.pre[mid] <= b) lo = mid;
+    if (t.rpre[mid] <= g) lo = mid;
     else hi = mid - 1;
   }
   return lo;
@@ -727,8 +764,8 @@ __device__ __forceinline__ void quant_routed_row(const FwdParams& p, int r, int 
 }
 
 // f16 copies of the token codes of every row in a big block: the GEMM1
-// operand that the tensor-memory path reads with TMA.  One warp per row slot
-// (block, row) of the big blocks; slots past a block's last row are skipped.
+// operand that the tensor-memory path reads with TMA.  One warp per row of
+// the big slots at a time, the rows spread evenly over the grid.
 // With per-expert smooth scales the routed rows are quantised here first
 // (every routed row, one warp each, their f16 copies included), and the slot
 // loop then copies only the shared expert's rows.
@@ -757,14 +794,12 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int nw = gridDim.x * (blockDim.x >> 5);
-  const long nrows = static_cast<long>(total) * TB;
-  for (long g = gw; g < nrows; g += nw) {
-    const int b = static_cast<int>(g / TB), i = static_cast<int>(g % TB);
-    const int sl = big_slot_of(tab, b);
-    const int tb = b - tab.pre[sl];
-    if (tb * TB + i >= tab.rows[sl]) continue;
+  // real rows of the big slots, spread evenly over the warps
+  const int nreal = tab.rpre[tab.n];
+  for (int g = gw; g < nreal; g += nw) {
+    const int sl = big_row_slot(tab, g);
     if (p.xq_per_row && tab.exp[sl] >= 0) continue;  // quantised and copied above
-    const int r = tab.row0[sl] + tb * TB + i;
+    const int r = tab.row0[sl] + (g - tab.rpre[sl]);
     // lane l converts codes 8 c .. 8 c + 7 for c = l, l + 32, ...: every warp
     // store covers 512 contiguous bytes of the f16 row
     const uint2* src = reinterpret_cast<const uint2*>((tab.exp[sl] >= 0 ? xq : xsq) +
@@ -838,13 +873,12 @@ __global__ void __launch_bounds__(kRqWarps * 32) requant_big_kernel(FwdParams p)
   float4* hrow = rq_smem + wid * (kRqMaxI / 4);
   const int gw = blockIdx.x * kRqWarps + wid;
   const int nw = gridDim.x * kRqWarps;
-  const long nrows = static_cast<long>(total) * TB;  // block-major row slots (some empty)
-  for (long g = gw; g < nrows; g += nw) {
-    const int b = static_cast<int>(g / TB), i = static_cast<int>(g % TB);
-    const int sl = big_slot_of(tab, b);
-    const int tb = b - tab.pre[sl];
-    if (tb * TB + i >= tab.rows[sl]) continue;
-    const int r = tab.row0[sl] + tb * TB + i;
+  // real rows of the big slots, spread evenly over the warps (row slots of
+  // the 128-row blocks would leave most warps idle when blocks are short)
+  const int nreal = tab.rpre[tab.n];
+  for (int g = gw; g < nreal; g += nw) {
+    const int sl = big_row_slot(tab, g);
+    const int r = tab.row0[sl] + (g - tab.rpre[sl]);
     const float4* gr = reinterpret_cast<const float4*>(hbuf + static_cast<size_t>(r) * (2 * I));
     const float4* ur = gr + n4;
     __half2* h2 = reinterpret_cast<__half2*>(x2h + static_cast<size_t>(r) * I);
