@@ -247,15 +247,17 @@ __device__ void dispatch_tail(const FwdParams& p, int32_t* dsm, int c, int off, 
   if (p.with_tickets) {
     // Split of the small-phase items over the GEMM CTAs, by cost: an item of
     // an expert with m rows streams the same weight bytes as any other but
-    // does m dot products per weight, so it counts 8 + m.  CTA b takes the
-    // items whose cumulative cost starts in [total*b/G, total*(b+1)/G).
+    // does m dot products per weight, so it counts 12 + m (the base measured
+    // best among 4 .. 128 on the decode workloads; a near-uniform split, base
+    // 128, made GEMM1 20 % slower).  CTA b takes the items whose cumulative
+    // cost starts in [total*b/G, total*(b+1)/G).
     __syncthreads();
     const int ns = slots[SlotTable::kNumSmall];  // written by thread 0 above
-    int32_t* wp = dsm;       // exclusive prefix of (8 + m) over the small slots; [ns + 1]
+    int32_t* wp = dsm;       // exclusive prefix of (12 + m) over the small slots; [ns + 1]
     int carry = 0;
     for (int base = 0; base <= ns; base += kDispatchThreads) {
       const int i = base + tid;
-      const int cost = (i < ns) ? 8 + s_rows[i] : 0;
+      const int cost = (i < ns) ? 12 + s_rows[i] : 0;
       int tot = 0;
       const int ex = block_exclusive_scan(cost, &tot, s_warp);
       if (i <= ns) wp[i] = carry + ex;
