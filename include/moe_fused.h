@@ -244,7 +244,7 @@ const char* moe_fused_kernel_name(int kernel_id);
  *   10 h [rows,2*inter] f32 (SwiGLU output in the first inter floats of a row
  *      of the weight-streaming path; dequantised gate | up of the tensor-core
  *      path)  11 x2 [rows,inter] int8  12 s2 [rows] f32
- *   13 y2 [bs_max*topk,h] bf16 (aliases region 10)  14 slot table
+ *   13 y2 [bs_max*topk,h] in x's dtype  14 slot table
  *   15 row_token [rows] int32  16 shared_row [bs_max] int32
  *   17 row-block counters  18 token counters [bs_max]  19 token totals [bs_max]
  *   20 small-expert item ranges  21 x1h [rows,h] f16  22 x2h [rows,inter] f16

@@ -86,12 +86,13 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
   // h rows are 2I floats wide: the tensor-core GEMM1 stores the dequantised
   // gate and up halves there for the requant kernel, the dp4a GEMM1 stores h
   // in the first I
+  // y2 has its own region: the small experts' GEMM2 runs in the same launch
+  // as their GEMM1, while other CTAs may still write and read h
   const size_t hbytes = rows * 2 * I * 4, ybytes = routed * h * 2;
-  take(L.hbuf, hbytes > ybytes ? hbytes : ybytes, moe::kRegH);
+  take(L.hbuf, hbytes, moe::kRegH);
   take(L.x2, rows * I, moe::kRegX2);
   take(L.s2, rows * 4, moe::kRegS2);
-  L.y2 = L.hbuf;
-  L.sizes[moe::kRegY2] = ybytes;
+  take(L.y2, ybytes, moe::kRegY2);
   take(L.slots, static_cast<size_t>(moe::SlotTable::words(c.num_experts)) * 4, moe::kRegSlots);
   take(L.row_token, rows * 4, moe::kRegRowToken);
   take(L.shared_row, bs * 4, moe::kRegSharedRow);
@@ -335,12 +336,17 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
   if (rc) return rc;
   const int sms = p.num_ctas;
   const moe::TcMaps& maps = hd->maps;
+  // the small experts' GEMM2 streams behind their GEMM1 in one launch when
+  // the forward runs that far (a forward stopped after GEMM1 keeps h intact)
+  const bool streamed = p.small_rows > 0 && last_kernel >= moe::kKGemm2Small;
   auto run = [&](int k) -> cudaError_t {
     switch (k) {
       case moe::kKDispatchQuant: return moe::launch_dispatch_quant(p, s);
       case moe::kKDispatchFinish: return moe::launch_dispatch_finish(p, s);
       case moe::kKExpand: return moe::launch_expand(p, s);
-      case moe::kKGemm1Small: return moe::launch_moe_gemm_small(p, moe::kGemm1SwiGLU, nullptr, sms, s);
+      case moe::kKGemm1Small:
+        return streamed ? moe::launch_moe_gemm_small_streamed(p, sms, s)
+                        : moe::launch_moe_gemm_small(p, moe::kGemm1SwiGLU, nullptr, sms, s);
       case moe::kKGemm1Big: return moe::launch_moe_gemm_big(p, maps, moe::kGemm1SwiGLU, nullptr, sms, s);
       case moe::kKRequantBig: return moe::launch_requant_big(p, s);
       case moe::kKGemm2Small: return moe::launch_moe_gemm_small(p, moe::kGemm2Bf16, nullptr, sms, s);
@@ -351,6 +357,7 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
   e = cudaSuccess;
   for (int k = 0; k <= last_kernel && e == cudaSuccess; ++k) {
     if (k == moe::kKDispatchFinish && p.disp_chunks <= 1) continue;  // one-CTA dispatch: nothing to launch
+    if (k == moe::kKGemm2Small && streamed) continue;                 // ran inside the GEMM1 launch
     e = timed(hd, k, s, [&] { return run(k); });
   }
   return cuda_fail(e);

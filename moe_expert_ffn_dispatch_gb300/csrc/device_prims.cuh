@@ -182,6 +182,37 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0,
 
 // generic-proxy shared-memory writes -> visible to the async proxy (tensor core, TMA)
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// global-memory data written by generic stores (of other CTAs, acquired
+// through a flag) -> visible to this thread's later bulk copies
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Spin until *flag >= want (acquire), with the same bound as the mbarrier
+// waits: false if the budget ran out (reported, abort raised) or another
+// role raised abort.
+__device__ __forceinline__ bool spin_until_ge(const int32_t* flag, int want, volatile int* abort, int32_t* status,
+                                              int site) {
+  if (ld_acquire_gpu(flag) >= want) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (ld_acquire_gpu(flag) >= want) return true;
+    __nanosleep(64);
+    if ((++n & 255u) == 0) {
+      if (abort && *abort) return false;
+      if (global_timer_ns() - t0 > kWaitBudgetNs) {
+        report_timeout(status, site);
+        if (abort) *abort = 1;
+        return false;
+      }
+    }
+  }
+}
 
 // true in exactly one lane of the (converged) warp: lets a warp run a loop
 // with warp-uniform values while a single lane issues TMA / tcgen05 work

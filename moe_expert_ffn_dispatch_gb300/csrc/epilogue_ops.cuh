@@ -136,6 +136,13 @@ __device__ void gemm1_item_done(const FwdParams& p, int blk, int tiles, int done
   if (*s_flag) {
     __threadfence();
     requant_rows(p, r0, n, s_red, ctid, big);
+    // the block's x2 / s2 are complete: one more count on its ticket
+    // (tiles + 1) tells a GEMM2 running in the same launch that it may read them
+    consumer_sync();
+    if (ctid == 0) {
+      __threadfence();
+      atomicAdd(ws_ptr<int32_t>(p, p.L.blk_ticket) + blk, 1);
+    }
   }
 }
 

@@ -47,7 +47,7 @@ constexpr int KC = 2048;               // K bytes per stage (one bulk copy per r
 constexpr int STAGES = 3;
 constexpr int kMaxK = kSmallMaxK;      // token rows of a run stay resident: MT x K bytes
 constexpr int kInfoSlots = 6;          // > STAGES: per-item token info ring
-constexpr int kSlotCache = 16;         // small-slot table entries a CTA can touch
+constexpr int kSlotCache = 8;          // small-slot table entries a CTA can touch, per GEMM
 constexpr int kRowsPerWarp = BN / kConsumerWarps;  // 4
 
 constexpr int OFF_W = 0;                                        // STAGES x [BN][KC] weights
@@ -55,8 +55,8 @@ constexpr int OFF_T = OFF_W + STAGES * BN * KC;                 // [m][K] token 
 constexpr int OFF_Y = OFF_T + MT * kMaxK;                       // 2 x [BN][MT] fp32
 constexpr int OFF_BAR = OFF_Y + 2 * BN * MT * 4;                // full, empty [STAGES]; tok_full, tok_empty
 constexpr int OFF_INFO = OFF_BAR + (2 * STAGES + 2) * 8;        // kInfoSlots x {scale, row, token}[MT]
-constexpr int OFF_SLOT = OFF_INFO + kInfoSlots * 3 * MT * 4;    // kSlotCache x {e, row0, rows}
-constexpr int OFF_MISC = OFF_SLOT + kSlotCache * 3 * 4;         // abort, flag, red[8], tok[MT]
+constexpr int OFF_SLOT = OFF_INFO + kInfoSlots * 3 * MT * 4;    // 2 x kSlotCache x {e, row0, rows}: GEMM1, GEMM2
+constexpr int OFF_MISC = OFF_SLOT + 2 * kSlotCache * 3 * 4;     // abort, flag, red[8], tok[MT]
 constexpr int SMEM_BYTES = OFF_MISC + (2 + kConsumerWarps + MT) * 4;
 static_assert(kRowsPerWarp * MT == 32, "one reduced value per lane");
 static_assert(kInfoSlots > STAGES, "info ring must outlive the stage ring");
@@ -160,8 +160,47 @@ struct SmallItem {
   int slot, e, row0, m, jt;
 };
 
+// Ring positions of a thread's role, carried from GEMM1 into GEMM2 when both
+// run in one launch (the rings and barriers are not re-initialised between).
+struct SmallState {
+  int stage_it = 0, item_no = 0, run_no = 0;
+};
+
+__device__ __forceinline__ void init_rings(char* smem) {
+  if (threadIdx.x == 0) {
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    for (int s = 0; s < 2 * STAGES + 2; ++s) mbar_init(&full[s], (s < STAGES || s == 2 * STAGES) ? 1 : kConsumerWarps);
+    *reinterpret_cast<volatile int*>(smem + OFF_MISC) = 0;  // abort flag
+    fence_barrier_init();
+  }
+}
+
+// this CTA's slots of one GEMM's item range into its shared-memory cache
+// (the caller synchronises the block afterwards)
+template <bool G1>
+__device__ __forceinline__ void cache_slots(const FwdParams& p, char* smem) {
+  const int J = G1 ? p.I / (BN / 2) : p.h / BN;
+  const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
+  const int st = SlotTable::stride(p.E);
+  const int32_t* sm_exp = slots + SlotTable::kHeader + 4 * st;
+  const int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges) + (G1 ? 0 : kMaxCtas + 1);
+  const long it_begin = ranges[blockIdx.x], it_end = ranges[blockIdx.x + 1];
+  const int slot_first = static_cast<int>(it_begin / J);
+  const int n_cached = it_end > it_begin ? static_cast<int>((it_end - 1) / J) - slot_first + 1 : 0;
+  int32_t* cache = reinterpret_cast<int32_t*>(smem + OFF_SLOT) + (G1 ? 0 : 3 * kSlotCache);
+  if (threadIdx.x < kSlotCache && threadIdx.x < n_cached) {
+    const int sl = slot_first + threadIdx.x;
+    cache[3 * threadIdx.x + 0] = sm_exp[sl];
+    cache[3 * threadIdx.x + 1] = sm_exp[st + sl];
+    cache[3 * threadIdx.x + 2] = sm_exp[2 * st + sl];
+  }
+}
+
+// One GEMM over this CTA's item range.  `streamed`: GEMM2 running in the
+// same launch right after GEMM1 -- each small slot's rows are read only once
+// the CTA that requantised them has marked the slot's ticket (tiles + 1).
 template <int MODE>
-__device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
+__device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss, bool streamed) {
   constexpr bool G1 = (MODE == kGemm1SwiGLU || MODE == kGemm1Raw);
   constexpr bool RAW = (MODE == kGemm1Raw || MODE == kGemm2Raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -171,7 +210,7 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
   float* info_scale = reinterpret_cast<float*>(smem + OFF_INFO);                 // [slot][MT]
   int32_t* info_row = reinterpret_cast<int32_t*>(smem + OFF_INFO) + kInfoSlots * MT;
   int32_t* info_tok = info_row + kInfoSlots * MT;
-  int32_t* slot_cache = reinterpret_cast<int32_t*>(smem + OFF_SLOT);            // [kSlotCache][3]
+  int32_t* slot_cache = reinterpret_cast<int32_t*>(smem + OFF_SLOT) + (G1 ? 0 : 3 * kSlotCache);  // [kSlotCache][3]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC);
   int* s_flag = reinterpret_cast<int*>(smem + OFF_MISC) + 1;
   float* s_red = reinterpret_cast<float*>(smem + OFF_MISC) + 2;
@@ -198,23 +237,6 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
   const int n_cached = it_end > it_begin ? static_cast<int>((it_end - 1) / J) - slot_first + 1 : 0;
   const int site = (G1 ? kKGemm1Small : kKGemm2Small) * 16;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    mbar_init(tok_full, 1);
-    mbar_init(tok_empty, kConsumerWarps);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (threadIdx.x < kSlotCache && threadIdx.x < n_cached) {
-    const int sl = slot_first + threadIdx.x;
-    slot_cache[3 * threadIdx.x + 0] = sm_exp[sl];
-    slot_cache[3 * threadIdx.x + 1] = sm_row0[sl];
-    slot_cache[3 * threadIdx.x + 2] = sm_rows[sl];
-  }
-  __syncthreads();
   const bool cached = n_cached <= kSlotCache;
   // items are walked as (slot, tile) pairs advanced one by one: no 64-bit
   // division by J per item
@@ -250,7 +272,14 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
     const int8_t* x2 = ws_ptr<int8_t>(p, p.L.x2);
     // token info is loaded one item ahead so its latency hides behind the copies
     const int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
-    auto load_info = [&](const SmallItem& x, int& tok, float& sc) {
+    // streamed GEMM2: a slot's s2 and x2 are read only after its requant is
+    // marked done (ticket = GEMM1 tiles + 1), by any CTA of this launch
+    const int32_t* blk_ticket = ws_ptr<int32_t>(p, p.L.blk_ticket);
+    const int g1_tiles = p.I / (BN / 2);
+    auto load_info = [&](const SmallItem& x, int& tok, float& sc) -> bool {
+      if (!G1 && streamed &&
+          !__all_sync(0xffffffffu, spin_until_ge(blk_ticket + x.slot, g1_tiles + 1, abort_flag, status, site + 5)))
+        return false;
       if (lane < x.m) {
         const int r = x.row0 + lane;
         tok = row_token[r];
@@ -259,6 +288,7 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
         else if (p.fold_routing && x.e >= 0) sc = __fmul_rn(s2[r], p.scales[tk_of_row[r]]);  // folded row scale
         else sc = s2[r];
       }
+      return true;
     };
     int nx_tok = 0;
     float nx_scale = 0.0f;
@@ -266,9 +296,10 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
     int ps = slot_first, pj = jt_first;  // position of nx
     if (it_begin < it_end) {
       nx = item_of(ps, pj);
-      load_info(nx, nx_tok, nx_scale);
+      if (!load_info(nx, nx_tok, nx_scale)) return;
     }
-    int stage_it = 0, item_no = 0, run_slot = -1, run_no = 0;
+    int &stage_it = ss.stage_it, &item_no = ss.item_no, &run_no = ss.run_no;
+    int run_slot = -1;
     for (long it = it_begin; it < it_end; ++it, ++item_no) {
       const SmallItem cur = nx;
       const int cur_tok = nx_tok;
@@ -287,6 +318,8 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
         }
         if (lane == 0) mbar_arrive_expect_tx(tok_full, static_cast<uint32_t>(cur.m * K));
         __syncwarp();
+        // x2 written by another CTA's generic stores, read here by a bulk copy
+        if (!G1 && streamed) fence_proxy_async_global();
         if (lane < cur.m) {
           const int8_t* trow =
               !G1 ? x2 + static_cast<size_t>(cur.row0 + lane) * p.I
@@ -325,7 +358,7 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
         }
         nx = item_of(ps, pj);
         // the items of one run share the expert's token rows, and so their info
-        if (nx.slot != cur.slot) load_info(nx, nx_tok, nx_scale);
+        if (nx.slot != cur.slot && !load_info(nx, nx_tok, nx_scale)) return;
       }
     }
     return;
@@ -335,7 +368,8 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem) {
   const int ctid = threadIdx.x;
   float* hbuf = ws_ptr<float>(p, p.L.hbuf);
   uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
-  int stage_it = 0, item_no = 0, run_items = 0, run_slot = -1, run_no = 0;
+  int &stage_it = ss.stage_it, &item_no = ss.item_no, &run_no = ss.run_no;
+  int run_items = 0, run_slot = -1;
   bool tok_ok = true;
   int cs = slot_first, cj = jt_first;  // position of the current item
   for (long it = it_begin; it < it_end; ++it, ++item_no) {
@@ -448,7 +482,31 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_small_kernel(FwdParams p
   // everything below reads what the preceding kernel wrote
   grid_dependency_wait();
   grid_launch_dependents();
-  small_path::run<MODE>(p, raw, smem);
+  constexpr bool G1 = (MODE == kGemm1SwiGLU || MODE == kGemm1Raw);
+  small_path::init_rings(smem);
+  small_path::cache_slots<G1>(p, smem);
+  __syncthreads();
+  small_path::SmallState ss;
+  small_path::run<MODE>(p, raw, smem, ss, false);
+}
+
+// GEMM2 streamed behind GEMM1 in one persistent launch (one CTA per SM, all
+// resident): each CTA runs its GEMM1 items, then its GEMM2 items through the
+// same rings, so its weight stream moves on to GEMM2 as soon as its own
+// GEMM1 work is issued; a GEMM2 slot waits (bounded) only for the requant of
+// that slot's rows, which the CTA completing the slot's GEMM1 tiles marks on
+// the slot's ticket.  GEMM1 work never waits on GEMM2, so every wait ends.
+__global__ void __launch_bounds__(kThreads, 1) moe_gemm_small_streamed_kernel(FwdParams p) {
+  extern __shared__ __align__(128) char smem[];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  small_path::init_rings(smem);
+  small_path::cache_slots<true>(p, smem);
+  small_path::cache_slots<false>(p, smem);
+  __syncthreads();
+  small_path::SmallState ss;
+  small_path::run<kGemm1SwiGLU>(p, nullptr, smem, ss, false);
+  small_path::run<kGemm2Bf16>(p, nullptr, smem, ss, true);
 }
 
 }  // namespace
@@ -457,7 +515,8 @@ cudaError_t moe_gemm_small_prepare_attributes() {
   const void* fns[] = {reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm1SwiGLU>),
                        reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm2Bf16>),
                        reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm1Raw>),
-                       reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm2Raw>)};
+                       reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm2Raw>),
+                       reinterpret_cast<const void*>(moe_gemm_small_streamed_kernel)};
   for (const void* f : fns) {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -476,6 +535,13 @@ cudaError_t launch_moe_gemm_small(const FwdParams& p, int mode, int32_t* raw_acc
     case kGemm2Raw: return cudaLaunchKernelEx(&cfg, moe_gemm_small_kernel<kGemm2Raw>, p, raw_acc);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_moe_gemm_small_streamed(const FwdParams& p, int num_ctas, cudaStream_t s) {
+  if (p.bs == 0) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(num_ctas), dim3(kThreads), SMEM_BYTES, s, attr);
+  return cudaLaunchKernelEx(&cfg, moe_gemm_small_streamed_kernel, p);
 }
 
 }  // namespace moe

@@ -175,6 +175,8 @@ cudaError_t launch_dispatch_finish(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_requant_big(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_combine(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_moe_gemm_small(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);
+// GEMM1 then GEMM2 of the small experts in one launch (GEMM2 streamed behind GEMM1)
+cudaError_t launch_moe_gemm_small_streamed(const FwdParams& p, int num_ctas, cudaStream_t s);
 cudaError_t launch_moe_gemm_big(const FwdParams& p, const TcMaps& maps, int mode, int32_t* raw_acc, int num_ctas,
                                 cudaStream_t s);
 cudaError_t moe_gemm_small_prepare_attributes();
