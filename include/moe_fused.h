@@ -256,8 +256,10 @@ int moe_fused_debug_region(moe_fused_handle_t* handle, int region, size_t* offse
 
 /* Phase-stop forward: enqueue kernels 0..last_kernel of the forward (kernel
  * ids as for get_timing) and stop, so that a test can read the intermediates
- * of that stage before a later stage reuses their space (h is overwritten by
- * y2 in GEMM2).  Same arguments, checks and errors as moe_fused_forward. */
+ * of that stage before a later stage changes them (a forward that stops
+ * before GEMM2 runs the small experts' GEMM1 in a launch of its own, without
+ * the GEMM2 that otherwise streams behind it).  Same arguments, checks and
+ * errors as moe_fused_forward. */
 int moe_fused_debug_forward_until(moe_fused_handle_t* handle, const moe_fused_args_t* args, void* workspace,
                                   size_t workspace_bytes, int last_kernel, void* stream);
 
@@ -270,6 +272,19 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* handle, const moe_fused_ar
  * dispatched are left untouched. */
 int moe_fused_debug_gemm_acc(moe_fused_handle_t* handle, const moe_fused_args_t* args, void* workspace,
                              size_t workspace_bytes, int which, int32_t* acc, void* stream);
+
+/* Exercise the kernels' bounded waits: one thread waits for something that
+ * never happens -- which = 0: an mbarrier phase nobody arrives on; which = 1:
+ * a workspace flag nobody sets (the cross-CTA ready-flag spin) -- gives up
+ * after the wait budget (2 s), records kErrWaitTimeout and site
+ * MOE_DEBUG_WAIT_SITE + which in the workspace's status word, and returns.
+ * Nothing faults or traps; the next forward clears the status.  Asynchronous
+ * on `stream`; read the result with moe_fused_get_status, which then returns
+ * MOE_ERR_DEVICE_TIMEOUT.  MOE_ERR_INVALID_ARG for a bad handle, workspace or
+ * `which`, MOE_ERR_WORKSPACE_TOO_SMALL below the reported size. */
+#define MOE_DEBUG_WAIT_SITE 240
+int moe_fused_debug_wait_timeout(moe_fused_handle_t* handle, void* workspace, size_t workspace_bytes, int which,
+                                 void* stream);
 
 #ifdef __cplusplus
 }

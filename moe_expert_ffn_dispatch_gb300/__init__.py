@@ -55,7 +55,8 @@ REGIONS = {"status": 0, "counts": 1, "offsets": 2, "row_of": 3, "tk_of_row": 4, 
 EXPORTS = ["moe_fused_create", "moe_fused_workspace_size", "moe_fused_forward", "moe_fused_get_status",
            "moe_fused_destroy", "moe_fused_strerror", "moe_fused_set_timing", "moe_fused_get_timing",
            "moe_fused_kernel_name", "moe_fused_dispatch_noalloc", "moe_fused_debug_region",
-           "moe_fused_debug_forward_until", "moe_fused_debug_gemm_acc"]
+           "moe_fused_debug_forward_until", "moe_fused_debug_gemm_acc", "moe_fused_debug_wait_timeout"]
+DEBUG_WAIT_SITE = 240  # MOE_DEBUG_WAIT_SITE
 
 P = ctypes.c_void_p
 I32 = ctypes.c_int32
@@ -113,6 +114,7 @@ def lib() -> ctypes.CDLL:
         L.moe_fused_debug_region.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t),
                                              ctypes.POINTER(ctypes.c_size_t)]
         L.moe_fused_debug_gemm_acc.argtypes = [P, ctypes.POINTER(Args), P, ctypes.c_size_t, ctypes.c_int, P, P]
+        L.moe_fused_debug_wait_timeout.argtypes = [P, P, ctypes.c_size_t, ctypes.c_int, P]
         L.moe_fused_debug_forward_until.argtypes = [P, ctypes.POINTER(Args), P, ctypes.c_size_t, ctypes.c_int, P]
         L.moe_fused_dispatch_noalloc.argtypes = [P, P, I32, I32, I32, P, P, P]
         for name in EXPORTS:
@@ -195,6 +197,11 @@ def moe_fused_debug_forward_until(handle: int, args: Args, workspace: int, works
 def moe_fused_debug_gemm_acc(handle: int, args: Args, workspace: int, workspace_bytes: int, which: int,
                              acc: int, stream: int) -> int:
     return lib().moe_fused_debug_gemm_acc(handle, ctypes.byref(args), workspace, workspace_bytes, which, acc, stream)
+
+
+def moe_fused_debug_wait_timeout(handle: int, workspace: int, workspace_bytes: int, which: int, stream: int) -> int:
+    """Test-only: a bounded wait that runs out (0: mbarrier, 1: cross-CTA flag)."""
+    return lib().moe_fused_debug_wait_timeout(handle, workspace, workspace_bytes, which, stream)
 
 
 # ------------------------------------------------------------ torch wrapper

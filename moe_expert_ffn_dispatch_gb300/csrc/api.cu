@@ -16,6 +16,7 @@
 
 #include <cuda.h>
 
+#include "device_prims.cuh"
 #include "moe_fused.h"
 #include "moe_internal.h"
 
@@ -271,6 +272,24 @@ int prepare_maps(moe_fused_handle* hd, const moe::FwdParams& p) {
   return MOE_OK;
 }
 
+// One thread waits for what never comes (see moe_fused_debug_wait_timeout):
+// an mbarrier phase without arrivals, or a flag nobody sets.  The bounded
+// wait records the timeout in the status word and returns.
+__global__ void debug_wait_kernel(int32_t* status, const int32_t* flag, int which) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    moe::mbar_init(&bar, 1);
+    abort_flag = 0;
+    moe::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  volatile int* ab = &abort_flag;
+  if (which == 0) moe::mbar_wait_bounded(&bar, 0, ab, status, MOE_DEBUG_WAIT_SITE);
+  else moe::spin_until_ge(flag, 1, ab, status, MOE_DEBUG_WAIT_SITE + 1);
+}
+
 int cuda_fail(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
   std::fprintf(stderr, "moe_fused: CUDA error %s\n", cudaGetErrorString(e));
@@ -473,6 +492,22 @@ int moe_fused_debug_gemm_acc(moe_fused_handle_t* hd, const moe_fused_args_t* arg
   if (rc) return rc;
   cudaError_t e = moe::launch_moe_gemm_small(p, mode, acc, p.num_ctas, s);
   if (e == cudaSuccess) e = moe::launch_moe_gemm_big(p, hd->maps, mode, acc, p.num_ctas, s);
+  return cuda_fail(e);
+}
+
+int moe_fused_debug_wait_timeout(moe_fused_handle_t* hd, void* workspace, size_t workspace_bytes, int which,
+                                 void* stream) {
+  if (!hd || !workspace || (which != 0 && which != 1)) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < hd->L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return MOE_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* status = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + hd->L.status);
+  // status words 0..31 start clean; word 32 is the flag that nobody sets
+  cudaError_t e = cudaMemsetAsync(status, 0, 64 * sizeof(int32_t), s);
+  if (e == cudaSuccess) {
+    debug_wait_kernel<<<1, 32, 0, s>>>(status, status + 32, which);
+    e = cudaGetLastError();
+  }
   return cuda_fail(e);
 }
 

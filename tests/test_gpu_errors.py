@@ -61,3 +61,29 @@ def test_create_rejects_bad_config():
     for cfg in bad:
         rc, h, _ = m.moe_fused_create(cfg)
         assert rc < 0 and h == 0
+
+
+@pytest.mark.parametrize("which", [0, 1], ids=["mbarrier", "flag"])
+def test_bounded_wait_runs_out_and_reports(which):
+    """A wait that nothing satisfies gives up after its 2 s budget and reports
+    through the status word (no fault, no trap); the context stays usable and
+    the next forward clears the status."""
+    import time
+    blk, a, keep, out = _setup()
+    ws = blk.workspace()
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    assert m.moe_fused_debug_wait_timeout(blk.handle, ws.data_ptr(), ws.numel(), which, stream.cuda_stream) == m.MOE_OK
+    st = blk.status()
+    elapsed = time.perf_counter() - t0
+    assert st["rc"] == m.MOE_ERR_DEVICE_TIMEOUT
+    assert st["error_flags"] & 1
+    assert st["error_site"] == m.DEBUG_WAIT_SITE + which
+    assert 1.5 < elapsed < 30.0
+    assert m.moe_fused_debug_wait_timeout(blk.handle, ws.data_ptr(), ws.numel(), 2, stream.cuda_stream) == \
+        m.MOE_ERR_INVALID_ARG
+    assert _fwd(blk, a) == m.MOE_OK
+    torch.cuda.synchronize()
+    st = blk.status()
+    assert st["rc"] == m.MOE_OK and st["error_flags"] == 0
