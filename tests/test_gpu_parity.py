@@ -170,3 +170,23 @@ def test_signature_variants_unfused_and_folded():
     inp = synth.make_inputs(wl)
     run_and_check(inp, DEV, staged=True, blk=make_block(wl, DEV, unfused=True))
     run_and_check(inp, DEV, staged=True, blk=make_block(wl, DEV, fold_routing=True))
+
+
+# Shape limits: hidden or inter above 4096 (the dp4a path is off, every expert
+# takes the tensor cores, K spans many exact 1024-wide chunks), hidden at its
+# maximum (16384), 1024 experts with top-16 (most experts 0-2 rows), and a
+# GEMM2 contraction of 8192.
+LIMIT_CASES = [
+    synth.custom("e1024_top16_h8192", bs=24, hidden=8192, num_experts=1024, topk=16, inter=64, has_shared=True,
+                 masked_fraction=0.125, seed=61),
+    synth.custom("hidden16384", bs=20, hidden=16384, num_experts=8, topk=4, inter=192, has_shared=True, seed=62),
+    synth.custom("inter8192", bs=24, hidden=256, num_experts=4, topk=2, inter=8192, has_shared=True,
+                 smooth=True, seed=63),
+]
+
+
+@pytest.mark.parametrize("wl", LIMIT_CASES, ids=lambda w: w.name)
+def test_shape_limits_staged_parity(wl):
+    inp = synth.make_inputs(wl)
+    blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True)
+    check_raw_accumulators(blk, inp, ref, di, dw, DEV)
