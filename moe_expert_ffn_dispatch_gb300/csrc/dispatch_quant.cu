@@ -266,26 +266,30 @@ __device__ void dispatch_tail(const FwdParams& p, int32_t* dsm, int c, int off, 
     __syncthreads();
     const int G = p.num_ctas;
     int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges);
+    // 32-bit throughout (J * wp[ns] <= 1024 * 1025 * 20 < 2^31): CTA b starts
+    // at cost b * q + min(b, r) with q, r = total divmod G, one division per
+    // CTA at most
     for (int g = 0; g < 2; ++g) {
-      const long J = g == 0 ? p.I / 16 : p.h / 32;   // items per small slot, GEMM1 / GEMM2
-      const long total = J * wp[ns];
+      const int J = g == 0 ? p.I / 16 : p.h / 32;   // items per small slot, GEMM1 / GEMM2
+      const int total = J * wp[ns];
+      const int q = total / G, r = total - q * G;
       for (int b = tid; b <= G; b += kDispatchThreads) {
-        long it;
+        int it;
         if (b == G || ns == 0) {
-          it = static_cast<long>(ns) * J;
+          it = ns * J;
         } else {
-          const long target = total * b / G;
+          const int target = b * q + (b < r ? b : r);
           int lo = 0, hi = ns - 1;  // last slot whose first item starts at or before target
           while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (J * wp[mid] <= target) lo = mid;
             else hi = mid - 1;
           }
-          const long cost = wp[lo + 1] - wp[lo];
-          const long k = (target - J * wp[lo] + cost - 1) / cost;
+          const int cost = wp[lo + 1] - wp[lo];
+          const int k = (target - J * wp[lo] + cost - 1) / cost;
           it = lo * J + (k < J ? k : J);
         }
-        ranges[g * (kMaxCtas + 1) + b] = static_cast<int32_t>(it);
+        ranges[g * (kMaxCtas + 1) + b] = it;
       }
     }
     // per-forward epoch of the last-arriver counters used by the GEMM kernels
