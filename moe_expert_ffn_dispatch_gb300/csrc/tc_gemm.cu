@@ -565,12 +565,15 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          if (64 * half + 32 * cc < mblk) {
-            uint32_t v[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * TB + 64 * half + 32 * cc, v);
+        // 16 columns at a time: columns past the block's rows are not read
+        // (at 16 rows a block, 32-column loads read twice what it needs and
+        // compete with the MMA for tensor memory)
+        for (int cc = 0; cc < 4; ++cc) {
+          if (64 * half + 16 * cc < mblk) {
+            uint32_t v[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * TB + 64 * half + 16 * cc, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[32 * cc + j] += __float2int_rn(__uint_as_float(v[j]));
+            for (int j = 0; j < 16; ++j) acc[16 * cc + j] += __float2int_rn(__uint_as_float(v[j]));
           }
         }
         tc_fence_before();
