@@ -924,7 +924,10 @@ __global__ void __launch_bounds__(kRqWarps * 32) requant_big_kernel(FwdParams p)
 
 // Combine of every token (FusedDeepMoE analysis §4.2) when the forward has big
 // blocks; otherwise the small-expert GEMM2 already combined every token.
-__global__ void __launch_bounds__(256) combine_kernel(FwdParams p) {
+// 4 CTAs of 256 threads resident per SM (at most 64 registers a thread), so
+// the grid of 4 per SM runs as one wave: uncapped (72 registers) only 3 fit
+// and a quarter of the grid ran as a second, partial wave.
+__global__ void __launch_bounds__(256, 4) combine_kernel(FwdParams p) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
