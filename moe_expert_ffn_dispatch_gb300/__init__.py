@@ -377,3 +377,80 @@ class MoeFused:
         if rc:
             raise MoeError(rc, "moe_fused_debug_gemm_acc")
         del keep
+
+
+def _packed(specs, device, pinned: bool = False):
+    """Tensors of `specs` [(name, shape, dtype)] as views into one buffer,
+    each starting on a 256-byte boundary: one copy moves them all."""
+    offs, off = [], 0
+    for name, shape, dtype in specs:
+        n = int(torch.Size(shape).numel()) * torch.empty(0, dtype=dtype).element_size()
+        offs.append((name, shape, dtype, off, n))
+        off += (n + 255) // 256 * 256
+    buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+    if pinned:
+        buf = buf.pin_memory()
+    views = {name: buf[o:o + n].view(dtype).view(shape) for name, shape, dtype, o, n in offs}
+    return buf, views
+
+
+class GraphedStep:
+    """One whole inference step captured as a CUDA graph: one host-to-device
+    copy of this step's inputs (packed in one pinned buffer), the forward, and
+    one device-to-host copy of output, share_output and expert_token_nums
+    (packed likewise).  For serving loops with a fixed batch shape: write the
+    next step's inputs into `host_inputs` in place, call `run()`, synchronise
+    `stream`, read `host_outputs`.
+
+    host_inputs: dict with "x", "expert_ids", "expert_scales" and optionally
+    "mask" (CPU tensors of the block's dtypes and shapes, bs <= bs_max); their
+    values are copied into the step's own pinned buffer, whose views become
+    `self.host_inputs`.  weights: dict as for MoeFused.forward_inputs (device
+    tensors, not copied).
+    """
+
+    def __init__(self, blk: MoeFused, host_inputs: Dict[str, torch.Tensor], weights: Dict[str, torch.Tensor],
+                 stream: Optional[torch.cuda.Stream] = None):
+        self.blk = blk
+        self.weights = weights
+        dev = blk.device
+        specs = [(k, tuple(v.shape), v.dtype) for k, v in host_inputs.items()]
+        self._hin, self.host_inputs = _packed(specs, "cpu", pinned=True)
+        self._din, self.dev_inputs = _packed(specs, dev)
+        for k, v in host_inputs.items():
+            self.host_inputs[k].copy_(v)
+        bs, h = host_inputs["x"].shape
+        ospecs = [("output", (bs, h), blk.act_dtype), ("expert_token_nums", (blk.cfg.num_experts,), torch.int32)]
+        if blk.cfg.has_shared:
+            ospecs.append(("share_output", (bs, h), blk.act_dtype))
+        self._dout, self.dev_outputs = _packed(ospecs, dev)
+        self._hout, self.host_outputs = _packed(ospecs, "cpu", pinned=True)
+        self.stream = stream if stream is not None else torch.cuda.Stream(device=dev)
+        blk.workspace()  # allocated before the capture
+        with torch.cuda.stream(self.stream):
+            self._step()  # eager once: builds the tensor maps, checks the arguments
+        self.stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self._step()
+        self.stream.synchronize()
+
+    def _step(self):
+        self._din.copy_(self._hin, non_blocking=True)
+        o = self.dev_outputs
+        self.blk.forward_inputs(self.dev_inputs, self.weights, out=o["output"], share_out=o.get("share_output"),
+                                token_nums=o["expert_token_nums"])
+        self._hout.copy_(self._dout, non_blocking=True)
+
+    def run(self):
+        """Replay the step, asynchronous on `self.stream` (synchronise that
+        stream before reading host_outputs)."""
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()
+
+    def h2d_bytes(self) -> int:
+        """Bytes of this step's inputs (the packed copy moves these plus alignment padding)."""
+        return sum(v.numel() * v.element_size() for v in self.host_inputs.values())
+
+    def d2h_bytes(self) -> int:
+        return sum(v.numel() * v.element_size() for v in self.host_outputs.values())

@@ -190,3 +190,28 @@ def test_shape_limits_staged_parity(wl):
     inp = synth.make_inputs(wl)
     blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True)
     check_raw_accumulators(blk, inp, ref, di, dw, DEV)
+
+
+def test_graphed_step_matches_eager_forward():
+    """The captured step (one packed H2D copy, the forward, one packed D2H copy
+    as one CUDA graph) gives the eager forward's outputs bit for bit, and
+    picks up new inputs written into its pinned host views in place."""
+    import moe_expert_ffn_dispatch_gb300 as m
+    wl = CASES[3]  # zipf_skew: small and tensor-core experts, masked tokens, the shared expert
+    inp = synth.make_inputs(wl)
+    blk = make_block(wl, DEV)
+    di, dw = device_inputs(inp, DEV), device_weights(inp, DEV)
+    step = m.GraphedStep(blk, {k: v.cpu() for k, v in di.items()}, dw)
+    host = step.host_inputs  # the step's own pinned input views
+    for trial in range(2):
+        step.run()
+        step.stream.synchronize()  # the step's own stream: nothing else orders it
+        got = {k: v.clone() for k, v in step.host_outputs.items()}
+        out, sout, nums = blk.forward_inputs({k: v.to(DEV) for k, v in host.items()}, dw)
+        torch.cuda.synchronize()
+        assert torch.equal(got["output"].view(torch.int16), out.cpu().view(torch.int16))
+        assert torch.equal(got["share_output"].view(torch.int16), sout.cpu().view(torch.int16))
+        assert torch.equal(got["expert_token_nums"], nums.cpu())
+        # next step's inputs, written in place
+        host["x"].copy_(torch.flip(host["x"], dims=[0]))
+        host["expert_ids"].copy_(torch.roll(host["expert_ids"], 1, dims=0))
