@@ -215,3 +215,31 @@ def test_graphed_step_matches_eager_forward():
         # next step's inputs, written in place
         host["x"].copy_(torch.flip(host["x"], dims=[0]))
         host["expert_ids"].copy_(torch.roll(host["expert_ids"], 1, dims=0))
+
+
+def _random_cases(n=10, seed=2024):
+    """Seeded random shapes within the library's limits (hidden and inter
+    multiples of 64, topk <= min(E, 16)): ragged K tails, partial tiles, both
+    GEMM paths, masks, smooth scales and the signature variants."""
+    import random
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        E = rng.choice([1, 2, 3, 5, 8, 17, 40])
+        topk = rng.randint(1, min(E, 16))
+        per_expert = rng.random() < 0.3
+        out.append(synth.custom(
+            "rand%d" % i, bs=rng.choice([1, 3, 9, 31, 64, 130, 257]), hidden=64 * rng.randint(1, 12),
+            num_experts=E, topk=topk, inter=64 * rng.randint(1, 10), has_shared=rng.random() < 0.7,
+            routing=rng.choice(["uniform", "zipf"]) if topk < E else "uniform",
+            masked_fraction=rng.choice([0.0, 0.0, 0.3]), smooth=per_expert or rng.random() < 0.4,
+            share_smooth=rng.random() < 0.3, seed=300 + i, act_dtype=rng.choice(["bf16", "bf16", "fp16"]),
+            scale_dtype=rng.choice(["f32", "f32", "bf16", "fp16"]), smooth_per_expert=per_expert))
+    return out
+
+
+@pytest.mark.parametrize("wl", _random_cases(), ids=lambda w: w.name)
+def test_random_shapes_staged_parity(wl):
+    inp = synth.make_inputs(wl)
+    blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True)
+    check_raw_accumulators(blk, inp, ref, di, dw, DEV)
