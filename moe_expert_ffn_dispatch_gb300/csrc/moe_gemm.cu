@@ -9,9 +9,9 @@
 //     x2 = RNE((h * 127) * (1/amax)) clamped to +-127.
 //   GEMM2 (§3.4, §5.2.2; epilogue §6.2; combine §4.2):
 //     acc2[r, j] = sum_i x2[r, i] * W2[e][j][i]
-//     y2[r, j] = bf16((float(acc2) * w2_scale[e][j]) * s2[r])
+//     y2[r, j] = act((float(acc2) * w2_scale[e][j]) * s2[r])   (act: bf16, or fp16)
 //     then, once every row of a token is done, the combine:
-//     output[t] = bf16(sum_k float(y2[row(t,k)]) * expert_scales[t, k]),
+//     output[t] = act(sum_k float(y2[row(t,k)]) * expert_scales[t, k]),
 //     fp32 sum from 0, k ascending, multiply and add rounded separately.
 //
 // This file holds the small-expert kernel; tc_gemm.cu the big-expert one.
@@ -28,8 +28,10 @@
 // The requant and the combine run in the CTA that completes the last tile of
 // a row block (GEMM1) or of a token (GEMM2): each such CTA fences its
 // writes and bumps a per-forward counter (reset by the dispatch kernel); the
-// one that brings a counter to its total does the work.  No CTA waits for
-// another.
+// one that brings a counter to its total does the work.  In a forward, GEMM2
+// streams behind GEMM1 in the same launch (moe_gemm_small_streamed_kernel):
+// the only wait on another CTA is a GEMM2 slot's bounded wait for the requant
+// of its rows, marked on the same counter.
 #include "device_prims.cuh"
 #include "epilogue_ops.cuh"
 #include "moe_internal.h"

@@ -15,9 +15,12 @@
 //
 // Tile: 128 weight rows x up to 128 token rows of one expert x all of K,
 // weights as the MMA's M operand (tensor-memory lanes, read by the MMA from
-// tensor memory), tokens as N (shared memory).  Shared-memory bandwidth is
-// what bounds this kernel: per 128 of K it carries the int8 weight stage
-// (TMA write + converter read) and the f16 token stage (TMA write + MMA read).  For
+// tensor memory), tokens as N (shared memory).  Per 128 of K the int8 weight
+// stage passes through shared memory once (TMA write, converter read) and so
+// does the f16 token stage (TMA write, MMA read).  What bounds the kernel is
+// the loop between the converter warps and the MMA through tensor memory:
+// the converters' ALU work and stores, and the MMA's reads of the weight
+// operand, which at small N (few token rows) cost about as much as at N = 128.  For
 // GEMM1 the 128 rows are 64 gate rows and the 64 matching up rows, laid out
 // so that each 32-lane quadrant of tensor memory holds 16 gate rows in its
 // lanes 0..15 and the 16 matching up rows in lanes 16..31 (every warp
@@ -35,15 +38,16 @@
 //               shared-memory ring that the other roles read
 //   warps 4..7  convert int8 weight stages to f16, one weight row per
 //               thread, into a 4-deep ring in tensor memory (the MMA's A
-//               operand), which keeps the f16 weights off shared memory
+//               operand), which keeps the f16 weights off shared memory;
+//               software-pipelined when the launch's blocks are short
 //   warp 1      one thread issues tcgen05.mma (M128, N = rows rounded to 16,
 //               K16) stage by stage into two tensor-memory accumulators,
 //               alternating per 1024 of K, and commits to the ring and
 //               accumulator barriers
 //   warps 8..15 drain accumulators (tcgen05.ld) into int32, then the
 //               epilogue (GEMM1: dequantised gate | up values, SwiGLU
-//               being applied by the requant kernel; GEMM2: bf16 dequant);
-//               two warps per tensor-memory lane quadrant
+//               being applied by the requant kernel; GEMM2: dequant to the
+//               activation dtype); two warps per tensor-memory lane quadrant
 // All rings are mbarrier full/empty pairs (the FIFO of the Mega-MoE
 // analysis §4); every wait is bounded.
 #include <cuda_fp16.h>
