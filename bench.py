@@ -57,13 +57,40 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def _code_only(src: str) -> str:
+    """C / CUDA source without comments and with whitespace collapsed (string
+    and character literals, e.g. inline PTX, kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sha(kernel: str) -> str:
-    """Hash of the kernel's source file and the headers it includes."""
+    """Hash of the code (comments and layout ignored) of the kernel's source
+    file and the headers it includes: ncu counters taken on one version stay
+    valid for another that differs only in comments."""
     csrc = os.path.join(ROOT, "moe_expert_ffn_dispatch_gb300", "csrc")
     hsh = hashlib.sha256()
     for name in (KERNEL_SOURCES[kernel], "device_prims.cuh", "epilogue_ops.cuh", "moe_internal.h"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            hsh.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            hsh.update(_code_only(f.read()).encode())
     return hsh.hexdigest()[:16]
 
 
