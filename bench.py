@@ -271,6 +271,17 @@ def host_alg(wl):
     return algorithmic_bytes(wl, counts, int(act.sum()))
 
 
+def per_forward_summary(us):
+    """Median, 10th and 90th percentile (nearest rank) of per-forward times."""
+    v = sorted(us)
+    if not v:
+        return {"median": None, "p10": None, "p90": None}
+
+    def rank(q):
+        return v[min(len(v) - 1, max(0, math.ceil(q * len(v)) - 1))]
+    return {"median": statistics.median(v), "p10": rank(0.10), "p90": rank(0.90)}
+
+
 def whole_job_tokens_per_s(bs, world_size, steps, seconds):
     """Tokens all ranks processed divided by the (max-over-ranks) time."""
     return bs * world_size * steps / seconds
@@ -358,6 +369,18 @@ def run_ours(args, wl, ws, rank, local):
     blk.set_timing(False)
     launches = sum(n for _, n in ktimes.values())  # the timed pass launches the same kernels
 
+    # ---- per-forward distribution: a third pass of the same K forwards with a
+    # pair of events around each forward (an event between two forwards ends
+    # the overlap of one forward's last kernel with the next one's first, so
+    # this pass gives the spread, not the headline)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_ev, b_ev in ev:
+        a_ev.record(stream)
+        blk.forward_inputs(di, weights, out=out, share_out=sout, token_nums=nums)
+        b_ev.record(stream)
+    torch.cuda.synchronize()
+    per_fwd = per_forward_summary([a_ev.elapsed_time(b_ev) * 1e3 for a_ev, b_ev in ev])
+
     # ---- end to end through the public API: host inputs in, host results out.
     # The step is one CUDA graph (GraphedStep): one H2D copy of the inputs from
     # pinned host memory, the forward, one D2H copy of the outputs.  If capture
@@ -434,6 +457,8 @@ def run_ours(args, wl, ws, rank, local):
                                "(%.1f us per forward instrumented)" % (args.steps, ms_instrumented / args.steps * 1e3)},
         "roofline_step": {**roofline_of(alg["step"], alg["int_ops"], ms_total / args.steps / 1e3, peaks),
                           "alg_bytes": alg["step"], "int_ops": alg["int_ops"]},
+        "per_forward_us": {**per_fwd, "timing": "CUDA events around each forward, third pass of the same %d "
+                                               "forwards" % args.steps},
         "kernels_us": {k: (v[0] / max(v[1], 1) * 1e3) for k, v in ktimes.items()},
         "gpu_launches": launches,
         "e2e": {"value": whole_job_tokens_per_s(wl.bs, ws, e2e_steps, e2e_s), "unit": "tokens/s",
@@ -441,6 +466,9 @@ def run_ours(args, wl, ws, rank, local):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "path": e2e_path},
         "clocks": clk.summary(),
     }
+    if inp.mask is not None:
+        # masked workloads: tokens that take part in the block (inactive ones only get zero rows)
+        res["active_tokens_per_s"] = whole_job_tokens_per_s(n_active, ws, args.steps, ms_total / 1e3)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     if ws > 1:

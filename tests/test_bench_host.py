@@ -36,3 +36,12 @@ def test_recorded_traffic_requires_matching_sha(tmp_path, monkeypatch):
         f.write("traffic_bytes_per_launch: 12345\nkernel_sha: 0000000000000000\n")
     assert bench.recorded_traffic("gemm1_big", "prefill") is None
     assert bench.recorded_traffic("gemm1_big", "mid512") is None
+
+
+def test_per_forward_summary_percentiles():
+    s = bench.per_forward_summary([float(i) for i in range(1, 101)])  # 1 .. 100
+    assert s["median"] == 50.5
+    assert s["p10"] == 10.0 and s["p90"] == 90.0
+    one = bench.per_forward_summary([7.0])
+    assert one == {"median": 7.0, "p10": 7.0, "p90": 7.0}
+    assert bench.per_forward_summary([])["median"] is None
