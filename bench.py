@@ -552,12 +552,17 @@ def main():
                     help="MOE_FLAG_FOLD_ROUTING: routing weight folded into the GEMM2 row scale")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the workload's expert count (smaller cases for profiler captures)")
+    ap.add_argument("--bs", type=int, default=0,
+                    help="override the workload's batch size (with --experts: the same rows per expert "
+                         "on fewer weights, for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_env()
     wl = synth.WORKLOADS[args.workload]
     if args.experts:
         wl = synth.Workload(**{**wl.__dict__, "num_experts": args.experts, "name": "%s_e%d" % (wl.name, args.experts)})
+    if args.bs:
+        wl = synth.Workload(**{**wl.__dict__, "bs": args.bs, "name": "%s_bs%d" % (wl.name, args.bs)})
     if args.impl == "reference":
         res = run_reference(args, wl, ws, rank)
     else:
