@@ -192,7 +192,10 @@ def algorithmic_bytes(wl, counts_per_expert, n_active, unfused=False):
     ops = {k: 0 for k in keys}
     any_big = False
     for m, routed in groups:
-        small = small_ok and m <= SMALL_ROWS
+        # a batch of at most SMALL_ROWS tokens runs every expert in the *_small
+        # kernels (more rows, from repeated ids, in several slots; the weights
+        # still count once here)
+        small = small_ok and (m <= SMALL_ROWS or bs <= SMALL_ROWS)
         any_big |= not small
         if small:
             out["gemm1_small"] += 2 * I * h + 8 * I + m * (h + I + 4)

@@ -225,12 +225,16 @@ int moe_fused_dispatch_noalloc(const int32_t* expert_ids, const uint8_t* x_activ
  * kernel id k < max_kernels the summed milliseconds ms[k] and launch count
  * launches[k] (host arrays), returns the number of kernel ids, and clears the
  * record.  Kernel ids: 0 dispatch + quant, 1 dispatch finish (multi-CTA
- * dispatch of batches with bs*topk > 2048; not launched otherwise), 2 expand
+ * dispatch of batches with bs*topk > 8192; not launched otherwise), 2 expand
  * (f16 token rows for the tensor-core GEMMs), 3 GEMM1 + SwiGLU (+ requant)
  * for experts with at most 8 rows (dp4a weight streaming), 4 GEMM1 + dequant
  * for the other experts (tcgen05), 5 SwiGLU + requant of their rows, 6 GEMM2
  * + dequant (+ combine when every expert has at most 8 rows), 7 GEMM2 +
- * dequant (tcgen05), 8 combine. */
+ * dequant (tcgen05), 8 combine.  A batch of at most 8 tokens runs every
+ * expert through kernels 3 and 6 (an expert that repeated ids give more than
+ * 8 rows in several slots of at most 8), so kernels 2, 4, 5, 7 and 8 are not
+ * launched for it (2 still is with per-expert smooth scales, for the per-row
+ * quant). */
 int moe_fused_set_timing(moe_fused_handle_t* handle, int enable);
 int moe_fused_get_timing(moe_fused_handle_t* handle, float* ms, int32_t* launches, int max_kernels);
 const char* moe_fused_kernel_name(int kernel_id);
@@ -249,7 +253,7 @@ const char* moe_fused_kernel_name(int kernel_id);
  *   17 row-block counters  18 token counters [bs_max]  19 token totals [bs_max]
  *   20 small-expert item ranges  21 x1h [rows,h] f16  22 x2h [rows,inter] f16
  *   23 multi-CTA dispatch counts [chunks][E] then skipped ids [chunks]
- *      (empty when bs_max*topk <= 2048: one CTA dispatches alone)
+ *      (empty when bs_max*topk <= 8192: one CTA dispatches alone)
  * `rows` = bs*topk + bs: routed row r at index r (r < R), the shared expert's
  * i-th active token at index bs*topk + i.  Writes *offset and *bytes. */
 int moe_fused_debug_region(moe_fused_handle_t* handle, int region, size_t* offset, size_t* bytes);

@@ -157,6 +157,10 @@ int build_params(moe_fused_handle* hd, const moe_fused_args_t* a, void* ws, size
   p->with_tickets = 1;
   const bool fused_ok = (c.flags & MOE_FLAG_UNFUSED) == 0 && c.hidden <= moe::kSmallMaxK && c.inter <= moe::kSmallMaxK;
   p->small_rows = fused_ok ? moe::kSmallRows : 0;
+  // a batch of at most small_rows tokens never needs the tensor-core path: an
+  // expert can exceed small_rows rows only through repeated ids, and then takes
+  // several small slots (its weights streamed once per slot)
+  p->small_only = p->small_rows > 0 && a->bs <= p->small_rows;
   p->num_ctas = hd->num_sms < moe::kMaxCtas ? hd->num_sms : moe::kMaxCtas;
   p->x = static_cast<const uint16_t*>(a->x);
   p->ids = a->expert_ids;
@@ -377,6 +381,12 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
   for (int k = 0; k <= last_kernel && e == cudaSuccess; ++k) {
     if (k == moe::kKDispatchFinish && p.disp_chunks <= 1) continue;  // one-CTA dispatch: nothing to launch
     if (k == moe::kKGemm2Small && streamed) continue;                 // ran inside the GEMM1 launch
+    // no big block can exist: the tensor-core GEMMs, their requant and the
+    // combine kernel would return at once (the small GEMM2 combines every
+    // token), and the expand kernel too unless it quantises per routed row
+    if (p.small_only && (k == moe::kKGemm1Big || k == moe::kKRequantBig || k == moe::kKGemm2Big ||
+                         k == moe::kKCombine || (k == moe::kKExpand && !p.xq_per_row)))
+      continue;
     e = timed(hd, k, s, [&] { return run(k); });
   }
   return cuda_fail(e);

@@ -180,7 +180,10 @@ __device__ void dispatch_tail(const FwdParams& p, int32_t* dsm, int c, int off, 
   }
 
   // 5. slot tables: experts with rows in ascending id, split by row count,
-  //    then the shared expert in the list its row count selects
+  //    then the shared expert in the list its row count selects.  In a batch
+  //    of at most small_rows tokens (small_only) every expert is small: one
+  //    with more rows (repeated ids) takes consecutive slots of at most
+  //    small_rows rows each, so the tensor-core launches have nothing to do.
   const int st = SlotTable::stride(E);
   int32_t* b_exp = slots + SlotTable::kHeader;
   int32_t* b_row0 = b_exp + st;
@@ -189,13 +192,15 @@ __device__ void dispatch_tail(const FwdParams& p, int32_t* dsm, int c, int off, 
   int32_t* s_exp = b_blk + st;
   int32_t* s_row0 = s_exp + st;
   int32_t* s_rows = s_row0 + st;
-  const int is_small = (tid < E) && (c > 0) && (c <= p.small_rows);
-  const int is_big = (tid < E) && (c > p.small_rows);
+  const int n_sub = (tid < E && c > 0) ? (p.small_only ? (c + p.small_rows - 1) / p.small_rows
+                                                       : (c <= p.small_rows ? 1 : 0))
+                                       : 0;
+  const int is_big = (tid < E) && !p.small_only && (c > p.small_rows);
   const int nblk = is_big ? (c + kTokenBlock - 1) / kTokenBlock : 0;
   // one scan of the three counters packed in 21-bit fields (each total < 2^21)
   unsigned long long packed_total = 0;
   const unsigned long long packed = block_exclusive_scan<unsigned long long>(
-      static_cast<unsigned long long>(is_small) | (static_cast<unsigned long long>(is_big) << 21) |
+      static_cast<unsigned long long>(n_sub) | (static_cast<unsigned long long>(is_big) << 21) |
           (static_cast<unsigned long long>(nblk) << 42),
       &packed_total, s_warp64);
   constexpr unsigned long long kField = (1ull << 21) - 1;
@@ -205,10 +210,10 @@ __device__ void dispatch_tail(const FwdParams& p, int32_t* dsm, int c, int off, 
   int n_small = static_cast<int>(packed_total & kField);
   int n_big = static_cast<int>((packed_total >> 21) & kField);
   int big_blk = static_cast<int>(packed_total >> 42);
-  if (is_small) {
-    s_exp[si] = tid;
-    s_row0[si] = off;
-    s_rows[si] = c;
+  for (int j = 0; j < n_sub; ++j) {
+    s_exp[si + j] = tid;
+    s_row0[si + j] = off + j * p.small_rows;
+    s_rows[si + j] = min(p.small_rows, c - j * p.small_rows);
   }
   if (is_big) {
     b_exp[bi] = tid;

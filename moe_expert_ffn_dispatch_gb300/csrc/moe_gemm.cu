@@ -16,7 +16,9 @@
 //
 // This file holds the small-expert kernel; tc_gemm.cu the big-expert one.
 // Both walk the slot table that dispatch built:
-//   small experts: <= kSmallRows rows (decode).  The weights are
+//   small experts: <= kSmallRows rows (decode; in a batch of at most
+//     kSmallRows tokens every expert, one that repeated ids give more rows
+//     taking several slots of at most kSmallRows rows).  The weights are
 //     read once from HBM and used for M <= 8 multiply-adds each, so the work
 //     is a batch of matrix-vector products: dp4a on exactly M rows, fed by
 //     2 KiB-per-row bulk copies (one producer warp, a 3-stage mbarrier

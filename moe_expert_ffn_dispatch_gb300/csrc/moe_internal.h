@@ -66,17 +66,24 @@ constexpr int kMaxCtas = 1023;  // persistent grid size limit (one CTA per SM)
 // with at most kSmallRows rows ("small", decode-like) go to the weight-
 // streaming dp4a kernel, the others ("big") to the tensor-core kernel in
 // token blocks of kTokenBlock rows.  The shared expert is one more slot in
-// whichever list its row count selects (expert id -1).  Stored as int32
-// words at layout.slots:
+// whichever list its row count selects (expert id -1).  In a batch of at
+// most kSmallRows tokens every expert is small: one whose repeated ids give
+// it more rows takes several small slots of at most kSmallRows rows (see
+// FwdParams::small_only).  Stored as int32 words at layout.slots:
 //   header: [0] n_big  [1] token blocks over big slots  [2] R  [3] S
 //           [4] n_small  [5..7] reserved
-//   then seven arrays of stride (E + 2):
+//   then seven arrays of stride (E + 2 + kSplitSlots):
 //     big:   expert id, first row, row count, exclusive prefix of blocks
 //     small: expert id, first row, row count
+constexpr int kMaxTopk = 16;
+// Extra small slots a batch of at most kSmallRows tokens can need: an expert
+// with c rows takes ceil(c / kSmallRows) slots, one more than its share of
+// the at most kSmallRows * kMaxTopk routed rows, kSmallRows rows a slot.
+constexpr int kSplitSlots = kMaxTopk;
 struct SlotTable {
   static constexpr int kHeader = 8;
   static constexpr int kNumBig = 0, kBigBlocks = 1, kRows = 2, kSharedRows = 3, kNumSmall = 4;
-  static __host__ __device__ int stride(int E) { return E + 2; }
+  static __host__ __device__ int stride(int E) { return E + 2 + kSplitSlots; }
   static __host__ __device__ int words(int E) { return kHeader + 7 * stride(E); }
 };
 
@@ -93,6 +100,9 @@ struct FwdParams {
   int32_t disp_chunks;    // dispatch chunks of kDispChunk pairs; <= 1: one CTA dispatches alone
   int32_t with_tickets;   // dispatch resets the GEMM epilogue counters (forward path)
   int32_t small_rows;     // row count up to which an expert takes the dp4a path (0: never)
+  int32_t small_only;     // bs <= small_rows: every expert takes the dp4a path (an expert with
+                          // more rows, from repeated ids, in slots of at most small_rows rows), so
+                          // no big block exists and the tensor-core launches are skipped
   int32_t num_ctas;       // grid of the GEMM launches (<= kMaxCtas)
   int32_t act_fp16;       // x, y2 and the outputs are fp16 (else bf16)
   int32_t scale_dtype;    // routed weight scales: 0 fp32, 1 bf16, 2 fp16

@@ -639,8 +639,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
 // prefix of their row counts) staged in shared memory once per CTA, so that
 // kernels working row by row find the slot of a row in a few shared-memory
 // probes instead of a chain of dependent global loads.  Layout: 5 arrays of
-// stride E + 2 ints (at most E + 1 slots), i.e. big_slots_smem_bytes(E).
-__host__ __device__ constexpr size_t big_slots_smem_bytes(int E) { return 5u * (E + 2) * sizeof(int32_t); }
+// the slot table's stride (at most E + 1 big slots), i.e. big_slots_smem_bytes(E).
+__host__ __device__ inline size_t big_slots_smem_bytes(int E) { return 5u * SlotTable::stride(E) * sizeof(int32_t); }
 
 struct BigSlots {
   const int32_t* pre;   // first block of each slot (n + 1 entries)

@@ -172,7 +172,9 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None):
         e_of_row = torch.zeros(R, dtype=torch.long)
         off = 0
         for e, c in enumerate(counts):
-            big_row[off:off + c] = (not small_ok) or c > SMALL_ROWS
+            # a batch of at most SMALL_ROWS tokens runs every expert on the dp4a
+            # path (an expert with more rows, from repeated ids, in several slots)
+            big_row[off:off + c] = (not small_ok) or (c > SMALL_ROWS and bs > SMALL_ROWS)
             e_of_row[off:off + c] = e
             off += c
         t_of_row = ref["tk_of_row"].long() // K

@@ -48,6 +48,41 @@ def test_all_tokens_one_expert_and_empty_experts():
     assert ref["expert_token_nums"].tolist() == [0, 0, 0, 0, 150, 0]
 
 
+def _repeated_ids_small_batch(smooth_per_expert):
+    """bs 8, 4 experts, top-4 with repeated ids: 9, 9, 9 and 5 rows, so three
+    experts exceed the 8-row dp4a limit and the batch needs 7 routed slots
+    plus the shared one (more than E + 2)."""
+    wl = synth.custom("repeated_ids_bs8" + ("_expert_smooth" if smooth_per_expert else ""), bs=8, hidden=256,
+                      num_experts=4, topk=4, inter=128, has_shared=True, smooth=smooth_per_expert,
+                      smooth_per_expert=smooth_per_expert, seed=34)
+    inp = synth.make_inputs(wl)
+    flat = torch.tensor([0] * 9 + [1] * 9 + [2] * 9 + [3] * 5, dtype=torch.int32)
+    perm = synth.permutation(34, 1, flat.numel())
+    inp.expert_ids = flat[perm].view(8, 4).contiguous()
+    return wl, inp
+
+
+@pytest.mark.parametrize("smooth_per_expert", [False, True], ids=["token_quant", "expert_smooth"])
+def test_repeated_ids_in_a_small_batch_take_split_dp4a_slots(smooth_per_expert):
+    """A batch of at most 8 tokens runs every expert on the dp4a path: an
+    expert that repeated ids give more than 8 rows takes several slots of at
+    most 8 rows, and none of the tensor-core launches (nor the separate
+    combine) runs; the expand kernel runs only to quantise per routed row."""
+    wl, inp = _repeated_ids_small_batch(smooth_per_expert)
+    blk = make_block(wl, DEV)
+    blk.set_timing(True)
+    blk.get_timing()
+    blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True, blk=blk)
+    launches = {k: n for k, (_, n) in blk.get_timing().items()}
+    blk.set_timing(False)
+    assert ref["expert_token_nums"].tolist() == [9, 9, 9, 5]
+    for k in ("gemm1_big", "requant_big", "gemm2_big", "combine"):
+        assert launches[k] == 0, launches
+    assert (launches["expand"] > 0) == smooth_per_expert, launches
+    assert launches["gemm1_small"] == 2, launches  # the staged forward and the full one
+    check_raw_accumulators(blk, inp, ref, di, dw, DEV)
+
+
 def test_skipped_ids():
     wl = synth.custom("skips", bs=33, hidden=256, num_experts=8, topk=3, inter=128, has_shared=True,
                       masked_fraction=0.1, seed=32)
