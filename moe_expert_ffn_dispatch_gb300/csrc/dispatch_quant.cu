@@ -143,7 +143,7 @@ __device__ void rank_range(const FwdParams& p, int32_t* running, int32_t* wcnt, 
 // expert_token_nums; the active-token list and shared rows; the slot tables;
 // the status words; the small-phase item ranges and the per-forward ticket
 // reset.  Thread tid < E holds its expert's count c and first row off; R is
-// the number of routed rows.  dsm: at least E + 2 ints of scratch.
+// the number of routed rows.  dsm: at least SlotTable::stride(E) ints of scratch.
 __device__ void dispatch_tail(const FwdParams& p, int32_t* dsm, int c, int off, int R, int skipped) {
   __shared__ int s_warp[32];
   __shared__ unsigned long long s_warp64[32];

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import synth
-from gpu_util import run_and_check, check_raw_accumulators, make_block, device_inputs, device_weights
+from gpu_util import run_and_check, check_raw_accumulators, make_block, device_inputs, device_weights, region
 
 pytestmark = pytest.mark.gpu
 
@@ -80,6 +80,17 @@ def test_repeated_ids_in_a_small_batch_take_split_dp4a_slots(smooth_per_expert):
         assert launches[k] == 0, launches
     assert (launches["expand"] > 0) == smooth_per_expert, launches
     assert launches["gemm1_small"] == 2, launches  # the staged forward and the full one
+    # slot table (bit-exact): header, then seven arrays of stride E + 2 + 16;
+    # experts in ascending id, each in slots of at most 8 rows, then the
+    # shared expert (id -1) on its 8 active tokens after the 32 routed rows
+    E, st = wl.num_experts, wl.num_experts + 2 + 16
+    tab = region(blk, "slots", torch.int32, (8 + 7 * st,)).tolist()
+    assert tab[0] == 0 and tab[1] == 0, tab[:8]              # no big slot, no big block
+    assert tab[2] == 32 and tab[3] == 8 and tab[4] == 8, tab[:8]  # R, S, small slots
+    small = tab[8 + 4 * st:]
+    assert small[:8] == [0, 0, 1, 1, 2, 2, 3, -1]
+    assert small[st:st + 8] == [0, 8, 9, 17, 18, 26, 27, 32]
+    assert small[2 * st:2 * st + 8] == [8, 1, 8, 1, 8, 1, 5, 8]
     check_raw_accumulators(blk, inp, ref, di, dw, DEV)
 
 
