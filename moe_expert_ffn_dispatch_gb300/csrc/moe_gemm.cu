@@ -294,55 +294,64 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
       }
       return true;
     };
+    // Streamed GEMM2: a new run's weight copies do not depend on the requant
+    // of its rows, so they are issued before the wait on the slot's ticket;
+    // the wait, the row info and the x2 rows follow (`deferred`).  Otherwise
+    // the next run's info is loaded one item ahead, behind this item's copies.
+    const bool deferred = !G1 && streamed;
     int nx_tok = 0;
     float nx_scale = 0.0f;
     SmallItem nx{};
     int ps = slot_first, pj = jt_first;  // position of nx
     if (it_begin < it_end) {
       nx = item_of(ps, pj);
-      if (!load_info(nx, nx_tok, nx_scale)) return;
+      if (!deferred && !load_info(nx, nx_tok, nx_scale)) return;
     }
     int &stage_it = ss.stage_it, &item_no = ss.item_no, &run_no = ss.run_no;
     int run_slot = -1;
+    // token rows of a new run (whole K), once the consumers are done with the
+    // previous run's rows; tok_full's release also publishes the run's first
+    // info entry when it was written after the item's weight copies
+    auto load_run_rows = [&](const SmallItem& x, int tok) -> bool {
+      if (run_no > 0) {
+        if (!mbar_wait_bounded(tok_empty, (run_no - 1) & 1, abort_flag, status, site + 3, false)) return false;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(tok_full, static_cast<uint32_t>(x.m * K));
+      __syncwarp();
+      // x2 written by another CTA's generic stores, read here by a bulk copy
+      if (!G1 && streamed) fence_proxy_async_global();
+      if (lane < x.m) {
+        const int8_t* trow =
+            !G1 ? x2 + static_cast<size_t>(x.row0 + lane) * p.I
+            : x.e < 0 ? xsq + static_cast<size_t>(tok) * p.h
+                      : xq + static_cast<size_t>(p.xq_per_row ? x.row0 + lane : tok) * p.h;
+        bulk_g2s(smem + OFF_T + lane * K, trow, static_cast<uint32_t>(K), tok_full, pol_t);
+      }
+      run_slot = x.slot;
+      ++run_no;
+      return true;
+    };
     for (long it = it_begin; it < it_end; ++it, ++item_no) {
       const SmallItem cur = nx;
-      const int cur_tok = nx_tok;
-      const float cur_scale = nx_scale;
+      int cur_tok = nx_tok;
+      float cur_scale = nx_scale;
       const int8_t* wbase = G1 ? (cur.e >= 0 ? p.w1 + static_cast<size_t>(cur.e) * NW * K : p.sw1)
                                : (cur.e >= 0 ? p.w2 + static_cast<size_t>(cur.e) * NW * K : p.sw2);
       int n;
       if (G1) n = (lane < BN / 2) ? cur.jt * (BN / 2) + lane : p.I + cur.jt * (BN / 2) + (lane - BN / 2);
       else n = cur.jt * BN + lane;
       const int8_t* wrow = wbase + static_cast<size_t>(n) * K;
-      if (cur.slot != run_slot) {
-        // a new run of items on one expert: load its token rows (whole K) once,
-        // after the consumers are done with the previous run's rows
-        if (run_no > 0) {
-          if (!mbar_wait_bounded(tok_empty, (run_no - 1) & 1, abort_flag, status, site + 3, false)) return;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(tok_full, static_cast<uint32_t>(cur.m * K));
-        __syncwarp();
-        // x2 written by another CTA's generic stores, read here by a bulk copy
-        if (!G1 && streamed) fence_proxy_async_global();
-        if (lane < cur.m) {
-          const int8_t* trow =
-              !G1 ? x2 + static_cast<size_t>(cur.row0 + lane) * p.I
-              : cur.e < 0 ? xsq + static_cast<size_t>(cur_tok) * p.h
-                          : xq + static_cast<size_t>(p.xq_per_row ? cur.row0 + lane : cur_tok) * p.h;
-          bulk_g2s(smem + OFF_T + lane * K, trow, static_cast<uint32_t>(K), tok_full, pol_t);
-        }
-        run_slot = cur.slot;
-        ++run_no;
-      }
+      const bool new_run = cur.slot != run_slot;
+      if (new_run && !deferred && !load_run_rows(cur, cur_tok)) return;
+      const int is = item_no % kInfoSlots;
       for (int kc = 0; kc < n_kc; ++kc, ++stage_it) {
         const int s = stage_it % STAGES;
         const int round = stage_it / STAGES;
         if (round > 0) {
           if (!mbar_wait_bounded(&empty[s], (round - 1) & 1, abort_flag, status, site + 1, false)) return;
         }
-        if (kc == 0 && lane < cur.m) {
+        if (kc == 0 && lane < cur.m && !(deferred && new_run)) {
           // published to the consumers by the release of the arrive below
-          const int is = item_no % kInfoSlots;
           info_scale[is * MT + lane] = cur_scale;
           info_row[is * MT + lane] = cur.row0 + lane;
           info_tok[is * MT + lane] = cur_tok;
@@ -354,6 +363,20 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
         __syncwarp();
         bulk_g2s(smem + OFF_W + (s * BN + lane) * KC, wrow + k0, bytes, &full[s], pol_w);
       }
+      if (new_run && deferred) {
+        // the consumers wait for tok_full before they compute this item, and
+        // read its info only after that
+        if (!load_info(cur, cur_tok, cur_scale)) return;
+        if (lane < cur.m) {
+          info_scale[is * MT + lane] = cur_scale;
+          info_row[is * MT + lane] = cur.row0 + lane;
+          info_tok[is * MT + lane] = cur_tok;
+        }
+        __syncwarp();
+        if (!load_run_rows(cur, cur_tok)) return;
+        nx_tok = cur_tok;  // the run's later items share its info
+        nx_scale = cur_scale;
+      }
       // next item's token info: its dependent loads run while this item's copies fly
       if (it + 1 < it_end) {
         if (++pj == J) {
@@ -362,7 +385,7 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
         }
         nx = item_of(ps, pj);
         // the items of one run share the expert's token rows, and so their info
-        if (nx.slot != cur.slot && !load_info(nx, nx_tok, nx_scale)) return;
+        if (!deferred && nx.slot != cur.slot && !load_info(nx, nx_tok, nx_scale)) return;
       }
     }
     return;

@@ -45,3 +45,31 @@ def test_per_forward_summary_percentiles():
     one = bench.per_forward_summary([7.0])
     assert one == {"median": 7.0, "p10": 7.0, "p90": 7.0}
     assert bench.per_forward_summary([])["median"] is None
+
+
+def _fake_smi(tmp_path, body):
+    d = tmp_path / "bin"
+    d.mkdir()
+    f = d / "nvidia-smi"
+    f.write_text("#!/bin/bash\n" + body)
+    f.chmod(0o755)
+    return str(d)
+
+
+def test_clock_sampler_starts_sampling_before_the_timed_region(tmp_path, monkeypatch):
+    # a sampler that takes 0.3 s to start: entering waits for its first line
+    bindir = _fake_smi(tmp_path, "sleep 0.3\nwhile true; do echo '2070, 2070, 500.0, 0x0000000000000004'; "
+                                 "sleep 0.05; done\n")
+    monkeypatch.setenv("PATH", bindir + os.pathsep + os.environ["PATH"])
+    with bench.ClockSampler(0) as c:
+        assert c.lines, "timed region would start before the first clock sample"
+    s = c.summary()
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] >= 1
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
+    monkeypatch.setenv("PATH", str(tmp_path))
+    with bench.ClockSampler(0) as c:
+        pass
+    assert c.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
