@@ -274,7 +274,6 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
     const int8_t* xq = ws_ptr<int8_t>(p, p.L.x_q);
     const int8_t* xsq = p.share_uses_xq ? xq : ws_ptr<int8_t>(p, p.L.xs_q);
     const int8_t* x2 = ws_ptr<int8_t>(p, p.L.x2);
-    // token info is loaded one item ahead so its latency hides behind the copies
     const int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
     // streamed GEMM2: a slot's s2 and x2 are read only after its requant is
     // marked done (ticket = GEMM1 tiles + 1), by any CTA of this launch
@@ -294,24 +293,22 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
       }
       return true;
     };
-    // Streamed GEMM2: a new run's weight copies do not depend on the requant
-    // of its rows, so they are issued before the wait on the slot's ticket;
-    // the wait, the row info and the x2 rows follow (`deferred`).  Otherwise
-    // the next run's info is loaded one item ahead, behind this item's copies.
-    const bool deferred = !G1 && streamed;
-    int nx_tok = 0;
-    float nx_scale = 0.0f;
+    // Each run's weight copies are issued first: they need only the slot
+    // table.  The run's row info (token, scale) and its token rows follow,
+    // for a streamed GEMM2 once the slot's rows are requantised.  The
+    // consumers acquire tok_full before they compute a run's first item and
+    // read its info only after that, so tok_full's release publishes that
+    // item's info entry; the run's later items publish theirs through the
+    // full[s] arrive of their first stage.
+    int run_tok = 0;
+    float run_scale = 0.0f;
     SmallItem nx{};
     int ps = slot_first, pj = jt_first;  // position of nx
-    if (it_begin < it_end) {
-      nx = item_of(ps, pj);
-      if (!deferred && !load_info(nx, nx_tok, nx_scale)) return;
-    }
+    if (it_begin < it_end) nx = item_of(ps, pj);
     int &stage_it = ss.stage_it, &item_no = ss.item_no, &run_no = ss.run_no;
     int run_slot = -1;
     // token rows of a new run (whole K), once the consumers are done with the
-    // previous run's rows; tok_full's release also publishes the run's first
-    // info entry when it was written after the item's weight copies
+    // previous run's rows
     auto load_run_rows = [&](const SmallItem& x, int tok) -> bool {
       if (run_no > 0) {
         if (!mbar_wait_bounded(tok_empty, (run_no - 1) & 1, abort_flag, status, site + 3, false)) return false;
@@ -333,8 +330,6 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
     };
     for (long it = it_begin; it < it_end; ++it, ++item_no) {
       const SmallItem cur = nx;
-      int cur_tok = nx_tok;
-      float cur_scale = nx_scale;
       const int8_t* wbase = G1 ? (cur.e >= 0 ? p.w1 + static_cast<size_t>(cur.e) * NW * K : p.sw1)
                                : (cur.e >= 0 ? p.w2 + static_cast<size_t>(cur.e) * NW * K : p.sw2);
       int n;
@@ -342,7 +337,6 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
       else n = cur.jt * BN + lane;
       const int8_t* wrow = wbase + static_cast<size_t>(n) * K;
       const bool new_run = cur.slot != run_slot;
-      if (new_run && !deferred && !load_run_rows(cur, cur_tok)) return;
       const int is = item_no % kInfoSlots;
       for (int kc = 0; kc < n_kc; ++kc, ++stage_it) {
         const int s = stage_it % STAGES;
@@ -350,11 +344,11 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
         if (round > 0) {
           if (!mbar_wait_bounded(&empty[s], (round - 1) & 1, abort_flag, status, site + 1, false)) return;
         }
-        if (kc == 0 && lane < cur.m && !(deferred && new_run)) {
+        if (kc == 0 && !new_run && lane < cur.m) {
           // published to the consumers by the release of the arrive below
-          info_scale[is * MT + lane] = cur_scale;
+          info_scale[is * MT + lane] = run_scale;
           info_row[is * MT + lane] = cur.row0 + lane;
-          info_tok[is * MT + lane] = cur_tok;
+          info_tok[is * MT + lane] = run_tok;
         }
         const int k0 = kc * KC;
         const int bytes = min(KC, K - k0);
@@ -363,29 +357,22 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
         __syncwarp();
         bulk_g2s(smem + OFF_W + (s * BN + lane) * KC, wrow + k0, bytes, &full[s], pol_w);
       }
-      if (new_run && deferred) {
-        // the consumers wait for tok_full before they compute this item, and
-        // read its info only after that
-        if (!load_info(cur, cur_tok, cur_scale)) return;
+      if (new_run) {
+        if (!load_info(cur, run_tok, run_scale)) return;
         if (lane < cur.m) {
-          info_scale[is * MT + lane] = cur_scale;
+          info_scale[is * MT + lane] = run_scale;
           info_row[is * MT + lane] = cur.row0 + lane;
-          info_tok[is * MT + lane] = cur_tok;
+          info_tok[is * MT + lane] = run_tok;
         }
         __syncwarp();
-        if (!load_run_rows(cur, cur_tok)) return;
-        nx_tok = cur_tok;  // the run's later items share its info
-        nx_scale = cur_scale;
+        if (!load_run_rows(cur, run_tok)) return;
       }
-      // next item's token info: its dependent loads run while this item's copies fly
       if (it + 1 < it_end) {
         if (++pj == J) {
           pj = 0;
           ++ps;
         }
         nx = item_of(ps, pj);
-        // the items of one run share the expert's token rows, and so their info
-        if (!deferred && nx.slot != cur.slot && !load_info(nx, nx_tok, nx_scale)) return;
       }
     }
     return;
