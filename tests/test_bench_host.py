@@ -73,3 +73,23 @@ def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
     with bench.ClockSampler(0) as c:
         pass
     assert c.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_algorithmic_bytes_follow_the_kernel_that_runs_each_expert():
+    import synth
+    # bs 8: an expert with 12 rows (repeated ids) still runs in the dp4a kernels
+    small_batch = synth.custom("acct8", bs=8, hidden=256, num_experts=4, topk=4, inter=128, has_shared=False)
+    a = bench.algorithmic_bytes(small_batch, [12, 8, 8, 4], 8)
+    assert a["gemm1_big"] == 0 and a["gemm2_big"] == 0 and a["requant_big"] == 0 and a["combine"] == 0
+    assert a["gemm1_small"] > 0 and a["touched_experts"] == 4 and a["rows"] == 32
+    # bs 16: the same 12-row expert takes the tensor-core kernels and the separate combine
+    batch16 = synth.custom("acct16", bs=16, hidden=256, num_experts=4, topk=2, inter=128, has_shared=False)
+    b = bench.algorithmic_bytes(batch16, [12, 8, 8, 4], 16)
+    h, I = 256, 128
+    assert b["gemm1_big"] == 2 * I * h + 8 * I + 12 * (h + 4 * I)
+    assert b["combine"] > 0
+    # the step total counts each touched expert's weights and scales once, plus
+    # x, ids and scales, output and expert_token_nums, whichever kernels run
+    w = 2 * I * h + h * I + 4 * (2 * I + h)
+    assert a["step"] == 4 * w + 8 * h * 2 + 8 * 4 * 8 + 8 * h * 2 + 4 * 4
+    assert b["step"] == 4 * w + 16 * h * 2 + 16 * 2 * 8 + 16 * h * 2 + 4 * 4
