@@ -152,7 +152,10 @@ typedef struct {
   int32_t error_site;      /* which wait gave up (kernel id * 16 + site)       */
   int32_t dispatched_rows; /* R: routed rows dispatched                        */
   int32_t shared_rows;     /* S: rows run through the shared expert            */
-  int32_t active_slots;    /* experts with at least one row (+1 for shared)    */
+  int32_t active_slots;    /* GEMM slots: experts with at least one row, +1    */
+                           /* for the shared expert (in a batch of at most 8   */
+                           /* tokens an expert with more rows, from repeated   */
+                           /* ids, counts once per slot of at most 8 rows)     */
   int32_t reserved[2];
 } moe_fused_status_t;
 
