@@ -18,6 +18,7 @@
 // q = RNE(xs * m) clamped to +-127, scale = 1 / m.  Every fp32 operation is an
 // explicit round-to-nearest intrinsic so no contraction can change a code.
 #include <cstring>
+#include <mutex>
 
 #include "device_prims.cuh"
 #include "moe_fused.h"
@@ -619,8 +620,11 @@ cudaError_t dispatch_prepare_attributes(int E) {
 // active-token list, slot table, status words) in the file-scope array
 // below, which every GPU that loads this library holds until the process
 // exits.  Host code must not pass the array's name to a kernel: on the host
-// that name is only a stand-in, so its device address is looked up once per
-// device with cudaGetSymbolAddress.
+// that name is only a stand-in, so its device address is looked up with
+// cudaGetSymbolAddress, once per CUDA context (the module, and with it the
+// array's address, is loaded per context: after cudaDeviceReset the next
+// primary context gets a fresh copy, so the cache is keyed on the context's
+// process-unique id, not on the device number).
 namespace moe {
 
 constexpr size_t kNoallocScratchBytes = size_t(2) << 20;  // 2 MiB
@@ -635,8 +639,76 @@ namespace moe {
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-char* g_noalloc_ptr[kMaxDevices] = {nullptr};
+// Set-up results per CUDA context: the array's device address in that
+// context (and the dispatch kernel's shared-memory attribute, set there).
+// A small table guarded by a mutex: host threads may make their first call
+// at the same time.
+struct NoallocCtx {
+  unsigned long long ctx_id;
+  char* ptr;
+};
+constexpr int kNoallocCtxSlots = 64;
+std::mutex g_noalloc_mu;
+NoallocCtx g_noalloc_ctx[kNoallocCtxSlots];
+int g_noalloc_used = 0;
+int g_noalloc_next = 0;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Process-unique id of the context current on this thread (0 if none).
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  if (!get_current || !get_id) {  // called under g_noalloc_mu
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    get_id = reinterpret_cast<CtxGetIdFn>(f);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return false;
+  if (!ctx) {
+    *id = 0;
+    return true;
+  }
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the static scratch in the current context; the first
+// call in a context looks it up (and sets the dispatch kernel's attribute).
+char* noalloc_scratch() {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) return nullptr;
+  if (id == 0) {
+    // no context current yet: make the current device's primary context
+    // current (cudaSetDevice initialises it), then read its id
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return nullptr;
+    if (!current_context_id(&id) || id == 0) return nullptr;
+  }
+  for (int i = 0; i < g_noalloc_used; ++i)
+    if (g_noalloc_ctx[i].ctx_id == id) return g_noalloc_ctx[i].ptr;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_dispatch_scratch) != cudaSuccess || !ptr) return nullptr;
+  if (dispatch_prepare_attributes(kNoallocMaxExperts) != cudaSuccess) return nullptr;
+  int slot;
+  if (g_noalloc_used < kNoallocCtxSlots) {
+    slot = g_noalloc_used++;
+  } else {
+    slot = g_noalloc_next;  // more contexts than slots: replace the oldest entry
+    g_noalloc_next = (g_noalloc_next + 1) % kNoallocCtxSlots;
+  }
+  g_noalloc_ctx[slot] = NoallocCtx{id, static_cast<char*>(ptr)};
+  return static_cast<char*>(ptr);
+}
 
 // Scratch layout inside the static array for (bs, topk, E).
 WsLayout noalloc_layout(int bs, int topk, int E) {
@@ -660,6 +732,8 @@ WsLayout noalloc_layout(int bs, int topk, int E) {
   return L;
 }
 
+bool aligned4(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3u) == 0; }
+
 }  // namespace
 
 // Returns 0, or a negative MOE_ERR_* value (see moe_fused.h).
@@ -668,17 +742,13 @@ int dispatch_noalloc(const int32_t* expert_ids, const uint8_t* mask, int bs, int
   if (bs < 0 || topk < 1 || topk > 16 || E < 1 || E > kNoallocMaxExperts || topk > E) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (static_cast<long long>(bs) * topk > kNoallocMaxPairs) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!expert_token_nums || (bs > 0 && !expert_ids)) return MOE_ERR_INVALID_ARG;
+  // the kernel reads ids and writes counts as int32 words
+  if (!aligned4(expert_token_nums) || (expert_ids && !aligned4(expert_ids)) || (expand_row && !aligned4(expand_row)))
+    return MOE_ERR_ALIGNMENT;
   const WsLayout L = noalloc_layout(bs, topk, E);
   if (L.total > kNoallocScratchBytes) return MOE_ERR_UNSUPPORTED_SHAPE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-  if (!g_noalloc_ptr[dev]) {
-    // once per device, with that device current
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_dispatch_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
-    if (dispatch_prepare_attributes(kNoallocMaxExperts) != cudaSuccess) return MOE_ERR_CUDA;
-    g_noalloc_ptr[dev] = static_cast<char*>(ptr);
-  }
+  char* scratch = noalloc_scratch();
+  if (!scratch) return MOE_ERR_CUDA;
   if (bs == 0) {
     return cudaMemsetAsync(expert_token_nums, 0, sizeof(int32_t) * E, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
@@ -693,7 +763,7 @@ int dispatch_noalloc(const int32_t* expert_ids, const uint8_t* mask, int bs, int
   p.ids = expert_ids;
   p.mask = mask;
   p.token_nums = expert_token_nums;
-  p.ws = g_noalloc_ptr[dev];
+  p.ws = scratch;
   p.L = L;
   dispatch_kernel<<<1, kDispatchThreads, dispatch_smem_bytes(E), s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
