@@ -25,7 +25,8 @@
  *   - Return 0 on success or a negative MOE_ERR_* code.  A call that returns an
  *     error before launching leaves every output untouched.
  *   - Tensors are dense, row-major, with the innermost dimension contiguous.
- *     Every pointer must be 16-byte aligned.
+ *     Every pointer must be 16-byte aligned unless its entry point states
+ *     another rule.
  */
 #ifndef MOE_FUSED_H
 #define MOE_FUSED_H
@@ -44,7 +45,7 @@ extern "C" {
 #define MOE_ERR_CUDA (-4)                 /* a CUDA runtime call failed (launch, attribute, memcpy)  */
 #define MOE_ERR_DEVICE_TIMEOUT (-5)       /* a bounded in-kernel wait gave up (see get_status)        */
 #define MOE_ERR_UNIMPLEMENTED (-6)
-#define MOE_ERR_ALIGNMENT (-7)            /* a pointer is not 16-byte aligned                          */
+#define MOE_ERR_ALIGNMENT (-7)            /* a pointer is not aligned as its entry point requires       */
 
 /* Static shape of one block.  Limits: 1 <= hidden, inter <= 16384 and both
  * multiples of 64; 1 <= num_experts <= 1024; 1 <= topk <= min(num_experts, 16);
@@ -211,14 +212,18 @@ const char* moe_fused_strerror(int code);
  * every GPU that loads the library keeps until the process exits.  Limits:
  * bs * topk <= 65536, num_experts <= 1024, 1 <= topk <= min(16, num_experts);
  * larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before any launch.  It calls
- * no allocating routine.  The first call on each device looks up the array's
- * device address (and sets the kernel's shared-memory attribute) with that
- * device current; make that first call before any stream capture.  Every call
- * on a device shares the one array: calls that may overlap on the GPU (on
- * different streams without ordering) race and must not be issued.  Nothing
- * in the array needs clearing between calls: the kernel initialises all it
- * reads.  Errors: INVALID_ARG (NULL expert_token_nums, or NULL expert_ids with
- * bs > 0), UNSUPPORTED_SHAPE, CUDA. */
+ * no allocating routine.  The first call in each CUDA context (per device,
+ * and again after that device's context is destroyed and recreated, e.g. by
+ * cudaDeviceReset) looks up the array's device address and sets the kernel's
+ * shared-memory attribute with that context current; make that first call
+ * before any stream capture.  The set-up is guarded by a lock, so host
+ * threads may make their first calls concurrently.  Every call on a device
+ * shares the one array: calls that may overlap on the GPU (on different
+ * streams without ordering) race and must not be issued.  Nothing in the
+ * array needs clearing between calls: the kernel initialises all it reads.
+ * Errors: INVALID_ARG (NULL expert_token_nums, or NULL expert_ids with
+ * bs > 0), ALIGNMENT (expert_ids, expert_token_nums or a non-NULL expand_row
+ * not 4-byte aligned), UNSUPPORTED_SHAPE, CUDA. */
 int moe_fused_dispatch_noalloc(const int32_t* expert_ids, const uint8_t* x_active_mask, int32_t bs, int32_t topk,
                                int32_t num_experts, int32_t* expert_token_nums, int32_t* expand_row, void* stream);
 
@@ -269,6 +274,18 @@ int moe_fused_debug_region(moe_fused_handle_t* handle, int region, size_t* offse
  * errors as moe_fused_forward. */
 int moe_fused_debug_forward_until(moe_fused_handle_t* handle, const moe_fused_args_t* args, void* workspace,
                                   size_t workspace_bytes, int last_kernel, void* stream);
+
+/* Range forward: enqueue kernels first_kernel..last_kernel of the forward
+ * (kernel ids as for get_timing) on the state the workspace already holds
+ * from an earlier call with the same args, e.g. GEMM2 and the combine after
+ * a test has planted requantised codes and row scales (regions 11, 12 and
+ * 22) into a workspace left by moe_fused_debug_forward_until(..., 5, ...).
+ * A range that starts after kernel 3 runs the small experts' GEMM2 as a
+ * launch of its own.  The per-token combine counters are reset by kernel 0
+ * only, so GEMM2 and the combine may run once per dispatch.  Same checks
+ * and errors as moe_fused_forward, plus INVALID_ARG for a bad range. */
+int moe_fused_debug_forward_range(moe_fused_handle_t* handle, const moe_fused_args_t* args, void* workspace,
+                                  size_t workspace_bytes, int first_kernel, int last_kernel, void* stream);
 
 /* Run one grouped GEMM with a raw INT32 epilogue on the dispatch state and
  * operands currently in `workspace` (left by a forward with the same args):

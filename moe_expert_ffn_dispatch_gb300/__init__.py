@@ -55,7 +55,8 @@ REGIONS = {"status": 0, "counts": 1, "offsets": 2, "row_of": 3, "tk_of_row": 4, 
 EXPORTS = ["moe_fused_create", "moe_fused_workspace_size", "moe_fused_forward", "moe_fused_get_status",
            "moe_fused_destroy", "moe_fused_strerror", "moe_fused_set_timing", "moe_fused_get_timing",
            "moe_fused_kernel_name", "moe_fused_dispatch_noalloc", "moe_fused_debug_region",
-           "moe_fused_debug_forward_until", "moe_fused_debug_gemm_acc", "moe_fused_debug_wait_timeout"]
+           "moe_fused_debug_forward_until", "moe_fused_debug_forward_range", "moe_fused_debug_gemm_acc",
+           "moe_fused_debug_wait_timeout"]
 DEBUG_WAIT_SITE = 240  # MOE_DEBUG_WAIT_SITE
 
 P = ctypes.c_void_p
@@ -116,6 +117,8 @@ def lib() -> ctypes.CDLL:
         L.moe_fused_debug_gemm_acc.argtypes = [P, ctypes.POINTER(Args), P, ctypes.c_size_t, ctypes.c_int, P, P]
         L.moe_fused_debug_wait_timeout.argtypes = [P, P, ctypes.c_size_t, ctypes.c_int, P]
         L.moe_fused_debug_forward_until.argtypes = [P, ctypes.POINTER(Args), P, ctypes.c_size_t, ctypes.c_int, P]
+        L.moe_fused_debug_forward_range.argtypes = [P, ctypes.POINTER(Args), P, ctypes.c_size_t, ctypes.c_int,
+                                                    ctypes.c_int, P]
         L.moe_fused_dispatch_noalloc.argtypes = [P, P, I32, I32, I32, P, P, P]
         for name in EXPORTS:
             if name not in ("moe_fused_strerror", "moe_fused_kernel_name"):
@@ -192,6 +195,12 @@ def moe_fused_debug_forward_until(handle: int, args: Args, workspace: int, works
                                   stream: int) -> int:
     return lib().moe_fused_debug_forward_until(handle, ctypes.byref(args), workspace, workspace_bytes, last_kernel,
                                                stream)
+
+
+def moe_fused_debug_forward_range(handle: int, args: Args, workspace: int, workspace_bytes: int, first_kernel: int,
+                                  last_kernel: int, stream: int) -> int:
+    return lib().moe_fused_debug_forward_range(handle, ctypes.byref(args), workspace, workspace_bytes, first_kernel,
+                                               last_kernel, stream)
 
 
 def moe_fused_debug_gemm_acc(handle: int, args: Args, workspace: int, workspace_bytes: int, which: int,
@@ -315,18 +324,23 @@ class MoeFused:
     def forward(self, x, expert_ids, expert_scales, w1, w1_scale, w2, w2_scale, share_w1=None,
                 share_w1_scale=None, share_w2=None, share_w2_scale=None, smooth=None, share_smooth=None,
                 mask=None, out=None, share_out=None, token_nums=None, workspace: Optional[torch.Tensor] = None,
-                stream: Optional[torch.cuda.Stream] = None, until: Optional[int] = None):
+                stream: Optional[torch.cuda.Stream] = None, until: Optional[int] = None,
+                start: Optional[int] = None):
         """Enqueue one forward; returns (output, share_output or None, expert_token_nums).
-        `until` (test use) stops after that kernel id (moe_fused_debug_forward_until)."""
+        `until` (test use) stops after that kernel id, `start` (test use) starts
+        at that kernel id on the state the workspace holds
+        (moe_fused_debug_forward_range)."""
         a, keep, outs = self.make_args(x, expert_ids, expert_scales, w1, w1_scale, w2, w2_scale, share_w1,
                                        share_w1_scale, share_w2, share_w2_scale, smooth, share_smooth, mask,
                                        out, share_out, token_nums)
         ws = self.workspace() if workspace is None else workspace
         s = (stream if stream is not None else torch.cuda.current_stream(self.device)).cuda_stream
-        if until is None:
+        if until is None and start is None:
             rc = moe_fused_forward(self.handle, a, ws.data_ptr(), ws.numel(), s)
         else:
-            rc = moe_fused_debug_forward_until(self.handle, a, ws.data_ptr(), ws.numel(), until, s)
+            first = 0 if start is None else start
+            last = len(KERNEL_NAMES) - 1 if until is None else until
+            rc = moe_fused_debug_forward_range(self.handle, a, ws.data_ptr(), ws.numel(), first, last, s)
         if rc:
             raise MoeError(rc, "moe_fused_forward")
         del keep

@@ -339,18 +339,24 @@ int moe_fused_create(const moe_fused_config_t* cfg, moe_fused_handle_t** out_han
 
 int moe_fused_forward(moe_fused_handle_t* hd, const moe_fused_args_t* args, void* workspace, size_t workspace_bytes,
                       void* stream) {
-  return moe_fused_debug_forward_until(hd, args, workspace, workspace_bytes, moe::kNumKernels - 1, stream);
+  return moe_fused_debug_forward_range(hd, args, workspace, workspace_bytes, 0, moe::kNumKernels - 1, stream);
 }
 
 int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t* args, void* workspace,
                                   size_t workspace_bytes, int last_kernel, void* stream) {
+  return moe_fused_debug_forward_range(hd, args, workspace, workspace_bytes, 0, last_kernel, stream);
+}
+
+int moe_fused_debug_forward_range(moe_fused_handle_t* hd, const moe_fused_args_t* args, void* workspace,
+                                  size_t workspace_bytes, int first_kernel, int last_kernel, void* stream) {
   moe::FwdParams p;
   int rc = build_params(hd, args, workspace, workspace_bytes, &p);
   if (rc) return rc;
-  if (last_kernel < 0 || last_kernel >= moe::kNumKernels) return MOE_ERR_INVALID_ARG;
+  if (first_kernel < 0 || last_kernel >= moe::kNumKernels || first_kernel > last_kernel) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (p.bs == 0) {
+    if (first_kernel > 0) return MOE_OK;  // nothing was dispatched: later stages have no work
     e = cudaMemsetAsync(args->expert_token_nums, 0, sizeof(int32_t) * hd->cfg.num_experts, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(p.ws + p.L.status, 0, 64 * sizeof(int32_t), s);
     return cuda_fail(e);
@@ -360,8 +366,10 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
   const int sms = p.num_ctas;
   const moe::TcMaps& maps = hd->maps;
   // the small experts' GEMM2 streams behind their GEMM1 in one launch when
-  // the forward runs that far (a forward stopped after GEMM1 keeps h intact)
-  const bool streamed = p.small_rows > 0 && last_kernel >= moe::kKGemm2Small;
+  // the range holds both (a range that stops after GEMM1 keeps h intact; one
+  // that starts after it runs the small GEMM2 as a launch of its own)
+  const bool streamed =
+      p.small_rows > 0 && first_kernel <= moe::kKGemm1Small && last_kernel >= moe::kKGemm2Small;
   auto run = [&](int k) -> cudaError_t {
     switch (k) {
       case moe::kKDispatchQuant: return moe::launch_dispatch_quant(p, s);
@@ -378,7 +386,7 @@ int moe_fused_debug_forward_until(moe_fused_handle_t* hd, const moe_fused_args_t
     }
   };
   e = cudaSuccess;
-  for (int k = 0; k <= last_kernel && e == cudaSuccess; ++k) {
+  for (int k = first_kernel; k <= last_kernel && e == cudaSuccess; ++k) {
     if (k == moe::kKDispatchFinish && p.disp_chunks <= 1) continue;  // one-CTA dispatch: nothing to launch
     if (k == moe::kKGemm2Small && streamed) continue;                 // ran inside the GEMM1 launch
     // no big block can exist: the tensor-core GEMMs, their requant and the
@@ -430,7 +438,7 @@ const char* moe_fused_strerror(int code) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case MOE_ERR_UNIMPLEMENTED: return "not implemented";
-    case MOE_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case MOE_ERR_ALIGNMENT: return "pointer not aligned (forward: 16-byte, workspace 256-byte; no-alloc dispatch: 4-byte)";
     default: return "unknown error";
   }
 }

@@ -2,7 +2,9 @@
 
 Every stage is compared (see tests/gpu_util.py for the tolerances): dispatch
 arrays, x_q / x_scale, int32 accumulators of both GEMMs, SwiGLU output,
-requantised codes, bf16 expert rows, output and share_output.  Shapes span
+requantised codes, bf16 expert rows, output and share_output -- the last three
+bit-exact wherever the requantised codes agree, and everywhere once the
+oracle's codes and row scales are planted before GEMM2.  Shapes span
 several tiles with ragged tails: multi-block experts (> 64 rows), a partial
 GEMM2 output tile (hidden % 128 == 64), a K tail (hidden % 256 != 0), one
 GEMM1 tile (inter = 64), empty experts, skipped ids, masks, smooth scales.
@@ -11,7 +13,8 @@ import pytest
 import torch
 
 import synth
-from gpu_util import run_and_check, check_raw_accumulators, make_block, device_inputs, device_weights, region
+from gpu_util import (check_planted_gemm2, check_raw_accumulators, device_inputs, device_weights, make_block,
+                      region, run_and_check)
 
 pytestmark = pytest.mark.gpu
 
@@ -30,6 +33,32 @@ CASES = [
                  routing="balanced", seed=25),
     synth.custom("bs1", bs=1, hidden=256, num_experts=8, topk=4, inter=128, has_shared=True, seed=26),
 ]
+
+
+# The decode shapes' contraction lengths (hidden 4096, inter 2048): the dp4a
+# GEMM1 streams K in two 2048-byte stages per weight row, the tensor-core
+# GEMMs drain four (GEMM1) and two (GEMM2) exact 1024-wide accumulation
+# chunks.  The int32 accumulators of both must be bit-exact there.
+FULL_K_CASES = [
+    # a batch of 8 tokens: every expert on the dp4a path
+    synth.custom("dp4a_fullk_shared_mask_smooth", bs=8, hidden=4096, num_experts=4, topk=2, inter=2048,
+                 has_shared=True, masked_fraction=0.25, smooth=True, share_smooth=True, seed=71),
+    synth.custom("dp4a_fullk_plain", bs=8, hidden=4096, num_experts=4, topk=2, inter=2048, has_shared=False,
+                 seed=72),
+    # 40 tokens, Zipf over 8 experts: hot experts on the tensor cores, cold ones on dp4a
+    synth.custom("mixed_fullk_zipf", bs=40, hidden=4096, num_experts=8, topk=2, inter=2048, has_shared=True,
+                 routing="zipf", masked_fraction=0.1, smooth=True, seed=73),
+]
+
+
+@pytest.mark.parametrize("wl", FULL_K_CASES, ids=lambda w: w.name)
+def test_full_k_staged_parity(wl):
+    inp = synth.make_inputs(wl)
+    blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True)
+    counts = ref["expert_token_nums"].tolist()
+    if wl.bs > 8:
+        assert any(c > 8 for c in counts) and any(0 < c <= 8 for c in counts), counts
+    check_raw_accumulators(blk, inp, ref, di, dw, DEV)
 
 
 @pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
@@ -72,9 +101,10 @@ def test_repeated_ids_in_a_small_batch_take_split_dp4a_slots(smooth_per_expert):
     blk = make_block(wl, DEV)
     blk.set_timing(True)
     blk.get_timing()
-    blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True, blk=blk)
+    blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True, blk=blk, planted=False)
     launches = {k: n for k, (_, n) in blk.get_timing().items()}
     blk.set_timing(False)
+    check_planted_gemm2(blk, inp, ref, di, dw)
     assert ref["expert_token_nums"].tolist() == [9, 9, 9, 5]
     for k in ("gemm1_big", "requant_big", "gemm2_big", "combine"):
         assert launches[k] == 0, launches
