@@ -1,10 +1,11 @@
 """Benchmark of the fused MoE expert block on GB300.
 
 One step = one forward of the whole block (dispatch, quant, GEMM1 + SwiGLU,
-requant, GEMM2, combine, shared expert) on one batch of the decode workload
-(bs 8 = 4 requests x 2 rows, h 4096, 256 experts, top-8, I 2048, shared
-expert), with weights and inputs already resident in HBM.  Prints one JSON
-line (rank 0).
+requant, GEMM2, combine, shared expert) on one batch, with weights and inputs
+already resident in HBM.  The default batch is the largest single-GPU
+workload, prefill: bs 4096 tokens, h 4096, 256 experts, top-8 with balanced
+routing (128 rows per expert), I 2048, shared expert.  `--workload` selects
+the others (tiny, decode8, decode64, mid512).  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -507,19 +508,39 @@ def _oracle_setup(wl):
 
 
 def cpu_baseline(wl, budget_s=15.0):
-    """The oracle as it stands, on the host cores, on a bounded sample: whole
-    forwards of the workload repeated until about `budget_s` of CPU time."""
+    """The oracle as it stands, on the host cores, on a bounded sample of about
+    `budget_s` seconds: whole forwards of the workload for batches of at most
+    512 tokens; for larger batches (prefill) forwards restricted to
+    consecutive 32-token samples in turn (the oracle's token_sample: dispatch
+    and quant of every token, the GEMMs and combine of the sampled tokens),
+    counting the active sampled tokens."""
     oracle, inp, cache = _oracle_setup(wl)
     threads = os.cpu_count() or 1
-    n, t0 = 0, time.perf_counter()
+    bs = wl.bs
+    chunk = bs if bs <= 512 else 32
+    mask = torch.ones(bs, dtype=torch.bool) if inp.mask is None else inp.mask.bool()
+    n, n_tok, t0 = 0, 0, time.perf_counter()
     while True:
-        oracle.forward(inp, threads=threads, expert_weights=lambda e: cache[e])
+        if chunk == bs:
+            oracle.forward(inp, threads=threads, expert_weights=lambda e: cache[e])
+            n_tok += bs
+        else:
+            samp = torch.zeros(bs, dtype=torch.bool)
+            lo = (n * chunk) % bs
+            samp[lo:lo + chunk] = True
+            oracle.forward(inp, threads=threads, token_sample=samp, expert_weights=lambda e: cache[e])
+            n_tok += int((samp & mask).sum())
         n += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": wl.bs * n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": "%d full forwards of %s (bs %d), weights pre-drawn on the host" % (n, wl.name, wl.bs)}
+    if chunk == bs:
+        sample = "%d full forwards of %s (bs %d), weights pre-drawn on the host" % (n, wl.name, bs)
+    else:
+        sample = ("%d forwards of %s (bs %d) restricted to %d-token samples (%d tokens: dispatch and quant of "
+                  "every token, GEMMs and combine of the sampled tokens' %d routed rows and shared row), "
+                  "weights pre-drawn on the host" % (n, wl.name, bs, chunk, n_tok, wl.topk))
+    return {"value": n_tok / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
 
 
 def run_reference(args, wl, ws, rank):
@@ -555,12 +576,28 @@ def run_reference(args, wl, ws, rank):
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_peaks():
+    """Build and run the peak-rate probe (csrc/peak_probe.cu): exact-integer
+    contraction rates of the two GEMM engines (dp4a, tcgen05 kind::f16 with A
+    in shared or tensor memory), the legacy mma.sync s8 rate, a read-only HBM
+    stream, and the K = 1024 exactness check of fp32 accumulation.  Prints
+    the probe's JSON line."""
+    from moe_expert_ffn_dispatch_gb300 import _build
+    exe = _build.build_peak_probe()
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=600)
+    line = out.stdout.strip().splitlines()[-1] if out.stdout.strip() else "{}"
+    print(line, flush=True)
+    return out.returncode
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="decode8", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    # default: the largest single-GPU configuration (prefill, bs 4096); the
+    # others are selectable and are also parity-test cases
+    ap.add_argument("--workload", default="prefill", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -574,7 +611,11 @@ def main():
     ap.add_argument("--bs", type=int, default=0,
                     help="override the workload's batch size (with --experts: the same rows per expert "
                          "on fewer weights, for profiler captures)")
+    ap.add_argument("--peaks", action="store_true",
+                    help="build and run the peak-rate probe of this GPU instead of the benchmark")
     args = ap.parse_args()
+    if args.peaks:
+        sys.exit(run_peaks())
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_env()
     wl = synth.WORKLOADS[args.workload]

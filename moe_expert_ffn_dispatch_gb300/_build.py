@@ -71,5 +71,19 @@ def build(verbose: bool = False, extra_flags=None) -> str:
     return SO
 
 
+def build_peak_probe(verbose: bool = False) -> str:
+    """The standalone peak-rate probe (csrc/peak_probe.cu), used by
+    `bench.py --peaks`; not part of the library."""
+    os.makedirs(BUILD, exist_ok=True)
+    src = os.path.join(CSRC, "peak_probe.cu")
+    exe = os.path.join(BUILD, "peak_probe")
+    if _stale(exe, [src] + [os.path.join(CSRC, h) for h in HEADERS]):
+        cmd = [nvcc()] + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC, src, "-o", exe]
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        subprocess.check_call(cmd)
+    return exe
+
+
 if __name__ == "__main__":
     print(build(verbose="-v" in sys.argv))
