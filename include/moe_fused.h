@@ -253,15 +253,17 @@ const char* moe_fused_kernel_name(int kernel_id);
  *   0 status  1 counts [E]  2 offsets [E+1]  3 row_of [bs*topk]
  *   4 tk_of_row [bs*topk]  5 active tokens [bs]  6 x_q [bs_max,h] int8
  *   7 x_scale [bs_max] f32  8 xs_q [bs_max,h] int8  9 xs_scale [bs_max]
- *   10 h [rows,2*inter] f32 (SwiGLU output in the first inter floats of a row
- *      of the weight-streaming path; dequantised gate | up of the tensor-core
- *      path)  11 x2 [rows,inter] int8  12 s2 [rows] f32
+ *   10 h [rows,2*inter] f32 (the SwiGLU output of each GEMM1 row in its
+ *      first inter floats, on both GEMM engines)  11 x2 [rows,inter] int8
+ *      (codes of weight-streaming rows)  12 s2 [rows] f32
  *   13 y2 [bs_max*topk,h] in x's dtype  14 slot table
  *   15 row_token [rows] int32  16 shared_row [bs_max] int32
  *   17 row-block counters  18 token counters [bs_max]  19 token totals [bs_max]
  *   20 small-expert item ranges  21 x1h [rows,h] f16  22 x2h [rows,inter] f16
  *   23 multi-CTA dispatch counts [chunks][E] then skipped ids [chunks]
  *      (empty when bs_max*topk <= 8192: one CTA dispatches alone)
+ *   24 amax2 [rows] f32: max |h| of each row of a tensor-core block (the
+ *      GEMM1 epilogue's atomic maximum, read by the requant kernel)
  * `rows` = bs*topk + bs: routed row r at index r (r < R), the shared expert's
  * i-th active token at index bs*topk + i.  Writes *offset and *bytes. */
 int moe_fused_debug_region(moe_fused_handle_t* handle, int region, size_t* offset, size_t* bytes);

@@ -84,9 +84,8 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
   take(L.x_scale, xq_rows * 4, moe::kRegXScale);
   take(L.xs_q, c.has_shared ? bs * h : 0, moe::kRegXsq);
   take(L.xs_scale, c.has_shared ? bs * 4 : 0, moe::kRegXsScale);
-  // h rows are 2I floats wide: the tensor-core GEMM1 stores the dequantised
-  // gate and up halves there for the requant kernel, the dp4a GEMM1 stores h
-  // in the first I
+  // h rows are 2I floats wide (both GEMM1 engines store the SwiGLU output in
+  // the first I)
   // y2 has its own region: the small experts' GEMM2 runs in the same launch
   // as their GEMM1, while other CTAs may still write and read h
   const size_t hbytes = rows * 2 * I * 4, ybytes = routed * h * 2;
@@ -105,6 +104,7 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
   take(L.x2h, rows * I * 2, moe::kRegX2h);
   const size_t chunks = routed > 4 * moe::kDispChunk ? (routed + moe::kDispChunk - 1) / moe::kDispChunk : 1;
   take(L.dcnt, chunks > 1 ? (chunks * E + chunks) * 4 : 0, moe::kRegDcnt);
+  take(L.amax2, rows * 4, moe::kRegAmax2);
   L.total = off;
   return L;
 }
@@ -491,7 +491,7 @@ int moe_fused_debug_region(moe_fused_handle_t* hd, int region, size_t* offset, s
   const size_t offs[moe::kNumRegions] = {L.status, L.counts, L.offsets, L.row_of, L.tk_of_row, L.active, L.x_q,
                                          L.x_scale, L.xs_q, L.xs_scale, L.hbuf, L.x2, L.s2, L.y2, L.slots,
                                          L.row_token, L.shared_row, L.blk_ticket, L.tok_ticket, L.tok_expect,
-                                         L.ranges, L.x1h, L.x2h, L.dcnt};
+                                         L.ranges, L.x1h, L.x2h, L.dcnt, L.amax2};
   if (region < 0 || region >= moe::kNumRegions) return MOE_ERR_INVALID_ARG;
   *offset = offs[region];
   *bytes = L.sizes[region];

@@ -21,9 +21,9 @@ constexpr int kErrWaitTimeout = 1;
 
 // ---------------------------------------------------------------- layout
 // Workspace regions (byte offsets, 256-byte aligned).  `rows` = bs_max*topk
-// routed rows + bs_max shared rows.  h (fp32 SwiGLU output) and y2 (bf16
-// GEMM2 output) share one region: h is dead once requant has run, the same
-// reuse the pages' ENABLE_REUSE_MEMORY applies to its swap / SwiGLU space.
+// routed rows + bs_max shared rows.  y2 has a region of its own (it no
+// longer aliases h: the small experts' GEMM2 runs in the same launch as
+// their GEMM1, while other CTAs may still write and read h).
 struct WsLayout {
   size_t status;     // 64 int32 status words
   size_t counts;     // [E] int32
@@ -35,10 +35,10 @@ struct WsLayout {
   size_t x_scale;    // [bs_max] f32
   size_t xs_q;       // [bs_max, h] int8 (shared-expert quant)
   size_t xs_scale;   // [bs_max] f32
-  size_t hbuf;       // [rows, 2I] f32: h in [0, I) (dp4a path) or g | u (tensor-core path); aliased by y2
+  size_t hbuf;       // [rows, 2I] f32: the SwiGLU output h of each GEMM1 row in [0, I)
   size_t x2;         // [rows, I] int8
   size_t s2;         // [rows] f32
-  size_t y2;         // [bs_max*topk, h] bf16 (== hbuf)
+  size_t y2;         // [bs_max*topk, h] bf16 (x's dtype)
   size_t slots;      // slot table (int32), see SlotTable
   size_t row_token;  // [rows] int32: token of each GEMM row (routed and shared)
   size_t shared_row; // [bs_max] int32: shared-expert row of token t, -1 if inactive
@@ -49,6 +49,7 @@ struct WsLayout {
   size_t x1h;        // [rows, h] f16: GEMM1 token operand of the rows in big blocks (codes as f16)
   size_t x2h;        // [rows, I] f16: GEMM2 token operand of the rows in big blocks
   size_t dcnt;       // multi-CTA dispatch: [chunks][E] rows per (chunk, expert), then [chunks] skipped ids
+  size_t amax2;      // [rows] f32 bits: max |h| of each tensor-core row (atomic max from the GEMM1 epilogue)
   size_t total;
   size_t sizes[32];  // bytes per region id (debug_region)
 };
@@ -57,7 +58,7 @@ struct WsLayout {
 enum Region : int {
   kRegStatus = 0, kRegCounts, kRegOffsets, kRegRowOf, kRegTkOfRow, kRegActive, kRegXq, kRegXScale,
   kRegXsq, kRegXsScale, kRegH, kRegX2, kRegS2, kRegY2, kRegSlots, kRegRowToken, kRegSharedRow,
-  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kRegRanges, kRegX1h, kRegX2h, kRegDcnt, kNumRegions
+  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kRegRanges, kRegX1h, kRegX2h, kRegDcnt, kRegAmax2, kNumRegions
 };
 
 constexpr int kMaxCtas = 1023;  // persistent grid size limit (one CTA per SM)

@@ -18,13 +18,16 @@
 // tensor memory), tokens as N (shared memory).  Per 128 of K the int8 weight
 // stage passes through shared memory once (TMA write, converter read) and so
 // does the f16 token stage (TMA write, MMA read).  What bounds the kernel is
-// the loop between the converter warps and the MMA through tensor memory:
-// the converters' ALU work and stores, and the MMA's reads of the weight
-// operand, which at small N (few token rows) cost about as much as at N = 128.  For
+// the stage loop between the producers, the converter warps and the MMA: at
+// full tiles a stage takes about 1050 cycles against 512 cycles of tensor
+// work (an isolated M128 N128 K16 MMA takes 64 cycles, random operands or
+// not), and taking out the token copies, the conversion arithmetic, the
+// tensor-memory stores or half of the MMAs each gains only 1-4 %.  For
 // GEMM1 the 128 rows are 64 gate rows and the 64 matching up rows, laid out
 // so that each 32-lane quadrant of tensor memory holds 16 gate rows in its
 // lanes 0..15 and the 16 matching up rows in lanes 16..31 (every warp
-// store then covers one 64-byte run of gate and one of up values).
+// store then covers one 64-byte run of gate and one of up values, and the
+// gate and up values of one output column meet in one warp for SwiGLU).
 // The requant of big blocks and the combine of forwards with big blocks run
 // as separate parallel kernels (below): done by the CTA that finishes a block
 // last, they would serialise 128-row blocks and 128-token tiles on a few SMs.
@@ -40,14 +43,14 @@
 //               thread, into a 4-deep ring in tensor memory (the MMA's A
 //               operand), which keeps the f16 weights off shared memory;
 //               software-pipelined when the launch's blocks are short
-//   warp 1      one thread issues tcgen05.mma (M128, N = rows rounded to 16,
-//               K16) stage by stage into two tensor-memory accumulators,
-//               alternating per 1024 of K, and commits to the ring and
-//               accumulator barriers
+//   warp 1      one elected lane issues tcgen05.mma (M128, N = rows rounded
+//               to 16, K16) stage by stage into two tensor-memory
+//               accumulators, alternating per 1024 of K; a stage's weight
+//               slot and token stage share one full / empty barrier pair
 //   warps 8..15 drain accumulators (tcgen05.ld) into int32, then the
-//               epilogue (GEMM1: dequantised gate | up values, SwiGLU
-//               being applied by the requant kernel; GEMM2: dequant to the
-//               activation dtype); two warps per tensor-memory lane quadrant
+//               epilogue (GEMM1: dequant, SwiGLU, h and the row maxima of
+//               |h| for the requant kernel; GEMM2: dequant to the activation
+//               dtype); two warps per tensor-memory lane quadrant
 // All rings are mbarrier full/empty pairs (the FIFO of the Mega-MoE
 // analysis §4); every wait is bounded.
 #include <cuda_fp16.h>
@@ -88,7 +91,8 @@ constexpr int F16_TILE = ATOMS * F16_ATOM;           // 32 KB
 constexpr int OFF_B16 = 0;                           // SB x ATOMS x [128][64] f16, swizzled (TMA)
 constexpr int OFF_A8 = OFF_B16 + SB * F16_TILE;      // S8 x [128][128] int8, swizzled (TMA)
 constexpr int OFF_BAR = OFF_A8 + S8 * A8_BYTES;
-constexpr int NBAR = 2 * S8 + 2 * SA + 2 * SB + 4 + 2 * SI;
+constexpr int NBAR = 2 * S8 + 2 * SA + 4 + 2 * SI + 1;
+static_assert(SA == SB, "one stage barrier pair covers a weight slot and a token stage");
 constexpr int OFF_INFO = OFF_BAR + NBAR * 8;         // tok_scale, tok_row, tok_tok [TB]
 constexpr int OFF_ITEM = OFF_INFO + 3 * TB * 4;      // SI decoded items, 8 ints each
 constexpr int OFF_MISC = OFF_ITEM + SI * 8 * 4;      // tmem slot, abort flag
@@ -163,6 +167,32 @@ __device__ __forceinline__ void int8x16_to_f16(uint4 in, uint4& lo, uint4& hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// SwiGLU of one dequantised gate / up pair (FusedDeepMoE analysis §6.1):
+// t = exp(-g), d = 1 + t, h = (g / d) * u, each step rounded once.
+__device__ __forceinline__ float swiglu_1(float g, float u) {
+  const float d = __fadd_rn(1.0f, expf(-g));
+  return __fmul_rn(__fdiv_rn(g, d), u);
+}
+
+// Max over the 16 lanes of each half-warp of 32 values per lane, scattered:
+// on return lane L (of 16) holds in v[0], v[1] the maxima of entries 2L and
+// 2L + 1 (four butterfly steps, each halving the entries a lane keeps; the
+// kept half is chosen by selects, so the array stays in registers).
+__device__ __forceinline__ void halfwarp_max_scatter(float (&v)[32], int lane) {
+#pragma unroll
+  for (int step = 0; step < 4; ++step) {
+    const int o = 8 >> step;       // lane distance 8, 4, 2, 1
+    const int n = 16 >> step;      // entries kept after this step
+    const bool hi = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const float keep = hi ? v[n + i] : v[i];
+      const float give = hi ? v[i] : v[n + i];
+      v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, o));
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kBigThreads, 1)
     moe_gemm_big_kernel(const __grid_constant__ TcMaps maps, FwdParams p, int32_t* raw) {
@@ -171,14 +201,16 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   extern __shared__ __align__(1024) char smem[];
   uint64_t* a8_full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* a8_empty = a8_full + S8;
-  uint64_t* a16_full = a8_empty + S8;
-  uint64_t* a16_empty = a16_full + SA;
-  uint64_t* b_full = a16_empty + SA;
-  uint64_t* b_empty = b_full + SB;
-  uint64_t* acc_full = b_empty + SB;
+  // stage s: its f16 weight slot (tensor memory) and its token stage (shared
+  // memory) are full once the four converter warps and the token copy have
+  // arrived; one MMA commit empties both
+  uint64_t* op_full = a8_empty + S8;
+  uint64_t* op_empty = op_full + SA;
+  uint64_t* acc_full = op_empty + SA;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* it_full = acc_empty + 2;
   uint64_t* it_empty = it_full + SI;
+  uint64_t* drain_bar = it_empty + SI;  // the MMA thread's final commit
   volatile int32_t* items = reinterpret_cast<volatile int32_t*>(smem + OFF_ITEM);
   float* tok_scale = reinterpret_cast<float*>(smem + OFF_INFO);
   int32_t* tok_row = reinterpret_cast<int32_t*>(smem + OFF_INFO) + TB;
@@ -208,12 +240,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       mbar_init(&a8_empty[s], kConvWarps);
     }
     for (int s = 0; s < SA; ++s) {
-      mbar_init(&a16_full[s], kConvWarps);
-      mbar_init(&a16_empty[s], 1);
-    }
-    for (int s = 0; s < SB; ++s) {
-      mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], 1);
+      mbar_init(&op_full[s], kConvWarps + 1);
+      mbar_init(&op_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -223,6 +251,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       mbar_init(&it_full[s], 1);
       mbar_init(&it_empty[s], kItemReaders);
     }
+    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -312,19 +341,19 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       const void* map_n = G1 ? &maps.b1n : &maps.b2n;
       for (int kb = 0; kb < n_kb; ++kb) {
         if (wrapped &&
-            !__all_sync(0xffffffffu, mbar_wait_bounded(&b_empty[s], ph ^ 1u, abort_flag, status, site + 2, false)))
+            !__all_sync(0xffffffffu, mbar_wait_bounded(&op_empty[s], ph ^ 1u, abort_flag, status, site + 2, false)))
           goto done_b;
         if (elect_one()) {
-          mbar_arrive_expect_tx(&b_full[s], bytes);
+          mbar_arrive_expect_tx(&op_full[s], bytes);
           char* dst = smem + OFF_B16 + s * F16_TILE;
 #pragma unroll
           for (int a = 0; a < ATOMS; ++a) {
             const int kx = kb * KB + a * KA;
             if (mblk > 64) {
-              tma_load_2d(dst + a * F16_ATOM, map, kx, r0, &b_full[s]);
+              tma_load_2d(dst + a * F16_ATOM, map, kx, r0, &op_full[s]);
             } else {
               for (int b = 0; b < nbox; ++b)
-                tma_load_2d(dst + a * F16_ATOM + b * kSmallBox * KA * 2, map_n, kx, r0 + b * kSmallBox, &b_full[s]);
+                tma_load_2d(dst + a * F16_ATOM + b * kSmallBox * KA * 2, map_n, kx, r0 + b * kSmallBox, &op_full[s]);
             }
           }
         }
@@ -383,7 +412,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       bool ok = n_stages > 0 && load_codes();
       for (long k = 0; k < n_stages && ok; ++k) {
         if (k >= SA)
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a16_empty[sa], pa ^ 1u, abort_flag, status, site + 4));
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&op_empty[sa], pa ^ 1u, abort_flag, status, site + 4));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -402,7 +431,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         tmem_st_wait();  // also on the way out after a failed wait: no store left in flight
         tc_fence_before();
         __syncwarp();
-        if (ok && lane == 0) mbar_arrive(&a16_full[sa]);
+        if (ok && lane == 0) mbar_arrive(&op_full[sa]);
         if (++sa == SA) { sa = 0; pa ^= 1u; }
       }
     } else {
@@ -414,7 +443,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         for (int kb = 0; kb < n_kb; ++kb) {
           ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a8_full[s8], p8, abort_flag, status, site + 3));
           if (ok && wrapped)
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a16_empty[sa], pa ^ 1u, abort_flag, status, site + 4));
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&op_empty[sa], pa ^ 1u, abort_flag, status, site + 4));
           if (ok) {
             tc_fence_after();
             const char* src = smem + OFF_A8 + s8 * A8_BYTES + row * KB;
@@ -441,7 +470,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(&a8_empty[s8]);
-            mbar_arrive(&a16_full[sa]);
+            mbar_arrive(&op_full[sa]);
           }
           if (!ok) break;
           if (++s8 == S8) { s8 = 0; p8 ^= 1u; }
@@ -452,76 +481,82 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     }
   } else if (aligned && warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
-    // One 128-K stage per iteration: wait for its weight slot (tensor
-    // memory) and token stage (shared memory), then one elected lane issues
-    // its eight K16 MMAs and commits the slot, the stage and, at the end of
-    // a 1024-K chunk, the accumulator.  Issuing stage by stage releases each
-    // weight slot as early as possible, which keeps the converters ahead.
-    // Ring slots and phases are running counters; the token descriptor
-    // advances by addition in its address field (16-byte units: +2 per K16
-    // step, +1024 per 16 KB atom); the weight operand is read from tensor
-    // memory, 8 columns per K16 step.
-    const uint32_t a_tmem0 = tmem + kAccCols;
-    const uint64_t b_desc0 = umma_desc_sw128(smem_u32(smem + OFF_B16));
-    int sa = 0, sb = 0;
-    uint32_t pa = 0, pb = 0;
-    long acc_n = 0;
-    bool ok = true;
-    for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&it_full[si], pi, abort_flag, status, site + 10))) break;
-      const int mblk = items[8 * si + 6];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&it_empty[si]);
-      if (++si == SI) { si = 0; pi ^= 1u; }
-      const uint32_t idesc = umma_idesc_f16(BM, (mblk + 15) & ~15);
-      uint32_t d_tmem = tmem;
-      int kc = 0;  // stage inside the current 1024-K chunk
-      for (int kb = 0; kb < n_kb; ++kb) {
-        if (kc == 0) {
-          const int buf = static_cast<int>(acc_n & 1);
-          d_tmem = tmem + buf * TB;
-          if (acc_n >= 2 &&
-              !__all_sync(0xffffffffu, mbar_wait_bounded(&acc_empty[buf], ((acc_n >> 1) - 1) & 1, abort_flag,
-                                                         status, site + 5))) {
+    // One 128-K stage per iteration: wait for the stage (its weight slot in
+    // tensor memory and its token stage in shared memory, one barrier), then
+    // one elected lane issues its eight K16 MMAs, one commit frees both, and
+    // at the end of a 1024-K chunk another commits the accumulator.  (One
+    // thread running the role alone, or rounds of two or four stages, measured
+    // slower.)  Ring slots and phases are running counters; the token
+    // descriptor advances by addition in its address field (16-byte units: +2
+    // per K16 step, +1024 per 16 KB atom); the weight operand is read from
+    // tensor memory, 8 columns per K16 step.
+    {
+      const uint32_t a_tmem0 = tmem + kAccCols;
+      const uint64_t b_desc0 = umma_desc_sw128(smem_u32(smem + OFF_B16));
+      int sa = 0;
+      uint32_t pa = 0;
+      long acc_n = 0;
+      bool ok = true;
+      for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&it_full[si], pi, abort_flag, status, site + 10))) break;
+        const int mblk = items[8 * si + 6];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&it_empty[si]);
+        if (++si == SI) { si = 0; pi ^= 1u; }
+        const uint32_t idesc = umma_idesc_f16(BM, (mblk + 15) & ~15);
+        uint32_t d_tmem = tmem;
+        int kc = 0;  // stage inside the current 1024-K chunk
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (kc == 0) {
+            const int buf = static_cast<int>(acc_n & 1);
+            d_tmem = tmem + buf * TB;
+            if (acc_n >= 2 &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(&acc_empty[buf], ((acc_n >> 1) - 1) & 1, abort_flag,
+                                                           status, site + 5))) {
+              ok = false;
+              break;
+            }
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&op_full[sa], pa, abort_flag, status, site + 6))) {
             ok = false;
             break;
           }
-        }
-        const bool w = mbar_wait_bounded(&a16_full[sa], pa, abort_flag, status, site + 6) &&
-                       mbar_wait_bounded(&b_full[sb], pb, abort_flag, status, site + 7);
-        if (!__all_sync(0xffffffffu, w)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const bool last = (kc + 1 == CHUNK_KB || kb + 1 == n_kb);
-        if (elect_one()) {
-          constexpr uint64_t kAtom = F16_ATOM >> 4;
-          const uint32_t at = a_tmem0 + sa * kAStageCols;
-          const uint64_t bd = b_desc0 + static_cast<uint64_t>(sb * (F16_TILE >> 4));
-          umma_f16_ts(d_tmem, at, bd, idesc, kc != 0 ? 1u : 0u);
-          umma_f16_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 32, bd + kAtom, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 40, bd + kAtom + 2, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
-          umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
-          umma_commit(&a16_empty[sa]);
-          umma_commit(&b_empty[sb]);
-          if (last) umma_commit(&acc_full[acc_n & 1]);
-        }
-        __syncwarp();
-        if (++sa == SA) { sa = 0; pa ^= 1u; }
-        if (++sb == SB) { sb = 0; pb ^= 1u; }
-        if (last) {
-          ++acc_n;
-          kc = 0;
-        } else {
-          ++kc;
+          tc_fence_after();
+          const bool last = (kc + 1 == CHUNK_KB || kb + 1 == n_kb);
+          if (elect_one()) {
+            constexpr uint64_t kAtom = F16_ATOM >> 4;
+            const uint32_t at = a_tmem0 + sa * kAStageCols;
+            const uint64_t bd = b_desc0 + static_cast<uint64_t>(sa * (F16_TILE >> 4));
+            umma_f16_ts(d_tmem, at, bd, idesc, kc != 0 ? 1u : 0u);
+            umma_f16_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 24, bd + 6, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 32, bd + kAtom, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 40, bd + kAtom + 2, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
+            umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
+            umma_commit(&op_empty[sa]);
+            if (last) umma_commit(&acc_full[acc_n & 1]);
+          }
+          __syncwarp();
+          if (++sa == SA) { sa = 0; pa ^= 1u; }
+          if (last) {
+            ++acc_n;
+            kc = 0;
+          } else {
+            ++kc;
+          }
         }
       }
+      // every MMA the elected lane issued completes before the CTA frees
+      // tensor memory: in a normal run the epilogue already waited for the
+      // last accumulator; after a wait gave up this bounded wait covers the
+      // MMAs still in flight (elect.sync picks the same lane in a converged warp)
+      if (elect_one()) umma_commit(drain_bar);
+      __syncwarp();
+      mbar_wait_bounded(drain_bar, 0, nullptr, status, site + 11);
     }
+    __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
     const int ctid = threadIdx.x - kEpiWarp0 * 32;   // 0..255
@@ -535,6 +570,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     const float* s2 = ws_ptr<float>(p, p.L.s2);
     const int32_t* tk_of_row_g = ws_ptr<int32_t>(p, p.L.tk_of_row);
     float* hbuf = ws_ptr<float>(p, p.L.hbuf);
+    int32_t* amax2 = ws_ptr<int32_t>(p, p.L.amax2);
     uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
     long acc_n = 0;
     for (long it = blockIdx.x; it < total && aligned; it += gridDim.x) {
@@ -595,19 +631,58 @@ __global__ void __launch_bounds__(kBigThreads, 1)
           if (tok < mblk && ng < NW) raw[static_cast<size_t>(tok_row[tok]) * NW + ng] = acc[j];
         }
       } else if (G1) {
-        // dequantised gate (lanes 0..15) or up (lanes 16..31) value of every
-        // token, into the row's gate | up halves; the requant kernel applies
-        // SwiGLU (a long expf / divide chain that would otherwise hold this
-        // epilogue, and with it the accumulators, for most of an item)
+        // Dequant (§6.1: (float(acc) * w_scale) * x_scale) and SwiGLU.  Lane
+        // l < 16 holds the gate row of output column `col` for the 64 tokens
+        // of this half, lane l + 16 the matching up row; each lane takes 32
+        // of the tokens (gate lanes the first 32, up lanes the last 32) and
+        // trades the other 32 values with its partner.  h goes to the row's
+        // first I floats; max |h| over this tile's columns is published per
+        // row by an atomic maximum on the float bits (h >= 0 bits order as
+        // integers), so that the requant needs one pass over h.
         const int ncol = gate ? col : p.I + col;
         const float ws = x.e >= 0 ? wscale_at(p.w1s, static_cast<size_t>(x.e) * NW + ncol, p.scale_dtype)
                                   : p.sw1s[ncol];
+        // token slots of this half that hold rows of the block: gate lanes
+        // need the first min(vt, 32), up lanes the next ones; 8-token chunks
+        // past them are skipped (warp-uniform), so short blocks pay for their
+        // rows only
+        const int vt = mblk - 64 * half;
+        if (vt > 0) {
+          const int n_g = vt < 32 ? vt : 32;
+          float hv[32];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int tok = 64 * half + j;
-          if (tok < mblk)
-            hbuf[static_cast<size_t>(tok_row[tok]) * (2 * p.I) + ncol] =
-                __fmul_rn(__fmul_rn(__int2float_rn(acc[j]), ws), tok_scale[tok]);
+          for (int c = 0; c < 4; ++c) {
+            if (8 * c < n_g) {
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const int j = 8 * c + jj;
+                // this lane's dequantised values of tokens j and 32 + j
+                const float lo = __fmul_rn(__fmul_rn(__int2float_rn(acc[j]), ws), tok_scale[64 * half + j]);
+                const float hi =
+                    __fmul_rn(__fmul_rn(__int2float_rn(acc[32 + j]), ws), tok_scale[64 * half + 32 + j]);
+                // gate lanes send gate(32 + j) and receive up(j); up lanes the reverse
+                const float other = __shfl_xor_sync(0xffffffffu, gate ? hi : lo, 16);
+                hv[j] = gate ? swiglu_1(lo, other) : swiglu_1(other, hi);
+              }
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) hv[8 * c + jj] = 0.0f;
+            }
+          }
+          const int tbase = 64 * half + (gate ? 0 : 32);  // token of hv[0]
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int tok = tbase + j;
+            if (tok < mblk) hbuf[static_cast<size_t>(tok_row[tok]) * (2 * p.I) + col] = hv[j];
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) hv[j] = fabsf(hv[j]);
+          halfwarp_max_scatter(hv, lane & 15);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int tok = tbase + 2 * (lane & 15) + u;
+            if (tok < mblk) atomicMax(amax2 + tok_row[tok], __float_as_int(hv[u]));
+          }
         }
       } else {
         const bool valid_n = col < p.h;
@@ -794,6 +869,13 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
 
   if (total == 0) return;
   const BigSlots tab = stage_big_slots(p, slots, ex_smem);
+  {
+    // clear the row maxima that the tensor-core GEMM1 epilogue raises
+    int32_t* amax2 = ws_ptr<int32_t>(p, p.L.amax2);
+    const int R = slots[SlotTable::kRows], S = slots[SlotTable::kSharedRows];
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < R + S; i += gridDim.x * blockDim.x)
+      amax2[i < R ? i : p.bs * p.topk + (i - R)] = 0;
+  }
   const int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
   const int8_t* xq = ws_ptr<int8_t>(p, p.L.x_q);
   const int8_t* xsq = p.share_uses_xq ? xq : ws_ptr<int8_t>(p, p.L.xs_q);
@@ -831,21 +913,11 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
   }
 }
 
-// SwiGLU and requant of the rows of big blocks (FusedDeepMoE analysis §6.1
-// and §7.2), one warp per row: h = (g / (1 + exp(-g))) * u from the row's
-// dequantised gate | up halves, amax = max(max|h|, 1e-4), s2 = amax * (1/127),
-// q = RNE((h * 127) * (1/amax)); writes the codes as f16 (the tensor-core
-// GEMM2 operand, exact) and s2.  Rows up to I = 2048 keep h in shared
-// memory between the two passes; longer rows recompute it in the second.
-__device__ __forceinline__ float swiglu_1(float g, float u) {
-  const float d = __fadd_rn(1.0f, expf(-g));
-  return __fmul_rn(__fdiv_rn(g, d), u);
-}
-__device__ __forceinline__ float4 swiglu_4(float4 g, float4 u) {
-  return make_float4(swiglu_1(g.x, u.x), swiglu_1(g.y, u.y), swiglu_1(g.z, u.z), swiglu_1(g.w, u.w));
-}
-// the codes of big rows are stored only as f16 (exact): the tensor-core GEMM2
-// reads nothing else
+// Requant of the rows of big blocks (FusedDeepMoE analysis §7.2), one warp
+// per row, one pass: the GEMM1 epilogue left the row's SwiGLU output h in
+// the first I floats of its h row and max |h| in amax2; amax = max(that,
+// 1e-4), s2 = amax * (1/127), q = RNE((h * 127) * (1/amax)) clamped to +-127.
+// Writes the codes as f16 (the tensor-core GEMM2 operand, exact) and s2.
 __device__ __forceinline__ void quant_store4(float4 v, float inv, int c, __half2* h2) {
   const float f[4] = {v.x, v.y, v.z, v.w};
   int8_t q[4];
@@ -854,30 +926,23 @@ __device__ __forceinline__ void quant_store4(float4 v, float inv, int c, __half2
   h2[2 * c] = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
   h2[2 * c + 1] = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
 }
-__device__ __forceinline__ float amax4(float a, float4 v) {
-  return fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-}
 
 constexpr int kRqWarps = 8;          // rows in flight per CTA (one per warp)
-constexpr int kRqMaxI = 2048;        // rows up to this I keep h in shared memory
 
 __global__ void __launch_bounds__(kRqWarps * 32) requant_big_kernel(FwdParams p) {
-  // [kRqWarps][kRqMaxI / 4] float4 when I <= kRqMaxI, then big_slots_smem_bytes(E)
-  extern __shared__ float4 rq_smem[];
+  extern __shared__ int32_t rq_smem[];  // big_slots_smem_bytes(E)
   grid_dependency_wait();
   grid_launch_dependents();
   const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
   const int total = slots[SlotTable::kBigBlocks];
   if (total == 0) return;
   const int I = p.I, n4 = I >> 2;
-  const bool staged = I <= kRqMaxI;
-  const BigSlots tab =
-      stage_big_slots(p, slots, reinterpret_cast<int32_t*>(rq_smem + (staged ? kRqWarps * (kRqMaxI / 4) : 0)));
+  const BigSlots tab = stage_big_slots(p, slots, rq_smem);
   const float* hbuf = ws_ptr<float>(p, p.L.hbuf);
+  const int32_t* amax2 = ws_ptr<int32_t>(p, p.L.amax2);
   __half* x2h = ws_ptr<__half>(p, p.L.x2h);
   float* s2 = ws_ptr<float>(p, p.L.s2);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  float4* hrow = rq_smem + wid * (kRqMaxI / 4);
   const int gw = blockIdx.x * kRqWarps + wid;
   const int nw = gridDim.x * kRqWarps;
   // real rows of the big slots, spread evenly over the warps (row slots of
@@ -886,42 +951,21 @@ __global__ void __launch_bounds__(kRqWarps * 32) requant_big_kernel(FwdParams p)
   for (int g = gw; g < nreal; g += nw) {
     const int sl = big_row_slot(tab, g);
     const int r = tab.row0[sl] + (g - tab.rpre[sl]);
-    const float4* gr = reinterpret_cast<const float4*>(hbuf + static_cast<size_t>(r) * (2 * I));
-    const float4* ur = gr + n4;
-    __half2* h2 = reinterpret_cast<__half2*>(x2h + static_cast<size_t>(r) * I);
-    // pass 1: h = SwiGLU(g, u) (into shared memory when the row fits) and amax;
-    // four g / u pairs of loads in flight per lane before any is used
-    float amax = 0.0f;
-    for (int c0 = lane; c0 < n4; c0 += 4 * 32) {
-      float4 gv[4], uv[4];
-#pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4) {
-        const int c = c0 + 32 * u4;
-        if (c < n4) {
-          gv[u4] = __ldcs(gr + c);
-          uv[u4] = __ldcs(ur + c);
-        }
-      }
-#pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4) {
-        const int c = c0 + 32 * u4;
-        if (c < n4) {
-          const float4 hv = swiglu_4(gv[u4], uv[u4]);
-          amax = amax4(amax, hv);
-          if (staged) hrow[c] = hv;
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    float amax = __int_as_float(amax2[r]);
     if (amax < 1e-4f) amax = 1e-4f;
     const float inv = __fdiv_rn(1.0f, amax);
-    // pass 2: codes (h from shared memory, or recomputed for long rows)
-    for (int c = lane; c < n4; c += 32) {
-      const float4 hv = staged ? hrow[c] : swiglu_4(gr[c], ur[c]);
-      quant_store4(hv, inv, c, h2);
+    const float4* hr = reinterpret_cast<const float4*>(hbuf + static_cast<size_t>(r) * (2 * I));
+    __half2* h2 = reinterpret_cast<__half2*>(x2h + static_cast<size_t>(r) * I);
+    // four loads in flight per lane before any is used
+    for (int c0 = lane; c0 < n4; c0 += 4 * 32) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c0 + 32 * u < n4) v[u] = __ldcs(hr + c0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c0 + 32 * u < n4) quant_store4(v[u], inv, c0 + 32 * u, h2);
     }
-    __syncwarp();  // this warp's h row is reused by its next row
     if (lane == 0) s2[r] = __fmul_rn(amax, 1.0f / 127.0f);
   }
 }
@@ -948,9 +992,8 @@ __global__ void __launch_bounds__(256, 4) combine_kernel(FwdParams p) {
 cudaError_t launch_requant_big(const FwdParams& p, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
-  const size_t smem = (p.I <= kRqMaxI ? static_cast<size_t>(kRqWarps) * kRqMaxI * sizeof(float) : 0) +
-                      big_slots_smem_bytes(p.E);
-  cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 3), dim3(kRqWarps * 32), smem, s, attr);
+  const size_t smem = big_slots_smem_bytes(p.E);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 4), dim3(kRqWarps * 32), smem, s, attr);
   return cudaLaunchKernelEx(&cfg, requant_big_kernel, p);
 }
 
@@ -971,8 +1014,7 @@ cudaError_t moe_gemm_big_prepare_attributes() {
     if (e != cudaSuccess) return e;
   }
   return cudaFuncSetAttribute(reinterpret_cast<const void*>(requant_big_kernel),
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kRqWarps * kRqMaxI * sizeof(float) + big_slots_smem_bytes(1024)));
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(big_slots_smem_bytes(1024)));
 }
 
 cudaError_t launch_expand(const FwdParams& p, cudaStream_t s) {

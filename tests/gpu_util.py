@@ -326,42 +326,24 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None, planted=True):
             assert torch.equal(region(blk, "xs_q", torch.int8, (bs, h))[act], ref["xs_q"][act])
             assert torch.equal(region(blk, "xs_scale", torch.float32, (bs,))[act], ref["xs_scale"][act])
         rows = bs * K + (bs if wl.has_shared else 0)
-        # GEMM1 outputs, rows 2I floats wide.  Rows of experts with at most
-        # SMALL_ROWS rows (dp4a path) hold the SwiGLU output h in [0, I):
-        # fp32 within exp ulps of the oracle.  Rows of the other experts
-        # (tensor-core path) hold the dequantised gate | up values, which must
-        # equal fp32 (float(acc1) * w_scale) * x_scale of the oracle's exact
-        # int32 accumulators bit for bit (SwiGLU is applied by the requant
-        # kernel, whose x2 / s2 are checked below).
+        # GEMM1 outputs, rows 2I floats wide: both engines leave the SwiGLU
+        # output h in the first I floats of a row, fp32 within exp ulps of the
+        # oracle (the dequant before it is exact: GEMM1's int32 accumulators are
+        # checked bit for bit by check_raw_accumulators)
         hb = staged_h.view(torch.float32)[:rows * 2 * I].view(rows, 2 * I)
         small_ok = h <= 4096 and I <= 4096 and not (blk.cfg.flags & m.FLAG_UNFUSED)
         counts = ref["expert_token_nums"].tolist()
         big_row = torch.zeros(R, dtype=torch.bool)
-        e_of_row = torch.zeros(R, dtype=torch.long)
         off = 0
         for e, c in enumerate(counts):
             # a batch of at most SMALL_ROWS tokens runs every expert on the dp4a
             # path (an expert with more rows, from repeated ids, in several slots)
             big_row[off:off + c] = (not small_ok) or (c > SMALL_ROWS and bs > SMALL_ROWS)
-            e_of_row[off:off + c] = e
             off += c
-        t_of_row = ref["tk_of_row"].long() // K
-        if (~big_row).any():
-            assert_rel(hb[:R][~big_row, :I], ref["h"][~big_row], H_REL, "h routed (dp4a rows)")
-        if big_row.any():
-            w1s = inp.w1_scale.to(torch.float32)
-            acc = ref["acc1"][big_row].to(torch.float32)
-            xsc_row = ref["x_scale"][:R][big_row] if per_row else ref["x_scale"][t_of_row[big_row]]
-            want = (acc * w1s[e_of_row[big_row]]) * xsc_row.view(-1, 1)
-            assert torch.equal(hb[:R][big_row], want), "gate | up routed (tensor-core rows)"
+        if R:
+            assert_rel(hb[:R, :I], ref["h"], H_REL, "h routed")
         if S:
-            if small_ok and S <= SMALL_ROWS:
-                assert_rel(hb[bs * K:bs * K + S, :I], ref["share_h"][act], H_REL, "h shared")
-            else:
-                xs_sh = ref["xs_scale"][act]  # the shared expert's own quant (its smooth vector)
-                acc = ref["share_acc1"][act].to(torch.float32)
-                want = (acc * inp.share_w1_scale.to(torch.float32).view(1, -1)) * xs_sh.view(-1, 1)
-                assert torch.equal(hb[bs * K:bs * K + S], want), "gate | up shared (tensor-core rows)"
+            assert_rel(hb[bs * K:bs * K + S, :I], ref["share_h"][act], H_REL, "h shared")
         # requant: dp4a rows keep int8 codes (x2); tensor-core rows keep them
         # only as exact f16 values (x2h, the tensor-core GEMM2 operand)
         x2 = region(blk, "x2", torch.int8, (rows, I)).clone()
