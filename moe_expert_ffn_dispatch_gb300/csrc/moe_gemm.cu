@@ -179,6 +179,21 @@ __device__ __forceinline__ void init_rings(char* smem) {
   }
 }
 
+// The producer's exit: wait (bounded, and not cut short by an abort) until
+// every bulk copy it issued has landed -- the last phase it armed on each
+// weight stage and on the token-row barrier -- so that no copy still writes
+// into this CTA's shared memory once the CTA ends.  Called by the whole
+// producer warp after its last GEMM phase.
+__device__ __forceinline__ void drain_copies(char* smem, const SmallState& ss, int32_t* status, int site) {
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* tok_full = full + 2 * STAGES;
+  for (int s = 0; s < STAGES && s < ss.stage_it; ++s) {
+    const int last_round = (ss.stage_it - 1 - s) / STAGES;
+    mbar_wait_bounded(&full[s], last_round & 1, nullptr, status, site);
+  }
+  if (ss.run_no > 0) mbar_wait_bounded(tok_full, (ss.run_no - 1) & 1, nullptr, status, site);
+}
+
 // this CTA's slots of one GEMM's item range into its shared-memory cache
 // (the caller synchronises the block afterwards)
 template <bool G1>
@@ -502,6 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_small_kernel(FwdParams p
   __syncthreads();
   small_path::SmallState ss;
   small_path::run<MODE>(p, raw, smem, ss, false);
+  if ((threadIdx.x >> 5) == kConsumerWarps)
+    small_path::drain_copies(smem, ss, ws_ptr<int32_t>(p, p.L.status), (G1 ? kKGemm1Small : kKGemm2Small) * 16 + 14);
 }
 
 // GEMM2 streamed behind GEMM1 in one persistent launch (one CTA per SM, all
@@ -521,6 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_small_streamed_kernel(Fw
   small_path::SmallState ss;
   small_path::run<kGemm1SwiGLU>(p, nullptr, smem, ss, false);
   small_path::run<kGemm2Bf16>(p, nullptr, smem, ss, true);
+  if ((threadIdx.x >> 5) == kConsumerWarps)
+    small_path::drain_copies(smem, ss, ws_ptr<int32_t>(p, p.L.status), kKGemm1Small * 16 + 14);
 }
 
 }  // namespace

@@ -45,8 +45,8 @@
 //               software-pipelined when the launch's blocks are short
 //   warp 1      one elected lane issues tcgen05.mma (M128, N = rows rounded
 //               to 16, K16) stage by stage into two tensor-memory
-//               accumulators, alternating per 1024 of K; a stage's weight
-//               slot and token stage share one full / empty barrier pair
+//               accumulators, alternating per 1024 of K, and commits to the
+//               ring and accumulator barriers
 //   warps 8..15 drain accumulators (tcgen05.ld) into int32, then the
 //               epilogue (GEMM1: dequant, SwiGLU, h and the row maxima of
 //               |h| for the requant kernel; GEMM2: dequant to the activation
@@ -91,8 +91,8 @@ constexpr int F16_TILE = ATOMS * F16_ATOM;           // 32 KB
 constexpr int OFF_B16 = 0;                           // SB x ATOMS x [128][64] f16, swizzled (TMA)
 constexpr int OFF_A8 = OFF_B16 + SB * F16_TILE;      // S8 x [128][128] int8, swizzled (TMA)
 constexpr int OFF_BAR = OFF_A8 + S8 * A8_BYTES;
-constexpr int NBAR = 2 * S8 + 2 * SA + 4 + 2 * SI + 1;
-static_assert(SA == SB, "one stage barrier pair covers a weight slot and a token stage");
+constexpr int NBAR = 2 * S8 + 2 * SA + 2 * SB + 4 + 2 * SI + 1;
+static_assert(SA == SB, "a stage's weight slot and token stage share one ring index");
 constexpr int OFF_INFO = OFF_BAR + NBAR * 8;         // tok_scale, tok_row, tok_tok [TB]
 constexpr int OFF_ITEM = OFF_INFO + 3 * TB * 4;      // SI decoded items, 8 ints each
 constexpr int OFF_MISC = OFF_ITEM + SI * 8 * 4;      // tmem slot, abort flag
@@ -167,6 +167,20 @@ __device__ __forceinline__ void int8x16_to_f16(uint4 in, uint4& lo, uint4& hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// A TMA producer's exit: wait (bounded, and not cut short by an abort) until
+// every copy it issued has landed, i.e. the last phase it armed on each slot
+// of its ring has completed, so that no copy still writes into this CTA's
+// shared memory once the CTA ends.  `s` / `ph`: the next slot and its phase
+// parity; slots before `s` were last armed in the current lap, the others
+// (once the ring has wrapped) in the previous one.  Called by the whole warp.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int n, int s, uint32_t ph, bool wrapped,
+                                           int32_t* status, int site) {
+  for (int i = 0; i < n; ++i) {
+    if (i < s) mbar_wait_bounded(&full[i], ph, nullptr, status, site);
+    else if (wrapped) mbar_wait_bounded(&full[i], ph ^ 1u, nullptr, status, site);
+  }
+}
+
 // SwiGLU of one dequantised gate / up pair (FusedDeepMoE analysis §6.1):
 // t = exp(-g), d = 1 + t, h = (g / d) * u, each step rounded once.
 __device__ __forceinline__ float swiglu_1(float g, float u) {
@@ -201,12 +215,11 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   extern __shared__ __align__(1024) char smem[];
   uint64_t* a8_full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* a8_empty = a8_full + S8;
-  // stage s: its f16 weight slot (tensor memory) and its token stage (shared
-  // memory) are full once the four converter warps and the token copy have
-  // arrived; one MMA commit empties both
-  uint64_t* op_full = a8_empty + S8;
-  uint64_t* op_empty = op_full + SA;
-  uint64_t* acc_full = op_empty + SA;
+  uint64_t* a16_full = a8_empty + S8;
+  uint64_t* a16_empty = a16_full + SA;
+  uint64_t* b_full = a16_empty + SA;
+  uint64_t* b_empty = b_full + SB;
+  uint64_t* acc_full = b_empty + SB;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* it_full = acc_empty + 2;
   uint64_t* it_empty = it_full + SI;
@@ -240,8 +253,12 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       mbar_init(&a8_empty[s], kConvWarps);
     }
     for (int s = 0; s < SA; ++s) {
-      mbar_init(&op_full[s], kConvWarps + 1);
-      mbar_init(&op_empty[s], 1);
+      mbar_init(&a16_full[s], kConvWarps);
+      mbar_init(&a16_empty[s], 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -320,7 +337,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         if (++s == S8) { s = 0; ph ^= 1u; wrapped = true; }
       }
     }
-  done_a:;
+  done_a:
+    drain_ring(a8_full, S8, s, ph, wrapped, status, site + 12);
   } else if (aligned && warp == kWarpB) {
     // ---------------------------------------------------- token TMA (f16)
     int s = 0;
@@ -341,19 +359,19 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       const void* map_n = G1 ? &maps.b1n : &maps.b2n;
       for (int kb = 0; kb < n_kb; ++kb) {
         if (wrapped &&
-            !__all_sync(0xffffffffu, mbar_wait_bounded(&op_empty[s], ph ^ 1u, abort_flag, status, site + 2, false)))
+            !__all_sync(0xffffffffu, mbar_wait_bounded(&b_empty[s], ph ^ 1u, abort_flag, status, site + 2, false)))
           goto done_b;
         if (elect_one()) {
-          mbar_arrive_expect_tx(&op_full[s], bytes);
+          mbar_arrive_expect_tx(&b_full[s], bytes);
           char* dst = smem + OFF_B16 + s * F16_TILE;
 #pragma unroll
           for (int a = 0; a < ATOMS; ++a) {
             const int kx = kb * KB + a * KA;
             if (mblk > 64) {
-              tma_load_2d(dst + a * F16_ATOM, map, kx, r0, &op_full[s]);
+              tma_load_2d(dst + a * F16_ATOM, map, kx, r0, &b_full[s]);
             } else {
               for (int b = 0; b < nbox; ++b)
-                tma_load_2d(dst + a * F16_ATOM + b * kSmallBox * KA * 2, map_n, kx, r0 + b * kSmallBox, &op_full[s]);
+                tma_load_2d(dst + a * F16_ATOM + b * kSmallBox * KA * 2, map_n, kx, r0 + b * kSmallBox, &b_full[s]);
             }
           }
         }
@@ -361,7 +379,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         if (++s == SB) { s = 0; ph ^= 1u; wrapped = true; }
       }
     }
-  done_b:;
+  done_b:
+    drain_ring(b_full, SB, s, ph, wrapped, status, site + 13);
   } else if (aligned && warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
     // ------------------------------- int8 -> f16 weight rows, into tensor memory
     // Thread = weight row = tensor-memory lane (warp 4 + q owns lanes 32 q ..).
@@ -412,7 +431,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       bool ok = n_stages > 0 && load_codes();
       for (long k = 0; k < n_stages && ok; ++k) {
         if (k >= SA)
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&op_empty[sa], pa ^ 1u, abort_flag, status, site + 4));
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a16_empty[sa], pa ^ 1u, abort_flag, status, site + 4));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -431,7 +450,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         tmem_st_wait();  // also on the way out after a failed wait: no store left in flight
         tc_fence_before();
         __syncwarp();
-        if (ok && lane == 0) mbar_arrive(&op_full[sa]);
+        if (ok && lane == 0) mbar_arrive(&a16_full[sa]);
         if (++sa == SA) { sa = 0; pa ^= 1u; }
       }
     } else {
@@ -443,7 +462,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         for (int kb = 0; kb < n_kb; ++kb) {
           ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a8_full[s8], p8, abort_flag, status, site + 3));
           if (ok && wrapped)
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&op_empty[sa], pa ^ 1u, abort_flag, status, site + 4));
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a16_empty[sa], pa ^ 1u, abort_flag, status, site + 4));
           if (ok) {
             tc_fence_after();
             const char* src = smem + OFF_A8 + s8 * A8_BYTES + row * KB;
@@ -470,7 +489,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(&a8_empty[s8]);
-            mbar_arrive(&op_full[sa]);
+            mbar_arrive(&a16_full[sa]);
           }
           if (!ok) break;
           if (++s8 == S8) { s8 = 0; p8 ^= 1u; }
@@ -481,12 +500,11 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     }
   } else if (aligned && warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
-    // One 128-K stage per iteration: wait for the stage (its weight slot in
-    // tensor memory and its token stage in shared memory, one barrier), then
-    // one elected lane issues its eight K16 MMAs, one commit frees both, and
-    // at the end of a 1024-K chunk another commits the accumulator.  (One
-    // thread running the role alone, or rounds of two or four stages, measured
-    // slower.)  Ring slots and phases are running counters; the token
+    // One 128-K stage per iteration: wait for its weight slot (tensor
+    // memory) and token stage (shared memory), then one elected lane issues
+    // its eight K16 MMAs and commits the slot, the stage and, at the end of a
+    // 1024-K chunk, the accumulator.  (One thread running the role alone, or
+    // rounds of two or four stages, measured slower.)  Ring slots and phases are running counters; the token
     // descriptor advances by addition in its address field (16-byte units: +2
     // per K16 step, +1024 per 16 KB atom); the weight operand is read from
     // tensor memory, 8 columns per K16 step.
@@ -517,7 +535,9 @@ __global__ void __launch_bounds__(kBigThreads, 1)
               break;
             }
           }
-          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&op_full[sa], pa, abort_flag, status, site + 6))) {
+          const bool w = mbar_wait_bounded(&a16_full[sa], pa, abort_flag, status, site + 6) &&
+                         mbar_wait_bounded(&b_full[sa], pa, abort_flag, status, site + 7);
+          if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;
           }
@@ -535,7 +555,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
             umma_f16_ts(d_tmem, at + 40, bd + kAtom + 2, idesc, 1u);
             umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
             umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
-            umma_commit(&op_empty[sa]);
+            umma_commit(&a16_empty[sa]);
+            umma_commit(&b_empty[sa]);
             if (last) umma_commit(&acc_full[acc_n & 1]);
           }
           __syncwarp();
