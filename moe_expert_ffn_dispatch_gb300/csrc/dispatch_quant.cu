@@ -578,7 +578,12 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_finish_kernel(Fw
 
 }  // namespace
 
-size_t dispatch_smem_bytes(int E) { return sizeof(int32_t) * static_cast<size_t>(33 * E); }
+// [E] + [32][E] of the ranking, and at least stride(E) + 1 ints for the
+// tail's prefix of the small slots' costs
+size_t dispatch_smem_bytes(int E) {
+  const int a = 33 * E, b = SlotTable::stride(E) + 1;
+  return sizeof(int32_t) * static_cast<size_t>(a > b ? a : b);
+}
 
 cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s) {
   const int nd = p.disp_chunks > 1 ? p.disp_chunks : 1;

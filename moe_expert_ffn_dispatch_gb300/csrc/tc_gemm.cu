@@ -92,7 +92,6 @@ constexpr int OFF_B16 = 0;                           // SB x ATOMS x [128][64] f
 constexpr int OFF_A8 = OFF_B16 + SB * F16_TILE;      // S8 x [128][128] int8, swizzled (TMA)
 constexpr int OFF_BAR = OFF_A8 + S8 * A8_BYTES;
 constexpr int NBAR = 2 * S8 + 2 * SA + 2 * SB + 4 + 2 * SI + 1;
-static_assert(SA == SB, "a stage's weight slot and token stage share one ring index");
 constexpr int OFF_INFO = OFF_BAR + NBAR * 8;         // tok_scale, tok_row, tok_tok [TB]
 constexpr int OFF_ITEM = OFF_INFO + 3 * TB * 4;      // SI decoded items, 8 ints each
 constexpr int OFF_MISC = OFF_ITEM + SI * 8 * 4;      // tmem slot, abort flag
@@ -511,8 +510,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     {
       const uint32_t a_tmem0 = tmem + kAccCols;
       const uint64_t b_desc0 = umma_desc_sw128(smem_u32(smem + OFF_B16));
-      int sa = 0;
-      uint32_t pa = 0;
+      int sa = 0, sb = 0;
+      uint32_t pa = 0, pb = 0;
       long acc_n = 0;
       bool ok = true;
       for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
@@ -536,7 +535,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
             }
           }
           const bool w = mbar_wait_bounded(&a16_full[sa], pa, abort_flag, status, site + 6) &&
-                         mbar_wait_bounded(&b_full[sa], pa, abort_flag, status, site + 7);
+                         mbar_wait_bounded(&b_full[sb], pb, abort_flag, status, site + 7);
           if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;
@@ -546,7 +545,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
           if (elect_one()) {
             constexpr uint64_t kAtom = F16_ATOM >> 4;
             const uint32_t at = a_tmem0 + sa * kAStageCols;
-            const uint64_t bd = b_desc0 + static_cast<uint64_t>(sa * (F16_TILE >> 4));
+            const uint64_t bd = b_desc0 + static_cast<uint64_t>(sb * (F16_TILE >> 4));
             umma_f16_ts(d_tmem, at, bd, idesc, kc != 0 ? 1u : 0u);
             umma_f16_ts(d_tmem, at + 8, bd + 2, idesc, 1u);
             umma_f16_ts(d_tmem, at + 16, bd + 4, idesc, 1u);
@@ -556,11 +555,12 @@ __global__ void __launch_bounds__(kBigThreads, 1)
             umma_f16_ts(d_tmem, at + 48, bd + kAtom + 4, idesc, 1u);
             umma_f16_ts(d_tmem, at + 56, bd + kAtom + 6, idesc, 1u);
             umma_commit(&a16_empty[sa]);
-            umma_commit(&b_empty[sa]);
+            umma_commit(&b_empty[sb]);
             if (last) umma_commit(&acc_full[acc_n & 1]);
           }
           __syncwarp();
           if (++sa == SA) { sa = 0; pa ^= 1u; }
+          if (++sb == SB) { sb = 0; pb ^= 1u; }
           if (last) {
             ++acc_n;
             kc = 0;

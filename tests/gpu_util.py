@@ -114,6 +114,16 @@ def assert_rel(got: torch.Tensor, ref: torch.Tensor, rel: float, what: str):
 SMALL_ROWS = 8  # experts with at most this many rows take the dp4a path (when h, I <= 4096)
 
 
+def small_max_rows(blk, wl):
+    """Largest row count of an expert (or the shared expert) that still runs on
+    the dp4a path: every expert in a batch of at most 8 tokens (an expert with
+    more rows, from repeated ids, in several 8-row slots), 8 otherwise; none
+    with MOE_FLAG_UNFUSED or hidden / inter above 4096."""
+    if not (wl.hidden <= 4096 and wl.inter <= 4096 and not (blk.cfg.flags & m.FLAG_UNFUSED)):
+        return 0
+    return (1 << 30) if wl.bs <= SMALL_ROWS else SMALL_ROWS
+
+
 def active_tokens(inp):
     bs = inp.wl.bs
     mask = torch.ones(bs, dtype=torch.bool) if inp.mask is None else inp.mask
@@ -131,14 +141,14 @@ def row_paths(blk, inp, counts):
     _, act = active_tokens(inp)
     S = int(act.numel()) if wl.has_shared else 0
     rows = bs * K + (bs if wl.has_shared else 0)
-    small_ok = h <= 4096 and I <= 4096 and not (blk.cfg.flags & m.FLAG_UNFUSED)
+    cap = small_max_rows(blk, wl)
     big = torch.zeros(rows, dtype=torch.bool)
     off = 0
     for c in counts:
-        big[off:off + c] = (not small_ok) or (c > SMALL_ROWS and bs > SMALL_ROWS)
+        big[off:off + c] = c > cap
         off += c
     if S:
-        big[bs * K:bs * K + S] = not (small_ok and S <= SMALL_ROWS)
+        big[bs * K:bs * K + S] = S > cap
     return big
 
 
@@ -331,15 +341,7 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None, planted=True):
         # oracle (the dequant before it is exact: GEMM1's int32 accumulators are
         # checked bit for bit by check_raw_accumulators)
         hb = staged_h.view(torch.float32)[:rows * 2 * I].view(rows, 2 * I)
-        small_ok = h <= 4096 and I <= 4096 and not (blk.cfg.flags & m.FLAG_UNFUSED)
         counts = ref["expert_token_nums"].tolist()
-        big_row = torch.zeros(R, dtype=torch.bool)
-        off = 0
-        for e, c in enumerate(counts):
-            # a batch of at most SMALL_ROWS tokens runs every expert on the dp4a
-            # path (an expert with more rows, from repeated ids, in several slots)
-            big_row[off:off + c] = (not small_ok) or (c > SMALL_ROWS and bs > SMALL_ROWS)
-            off += c
         if R:
             assert_rel(hb[:R, :I], ref["h"], H_REL, "h routed")
         if S:
@@ -348,11 +350,7 @@ def run_and_check(inp, dev, staged=True, bs_max=None, blk=None, planted=True):
         # only as exact f16 values (x2h, the tensor-core GEMM2 operand)
         x2 = region(blk, "x2", torch.int8, (rows, I)).clone()
         x2h = region(blk, "x2h", torch.int16, (rows, I)).view(torch.float16).to(torch.int8)
-        shared_big = bool(S) and not (small_ok and S <= SMALL_ROWS)
-        row_big = torch.zeros(rows, dtype=torch.bool)
-        row_big[:R] = big_row
-        if shared_big:
-            row_big[bs * K:bs * K + S] = True
+        row_big = row_paths(blk, inp, counts)
         x2[row_big] = x2h[row_big]
         s2 = region(blk, "s2", torch.float32, (rows,))
         assert_codes_close(x2[:R], ref["x2"], "x2 routed")

@@ -14,7 +14,7 @@ import torch
 
 import synth
 from gpu_util import (check_planted_gemm2, check_raw_accumulators, device_inputs, device_weights, make_block,
-                      region, run_and_check)
+                      region, run_and_check, small_max_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,6 +48,13 @@ FULL_K_CASES = [
     # 40 tokens, Zipf over 8 experts: hot experts on the tensor cores, cold ones on dp4a
     synth.custom("mixed_fullk_zipf", bs=40, hidden=4096, num_experts=8, topk=2, inter=2048, has_shared=True,
                  routing="zipf", masked_fraction=0.1, smooth=True, seed=73),
+    # 128 tokens over 16 experts: 6 and 7 rows on dp4a, 12-121 rows and the 128-row
+    # shared expert on the tensor cores (one to two 128-row blocks)
+    synth.custom("mixed_fullk_e16", bs=128, hidden=4096, num_experts=16, topk=4, inter=2048,
+                 has_shared=True, routing="zipf", seed=76),
+    # 160 tokens over 32 experts: 14 experts with at most 8 rows, 18 on the tensor cores
+    synth.custom("mixed_fullk_e32", bs=160, hidden=4096, num_experts=32, topk=4, inter=2048, has_shared=True,
+                 routing="zipf", seed=78),
 ]
 
 
@@ -58,6 +65,15 @@ def test_full_k_staged_parity(wl):
     counts = ref["expert_token_nums"].tolist()
     if wl.bs > 8:
         assert any(c > 8 for c in counts) and any(0 < c <= 8 for c in counts), counts
+    # the slot table's split (bit-exact): experts up to the cap in slots of at
+    # most 8 rows on dp4a, the others (and the shared expert above the cap) in
+    # big slots on the tensor cores
+    cap = small_max_rows(blk, wl)
+    S = (int(inp.mask.sum()) if inp.mask is not None else wl.bs) if wl.has_shared else 0
+    want_big = sum(c > cap for c in counts) + int(S > cap)
+    want_small = sum((c + 7) // 8 for c in counts if 0 < c <= cap) + ((S + 7) // 8 if 0 < S <= cap else 0)
+    tab = region(blk, "slots", torch.int32, (8,)).tolist()
+    assert (tab[0], tab[4]) == (want_big, want_small), (tab[:8], want_big, want_small)
     check_raw_accumulators(blk, inp, ref, di, dw, DEV)
 
 
