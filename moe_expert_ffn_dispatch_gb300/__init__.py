@@ -468,3 +468,110 @@ class GraphedStep:
 
     def d2h_bytes(self) -> int:
         return sum(v.numel() * v.element_size() for v in self.host_outputs.values())
+
+
+class PipelinedStep:
+    """A serving loop whose host copies overlap the neighbouring steps'
+    forwards.  Step k uses buffer set k % depth (each set: pinned host inputs
+    and outputs, packed device inputs and outputs, and a CUDA graph of the
+    forward on them).  submit() enqueues, for the step's set:
+      * the packed host-to-device copy of its inputs, on the copy-in stream,
+        once the forward that last read that set's device inputs is done;
+      * its forward (the set's graph), on the compute stream, once those
+        inputs have landed and the copy that last read the set's device
+        outputs is done -- forwards run one after another on this stream,
+        sharing the block's workspace;
+      * the packed device-to-host copy of its outputs, on the copy-out
+        stream, once the forward is done.
+    So while step k computes, step k + 1's inputs and step k - 1's outputs
+    move.  Every step still copies all of its inputs in and all of its outputs
+    out.
+
+    host_inputs: initial values of every set's inputs (as for GraphedStep).
+    Before writing step k's inputs, take the views from inputs_for(k) (it
+    waits until that set's previous input copy has left the buffer).
+    result(k) waits for step k's outputs and returns the set's host output
+    views, valid until step k + depth is submitted.
+    """
+
+    def __init__(self, blk: MoeFused, host_inputs: Dict[str, torch.Tensor], weights: Dict[str, torch.Tensor],
+                 depth: int = 2):
+        if depth < 2:
+            raise ValueError("depth must be at least 2")
+        self.blk, self.weights, self.depth = blk, weights, depth
+        dev = blk.device
+        specs = [(k, tuple(v.shape), v.dtype) for k, v in host_inputs.items()]
+        bs, h = host_inputs["x"].shape
+        ospecs = [("output", (bs, h), blk.act_dtype), ("expert_token_nums", (blk.cfg.num_experts,), torch.int32)]
+        if blk.cfg.has_shared:
+            ospecs.append(("share_output", (bs, h), blk.act_dtype))
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_comp = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
+        blk.workspace()  # allocated before the captures
+        self.sets = []
+        for _ in range(depth):
+            st = {}
+            st["hin_buf"], st["hin"] = _packed(specs, "cpu", pinned=True)
+            st["din_buf"], st["din"] = _packed(specs, dev)
+            st["dout_buf"], st["dout"] = _packed(ospecs, dev)
+            st["hout_buf"], st["hout"] = _packed(ospecs, "cpu", pinned=True)
+            for k, v in host_inputs.items():
+                st["hin"][k].copy_(v)
+            st["din_buf"].copy_(st["hin_buf"])
+            for name in ("ev_in", "ev_fwd", "ev_out"):
+                st[name] = torch.cuda.Event()
+            with torch.cuda.stream(self.s_comp):
+                self._forward(st)  # eager once: builds the tensor maps, checks the arguments
+            self.s_comp.synchronize()
+            st["graph"] = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(st["graph"], stream=self.s_comp):
+                self._forward(st)
+            self.s_comp.synchronize()
+            self.sets.append(st)
+        self.submitted = 0
+
+    def _forward(self, st):
+        o = st["dout"]
+        self.blk.forward_inputs(st["din"], self.weights, out=o["output"], share_out=o.get("share_output"),
+                                token_nums=o["expert_token_nums"])
+
+    def inputs_for(self, k: int) -> Dict[str, torch.Tensor]:
+        """Host input views of step k's set, once its previous copy-in is done."""
+        st = self.sets[k % self.depth]
+        st["ev_in"].synchronize()
+        return st["hin"]
+
+    def submit(self) -> int:
+        """Enqueue the next step; returns its index."""
+        k = self.submitted
+        st = self.sets[k % self.depth]
+        self.s_in.wait_event(st["ev_fwd"])    # the set's device inputs are free
+        with torch.cuda.stream(self.s_in):
+            st["din_buf"].copy_(st["hin_buf"], non_blocking=True)
+            st["ev_in"].record(self.s_in)
+        self.s_comp.wait_event(st["ev_in"])
+        self.s_comp.wait_event(st["ev_out"])  # the set's device outputs are free
+        with torch.cuda.stream(self.s_comp):
+            st["graph"].replay()
+            st["ev_fwd"].record(self.s_comp)
+        self.s_out.wait_event(st["ev_fwd"])
+        with torch.cuda.stream(self.s_out):
+            st["hout_buf"].copy_(st["dout_buf"], non_blocking=True)
+            st["ev_out"].record(self.s_out)
+        self.submitted = k + 1
+        return k
+
+    def result(self, k: int) -> Dict[str, torch.Tensor]:
+        """Host output views of step k (waits for its copy-out)."""
+        if not (self.submitted - self.depth <= k < self.submitted):
+            raise ValueError("step %d is not among the last %d submitted" % (k, self.depth))
+        st = self.sets[k % self.depth]
+        st["ev_out"].synchronize()
+        return st["hout"]
+
+    def h2d_bytes(self) -> int:
+        return sum(v.numel() * v.element_size() for v in self.sets[0]["hin"].values())
+
+    def d2h_bytes(self) -> int:
+        return sum(v.numel() * v.element_size() for v in self.sets[0]["hout"].values())
