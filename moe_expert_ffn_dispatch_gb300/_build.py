@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 SO = os.path.join(HERE, "_moe_fused.so")
 SOURCES = ["api.cu", "dispatch_quant.cu", "moe_gemm.cu", "tc_gemm.cu"]
-HEADERS = ["device_prims.cuh", "epilogue_ops.cuh", "moe_internal.h"]
+HEADERS = ["device_prims.cuh", "epilogue_ops.cuh", "moe_internal.h", "quant_ops.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

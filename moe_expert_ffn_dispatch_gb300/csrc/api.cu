@@ -8,7 +8,10 @@
 //   requant of big blocks -> GEMM2 + bf16 dequant (+ combine when no big
 //   blocks) -> GEMM2 (big) -> combine (when big blocks exist).
 // Kernel boundaries carry the dependencies; inside a GEMM launch the fused
-// epilogues run in the CTA that finishes a block last.  No CTA waits.
+// epilogues run in the CTA that finishes a block last, and a GEMM2 streamed
+// behind GEMM1 waits (bounded) for the requant of its rows.  A batch of at
+// most 8 tokens with per-token quant runs the whole forward as one launch
+// (moe_decode_one_launch_kernel).
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -36,6 +39,9 @@ struct moe_fused_handle {
   moe::TcMaps maps;          // tensor maps of the last forward's operands
   const void* map_key[5];    // pointers they were built for
   bool maps_valid;
+  // workspaces whose grid-barrier arrival count (one-launch decode kernel)
+  // this handle has zeroed; the kernel leaves it at zero after every barrier
+  std::vector<const void*> barrier_ready;
 };
 
 namespace {
@@ -361,6 +367,24 @@ int moe_fused_debug_forward_range(moe_fused_handle_t* hd, const moe_fused_args_t
     if (e == cudaSuccess) e = cudaMemsetAsync(p.ws + p.L.status, 0, 64 * sizeof(int32_t), s);
     return cuda_fail(e);
   }
+  // A batch of at most small_rows tokens with per-token quant: the whole
+  // forward is one launch (dispatch and quant repeated per CTA, then the
+  // streamed GEMMs behind a grid barrier).  The barrier's arrival count must
+  // be zero before the workspace's first such forward; the kernel leaves it
+  // at zero.  After a wait that gave up it may not be: get_status, which
+  // reports that, makes the next forward zero it again.
+  if (p.small_only && !p.xq_per_row && first_kernel == moe::kKDispatchQuant && last_kernel >= moe::kKGemm2Small) {
+    auto& known = hd->barrier_ready;
+    bool seen = false;
+    for (const void* w : known) seen = seen || (w == workspace);
+    if (!seen) {
+      e = cudaMemsetAsync(p.ws + p.L.status + sizeof(int32_t) * moe::kStBarArrive, 0, sizeof(int32_t), s);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (known.size() >= 64) known.erase(known.begin());
+      known.push_back(workspace);
+    }
+    return cuda_fail(timed(hd, moe::kKGemm1Small, s, [&] { return moe::launch_moe_decode_one_launch(p, s); }));
+  }
   rc = prepare_maps(hd, p);
   if (rc) return rc;
   const int sms = p.num_ctas;
@@ -415,7 +439,18 @@ int moe_fused_get_status(moe_fused_handle_t* hd, const void* workspace, void* st
   out->shared_rows = w[moe::kStSharedRows];
   out->active_slots = w[moe::kStSlots];
   out->reserved[0] = out->reserved[1] = 0;
-  return (out->error_flags & moe::kErrWaitTimeout) ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+  if (out->error_flags & moe::kErrWaitTimeout) {
+    // a grid barrier that gave up can leave arrivals counted: zero the count
+    // again before this workspace's next one-launch forward
+    auto& known = hd->barrier_ready;
+    for (size_t i = 0; i < known.size(); ++i)
+      if (known[i] == workspace) {
+        known.erase(known.begin() + static_cast<long>(i));
+        break;
+      }
+    return MOE_ERR_DEVICE_TIMEOUT;
+  }
+  return MOE_OK;
 }
 
 int moe_fused_destroy(moe_fused_handle_t* hd) {

@@ -169,6 +169,19 @@ __device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred)
   return r != 0;
 }
 
+// Named barrier that also returns how many of its threads had `pred` set.
+__device__ __forceinline__ int named_barrier_count(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.popc.u32 %0, %2, %3, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
+      : "memory");
+  return static_cast<int>(r);
+}
+
 // ------------------------------------------------------------ TMA tensor
 // 2-D tiled bulk tensor copy global -> shared, completing bytes on `bar`.
 // `tmap` is the address of a CUtensorMap kernel parameter (__grid_constant__).
@@ -212,6 +225,42 @@ __device__ __forceinline__ bool spin_until_ge(const int32_t* flag, int want, vol
       }
     }
   }
+}
+
+// Grid-wide barrier of a launch whose CTAs are all resident (one per SM),
+// called by one thread of each CTA.  *arrive counts the CTAs other than CTA 0
+// that have arrived and is zero between barriers; *release is the barrier's
+// generation.  A CTA reads the generation before it arrives and waits for it
+// to change; CTA 0 waits for the G - 1 arrivals, puts the count back to zero
+// and then advances the generation.  What a CTA wrote before the call (its
+// other threads' writes ordered by a CTA barrier first) is visible to every
+// CTA after it: a fence before each arrival, acquire loads on the way out.
+// Bounded: false once the wait budget runs out (reported in the status).
+__device__ __forceinline__ bool grid_barrier(int32_t* arrive, int32_t* release, int G, int32_t* status, int site) {
+  __threadfence();
+  const uint64_t t0 = global_timer_ns();
+  uint32_t n = 0;
+  if (blockIdx.x == 0) {
+    while (ld_acquire_gpu(arrive) != G - 1) {
+      if ((++n & 255u) == 0 && global_timer_ns() - t0 > kWaitBudgetNs) {
+        report_timeout(status, site);
+        return false;
+      }
+    }
+    *reinterpret_cast<volatile int32_t*>(arrive) = 0;
+    __threadfence();
+    atomicAdd(release, 1);
+    return true;
+  }
+  const int gen = ld_acquire_gpu(release);
+  atomicAdd(arrive, 1);
+  while (ld_acquire_gpu(release) == gen) {
+    if ((++n & 255u) == 0 && global_timer_ns() - t0 > kWaitBudgetNs) {
+      report_timeout(status, site);
+      return false;
+    }
+  }
+  return true;
 }
 
 // true in exactly one lane of the (converged) warp: lets a warp run a loop

@@ -9,6 +9,7 @@
 
 #include "device_prims.cuh"
 #include "moe_internal.h"
+#include "quant_ops.cuh"
 
 namespace moe {
 namespace {
@@ -16,7 +17,6 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
-constexpr float kAmaxEps = 1e-4f;
 constexpr float kInv127 = 1.0f / 127.0f;  // the fp32 nearest to 1/127
 
 __device__ __forceinline__ void consumer_sync() { named_barrier_sync(1, kConsumers); }

@@ -37,6 +37,7 @@
 #include "device_prims.cuh"
 #include "epilogue_ops.cuh"
 #include "moe_internal.h"
+#include "quant_ops.cuh"
 
 namespace moe {
 
@@ -57,11 +58,13 @@ constexpr int kRowsPerWarp = BN / kConsumerWarps;  // 4
 constexpr int OFF_W = 0;                                        // STAGES x [BN][KC] weights
 constexpr int OFF_T = OFF_W + STAGES * BN * KC;                 // [m][K] token rows of the current run
 constexpr int OFF_Y = OFF_T + MT * kMaxK;                       // 2 x [BN][MT] fp32
-constexpr int OFF_BAR = OFF_Y + 2 * BN * MT * 4;                // full, empty [STAGES]; tok_full, tok_empty
-constexpr int OFF_INFO = OFF_BAR + (2 * STAGES + 2) * 8;        // kInfoSlots x {scale, row, token}[MT]
+constexpr int kNumBars = 2 * STAGES + 3;                        // full, empty [STAGES]; tok_full, tok_empty; ready
+constexpr int OFF_BAR = OFF_Y + 2 * BN * MT * 4;
+constexpr int OFF_INFO = OFF_BAR + kNumBars * 8;                // kInfoSlots x {scale, row, token}[MT]
 constexpr int OFF_SLOT = OFF_INFO + kInfoSlots * 3 * MT * 4;    // 2 x kSlotCache x {e, row0, rows}: GEMM1, GEMM2
-constexpr int OFF_MISC = OFF_SLOT + 2 * kSlotCache * 3 * 4;     // abort, flag, red[8], tok[MT]
-constexpr int SMEM_BYTES = OFF_MISC + (2 + kConsumerWarps + MT) * 4;
+constexpr int OFF_MISC = OFF_SLOT + 2 * kSlotCache * 3 * 4;     // abort, flag, red[8], tok[MT], range[4]
+constexpr int MISC_RANGE = 2 + kConsumerWarps + MT;             // item range {begin, end} of GEMM1, GEMM2
+constexpr int SMEM_BYTES = OFF_MISC + (MISC_RANGE + 4) * 4;
 static_assert(kRowsPerWarp * MT == 32, "one reduced value per lane");
 static_assert(kInfoSlots > STAGES, "info ring must outlive the stage ring");
 
@@ -168,12 +171,30 @@ struct SmallItem {
 // run in one launch (the rings and barriers are not re-initialised between).
 struct SmallState {
   int stage_it = 0, item_no = 0, run_no = 0;
+  bool ready_seen = false;  // the producer has seen the one-launch kernel's `ready` barrier complete
 };
+
+// This CTA's contiguous run of items of one GEMM (consecutive tiles of one
+// expert are contiguous in memory), and whether the forward has big blocks
+// (then the combine kernel, not the small GEMM2, combines the tokens).
+struct SmallRange {
+  int it_begin, it_end;
+  bool has_big;
+};
+
+// The range as the dispatch kernel left it in the workspace.
+template <bool G1>
+__device__ __forceinline__ SmallRange global_range(const FwdParams& p) {
+  const int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges) + (G1 ? 0 : kMaxCtas + 1);
+  const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
+  return SmallRange{ranges[blockIdx.x], ranges[blockIdx.x + 1], slots[SlotTable::kBigBlocks] > 0};
+}
 
 __device__ __forceinline__ void init_rings(char* smem) {
   if (threadIdx.x == 0) {
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    for (int s = 0; s < 2 * STAGES + 2; ++s) mbar_init(&full[s], (s < STAGES || s == 2 * STAGES) ? 1 : kConsumerWarps);
+    for (int s = 0; s < kNumBars; ++s)
+      mbar_init(&full[s], (s < STAGES || s == 2 * STAGES || s == 2 * STAGES + 2) ? 1 : kConsumerWarps);
     *reinterpret_cast<volatile int*>(smem + OFF_MISC) = 0;  // abort flag
     fence_barrier_init();
   }
@@ -194,32 +215,43 @@ __device__ __forceinline__ void drain_copies(char* smem, const SmallState& ss, i
   if (ss.run_no > 0) mbar_wait_bounded(tok_full, (ss.run_no - 1) & 1, nullptr, status, site);
 }
 
-// this CTA's slots of one GEMM's item range into its shared-memory cache
-// (the caller synchronises the block afterwards)
+// this CTA's slots of one GEMM's item range into its shared-memory cache, by
+// threads [0, kSlotCache): `sm_exp` is the small slots' expert array, the
+// first-row and row-count arrays follow it at `stride` (the workspace's slot
+// table, or the one-launch kernel's own copy in shared memory).  The caller
+// synchronises the block afterwards.
 template <bool G1>
-__device__ __forceinline__ void cache_slots(const FwdParams& p, char* smem) {
+__device__ __forceinline__ void cache_slots(const FwdParams& p, char* smem, const SmallRange& rg,
+                                            const int32_t* sm_exp, int stride) {
   const int J = G1 ? p.I / (BN / 2) : p.h / BN;
-  const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
-  const int st = SlotTable::stride(p.E);
-  const int32_t* sm_exp = slots + SlotTable::kHeader + 4 * st;
-  const int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges) + (G1 ? 0 : kMaxCtas + 1);
-  const long it_begin = ranges[blockIdx.x], it_end = ranges[blockIdx.x + 1];
-  const int slot_first = static_cast<int>(it_begin / J);
-  const int n_cached = it_end > it_begin ? static_cast<int>((it_end - 1) / J) - slot_first + 1 : 0;
+  const int slot_first = rg.it_begin / J;
+  const int n_cached = rg.it_end > rg.it_begin ? (rg.it_end - 1) / J - slot_first + 1 : 0;
   int32_t* cache = reinterpret_cast<int32_t*>(smem + OFF_SLOT) + (G1 ? 0 : 3 * kSlotCache);
   if (threadIdx.x < kSlotCache && threadIdx.x < n_cached) {
     const int sl = slot_first + threadIdx.x;
     cache[3 * threadIdx.x + 0] = sm_exp[sl];
-    cache[3 * threadIdx.x + 1] = sm_exp[st + sl];
-    cache[3 * threadIdx.x + 2] = sm_exp[2 * st + sl];
+    cache[3 * threadIdx.x + 1] = sm_exp[stride + sl];
+    cache[3 * threadIdx.x + 2] = sm_exp[2 * stride + sl];
   }
 }
 
-// One GEMM over this CTA's item range.  `streamed`: GEMM2 running in the
-// same launch right after GEMM1 -- each small slot's rows are read only once
-// the CTA that requantised them has marked the slot's ticket (tiles + 1).
+template <bool G1>
+__device__ __forceinline__ void cache_slots_global(const FwdParams& p, char* smem, const SmallRange& rg) {
+  const int st = SlotTable::stride(p.E);
+  cache_slots<G1>(p, smem, rg, ws_ptr<int32_t>(p, p.L.slots) + SlotTable::kHeader + 4 * st, st);
+}
+
+// One GEMM over this CTA's item range `rg`.  `streamed`: GEMM2 running in
+// the same launch right after GEMM1 -- each small slot's rows are read only
+// once the CTA that requantised them has marked the slot's ticket (tiles + 1).
+// `ready` (one-launch kernel, else null): the producer reads nothing another
+// CTA writes in this launch -- the slot table in the workspace, the token
+// rows, the row info, the tickets -- before this barrier's first phase has
+// completed (the grid barrier behind the dispatch); its weight copies need
+// only the slot cache and may start earlier.
 template <int MODE>
-__device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss, bool streamed) {
+__device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss, bool streamed, const SmallRange& rg,
+                    uint64_t* ready) {
   constexpr bool G1 = (MODE == kGemm1SwiGLU || MODE == kGemm1Raw);
   constexpr bool RAW = (MODE == kGemm1Raw || MODE == kGemm2Raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -245,13 +277,9 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
   const int32_t* sm_exp = slots + SlotTable::kHeader + 4 * st;
   const int32_t* sm_row0 = sm_exp + st;
   const int32_t* sm_rows = sm_row0 + st;
-  // contiguous run of items for this CTA (consecutive tiles of one expert are
-  // contiguous in memory), split by cost in the dispatch kernel
-  // with big blocks in the forward, tokens are combined by the combine kernel
-  const bool has_big = slots[SlotTable::kBigBlocks] > 0;
-  const int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges) + (G1 ? 0 : kMaxCtas + 1);
-  const long it_begin = ranges[blockIdx.x];
-  const long it_end = ranges[blockIdx.x + 1];
+  const bool has_big = rg.has_big;
+  const long it_begin = rg.it_begin;
+  const long it_end = rg.it_end;
   const int slot_first = static_cast<int>(it_begin / J);
   const int n_cached = it_end > it_begin ? static_cast<int>((it_end - 1) / J) - slot_first + 1 : 0;
   const int site = (G1 ? kKGemm1Small : kKGemm2Small) * 16;
@@ -315,6 +343,14 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
     // read its info only after that, so tok_full's release publishes that
     // item's info entry; the run's later items publish theirs through the
     // full[s] arrive of their first stage.
+    auto wait_ready = [&]() -> bool {
+      if (ready == nullptr || ss.ready_seen) return true;
+      if (!mbar_wait_bounded(ready, 0, abort_flag, status, site + 6, false)) return false;
+      ss.ready_seen = true;
+      return *abort_flag == 0;
+    };
+    // slots beyond the cache are read from the workspace's slot table
+    if (!cached && it_begin < it_end && !wait_ready()) return;
     int run_tok = 0;
     float run_scale = 0.0f;
     SmallItem nx{};
@@ -330,8 +366,9 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
       }
       if (lane == 0) mbar_arrive_expect_tx(tok_full, static_cast<uint32_t>(x.m * K));
       __syncwarp();
-      // x2 written by another CTA's generic stores, read here by a bulk copy
-      if (!G1 && streamed) fence_proxy_async_global();
+      // x2 (or, in the one-launch kernel, x_q) written by another CTA's
+      // generic stores, read here by a bulk copy
+      if ((!G1 && streamed) || ready != nullptr) fence_proxy_async_global();
       if (lane < x.m) {
         const int8_t* trow =
             !G1 ? x2 + static_cast<size_t>(x.row0 + lane) * p.I
@@ -373,6 +410,7 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
         bulk_g2s(smem + OFF_W + (s * BN + lane) * KC, wrow + k0, bytes, &full[s], pol_w);
       }
       if (new_run) {
+        if (!wait_ready()) return;
         if (!load_info(cur, run_tok, run_scale)) return;
         if (lane < cur.m) {
           info_scale[is * MT + lane] = run_scale;
@@ -500,6 +538,280 @@ __device__ void run(const FwdParams& p, int32_t* raw, char* smem, SmallState& ss
   }
 }
 
+
+// ================================================================ one launch
+// A batch of at most kSmallRows tokens (every expert small) runs its whole
+// forward in one launch, the persistent single launch of the Mega-MoE FIFO
+// analysis (§5.1-§5.2) at decode batch sizes.  Each CTA repeats the dispatch
+// of the at most kSmallRows * kMaxTopk (t, k) pairs in its own shared memory
+// (the dispatch kernel's counting-sort order, slot table and cost split), so
+// its weight copies can start at once; CTA 0 writes the dispatch arrays into
+// the workspace, CTAs 1 .. bs quantise one token each, every CTA clears a
+// share of the tickets, and one grid barrier later the GEMM1 -> GEMM2 stream
+// runs as in the streamed kernel.
+
+// Scratch of the per-CTA dispatch: int32 words in the token-row area, which
+// receives no token row before the grid barrier.
+constexpr int kMaxPairs = kSmallRows * kMaxTopk;     // (t, k) pairs of a batch
+constexpr int kMaxSmallSlots = kMaxPairs + 1;        // a slot per routed row, plus the shared expert's
+constexpr int TD_PE = 0;                             // [kMaxPairs] expert of pair f, -1 if not routed
+constexpr int TD_ROW = TD_PE + kMaxPairs;            // [kMaxPairs] rank of pair f in its expert, then its row
+constexpr int TD_SCAN = TD_ROW + kMaxPairs;          // [8] warp totals of a scan
+constexpr int TD_MISC = TD_SCAN + 8;                 // [8] skipped pairs, R, small slots, active tokens, shared rows
+constexpr int TD_AFLAG = TD_MISC + 8;                // [kSmallRows] token t active
+constexpr int TD_ACT = TD_AFLAG + kSmallRows;        // [kSmallRows] active tokens in ascending order
+constexpr int TD_SROW = TD_ACT + kSmallRows;         // [kSmallRows] shared-expert row of token t, -1 if inactive
+constexpr int TD_SLOT = TD_SROW + kSmallRows;        // 3 x [kMaxSmallSlots] small slots: expert, first row, rows
+constexpr int TD_WP = TD_SLOT + 3 * kMaxSmallSlots;  // [kMaxSmallSlots + 1] exclusive prefix of the slot costs
+constexpr int TD_CNT = TD_WP + kMaxSmallSlots + 1;   // [1024] rows per expert
+constexpr int TD_OFF = TD_CNT + 1024;                // [1024] first row per expert
+constexpr int TD_WORDS = TD_OFF + 1024;
+static_assert(TD_WORDS * 4 <= MT * kMaxK, "dispatch scratch fits the token-row area");
+static_assert(4 * kConsumers >= 1024, "four experts per consumer thread cover E <= 1024");
+static_assert(kMaxSmallSlots < kConsumers, "one slot per consumer thread in the cost scan");
+
+// Exclusive prefix sum of one int per consumer thread, and the total.  s_w:
+// kConsumerWarps ints of scratch.  Both consumer barriers are inside.
+__device__ __forceinline__ int consumer_excl_scan(int v, int32_t* s_w, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_w[warp] = incl;
+  consumer_sync();
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) {
+    const int x = s_w[w];
+    before += w < warp ? x : 0;
+    tot += x;
+  }
+  *total = tot;
+  consumer_sync();
+  return incl - v + before;
+}
+
+// The dispatch of the batch into this CTA's shared memory, by the consumer
+// threads: the rows of every pair (rank by flat index t * topk + k inside its
+// expert, experts in ascending id), the small slots (an expert with c rows in
+// ceil(c / small_rows) slots, then the shared expert on the active tokens),
+// this CTA's item ranges of both GEMMs and its slot caches.
+__device__ void local_dispatch(const FwdParams& p, char* smem) {
+  int32_t* td = reinterpret_cast<int32_t*>(smem + OFF_T);
+  int32_t* rng = reinterpret_cast<int32_t*>(smem + OFF_MISC) + MISC_RANGE;
+  int32_t* s_exp = td + TD_SLOT;
+  int32_t* s_row0 = s_exp + kMaxSmallSlots;
+  int32_t* s_rows = s_row0 + kMaxSmallSlots;
+  const int ctid = threadIdx.x;
+  const int E = p.E, K = p.topk, bs = p.bs, P = bs * K, sr = p.small_rows;
+  // 1. the expert of every pair (-1: token masked out, or id outside [0, E))
+  for (int e = ctid; e < E; e += kConsumers) td[TD_CNT + e] = 0;
+  bool skip = false;
+  if (ctid < P) {
+    const int t = ctid / K;
+    const bool act = p.mask == nullptr || p.mask[t] != 0;
+    const int id = p.ids[ctid];
+    const bool valid = act && id >= 0 && id < E;
+    skip = act && !valid;
+    td[TD_PE + ctid] = valid ? id : -1;
+  }
+  if (ctid < bs) td[TD_AFLAG + ctid] = (p.mask == nullptr || p.mask[ctid] != 0) ? 1 : 0;
+  const int skipped = named_barrier_count(1, kConsumers, skip);
+  // 2. rank of each pair among its expert's pairs; rows per expert
+  if (ctid < P) {
+    const int e = td[TD_PE + ctid];
+    if (e >= 0) {
+      int rank = 0;
+      for (int f = 0; f < ctid; ++f) rank += td[TD_PE + f] == e;
+      td[TD_ROW + ctid] = rank;
+      atomicAdd(&td[TD_CNT + e], 1);
+    }
+  }
+  consumer_sync();
+  // 3. first row and first slot of every expert: one scan of the row count
+  //    and the slot count packed in 16-bit halves (both totals <= kMaxPairs)
+  int c[4], n[4], mine = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * ctid + j;
+    c[j] = e < E ? td[TD_CNT + e] : 0;
+    n[j] = (c[j] + sr - 1) / sr;
+    mine += c[j] | (n[j] << 16);
+  }
+  int tot;
+  const int ex = consumer_excl_scan(mine, td + TD_SCAN, &tot);
+  {
+    int rc = ex & 0xFFFF, rn = ex >> 16;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * ctid + j;
+      if (e < E) {
+        td[TD_OFF + e] = rc;
+        for (int q = 0; q < n[j]; ++q) {
+          s_exp[rn + q] = e;
+          s_row0[rn + q] = rc + q * sr;
+          s_rows[rn + q] = min(sr, c[j] - q * sr);
+        }
+      }
+      rc += c[j];
+      rn += n[j];
+    }
+  }
+  const int R = tot & 0xFFFF, ns_routed = tot >> 16;
+  consumer_sync();
+  // 4. row of every pair; the active tokens and the shared expert's slot
+  if (ctid < P) {
+    const int e = td[TD_PE + ctid];
+    if (e >= 0) td[TD_ROW + ctid] += td[TD_OFF + e];
+  }
+  if (ctid == 0) {
+    int S = 0;
+    for (int t = 0; t < bs; ++t) {
+      if (td[TD_AFLAG + t]) {
+        td[TD_ACT + S] = t;
+        td[TD_SROW + t] = bs * K + S;
+        ++S;
+      } else {
+        td[TD_SROW + t] = -1;
+      }
+    }
+    int ns = ns_routed;
+    const int shared_rows = p.has_shared ? S : 0;  // S <= bs <= small_rows: one small slot
+    if (shared_rows > 0) {
+      s_exp[ns] = -1;
+      s_row0[ns] = bs * K;
+      s_rows[ns] = shared_rows;
+      ++ns;
+    }
+    td[TD_MISC + 0] = skipped;
+    td[TD_MISC + 1] = R;
+    td[TD_MISC + 2] = ns;
+    td[TD_MISC + 3] = S;
+    td[TD_MISC + 4] = shared_rows;
+  }
+  consumer_sync();
+  // 5. cost prefix of the small slots, this CTA's item ranges, its caches
+  const int ns = td[TD_MISC + 2];
+  int wtot;
+  const int wex = consumer_excl_scan(ctid < ns ? 12 + s_rows[ctid] : 0, td + TD_SCAN, &wtot);
+  if (ctid <= ns) td[TD_WP + ctid] = wex;
+  consumer_sync();
+  if (ctid < 4) {
+    const int J = (ctid >> 1) == 0 ? p.I / (BN / 2) : p.h / BN;
+    rng[ctid] = small_item_start(td + TD_WP, ns, J, p.num_ctas, blockIdx.x + (ctid & 1));
+  }
+  consumer_sync();
+  cache_slots<true>(p, smem, SmallRange{rng[0], rng[1], false}, s_exp, kMaxSmallSlots);
+  cache_slots<false>(p, smem, SmallRange{rng[2], rng[3], false}, s_exp, kMaxSmallSlots);
+}
+
+// CTA 0's copy of the dispatch into the workspace: what the dispatch kernel
+// writes for the same batch (counts, offsets, expert_token_nums, row maps,
+// active list, slot table, status words, the item ranges of every CTA, the
+// per-token GEMM2 counters).  By the consumer threads.
+__device__ void publish_dispatch(const FwdParams& p, const int32_t* td) {
+  const int ctid = threadIdx.x;
+  const int E = p.E, K = p.topk, bs = p.bs, P = bs * K, G = p.num_ctas;
+  const int skipped = td[TD_MISC], R = td[TD_MISC + 1], ns = td[TD_MISC + 2], S = td[TD_MISC + 3];
+  const int shared_rows = td[TD_MISC + 4];
+  const int32_t* s_exp = td + TD_SLOT;
+  int32_t* counts = ws_ptr<int32_t>(p, p.L.counts);
+  int32_t* offsets = ws_ptr<int32_t>(p, p.L.offsets);
+  int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
+  int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
+  int32_t* row_token = ws_ptr<int32_t>(p, p.L.row_token);
+  int32_t* active = ws_ptr<int32_t>(p, p.L.active);
+  int32_t* shared_row = ws_ptr<int32_t>(p, p.L.shared_row);
+  int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
+  int32_t* status = ws_ptr<int32_t>(p, p.L.status);
+  int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges);
+  for (int e = ctid; e < E; e += kConsumers) {
+    const int c = td[TD_CNT + e];
+    counts[e] = c;
+    offsets[e] = td[TD_OFF + e];
+    p.token_nums[e] = c;
+  }
+  if (ctid < P) {
+    const int r = td[TD_PE + ctid] >= 0 ? td[TD_ROW + ctid] : -1;
+    row_of[ctid] = r;
+    if (r >= 0) {
+      tk_of_row[r] = ctid;
+      row_token[r] = ctid / K;
+    }
+  }
+  if (ctid < S) {
+    active[ctid] = td[TD_ACT + ctid];
+    if (p.has_shared) row_token[bs * K + ctid] = td[TD_ACT + ctid];
+  }
+  if (p.has_shared && ctid < bs) shared_row[ctid] = td[TD_SROW + ctid];
+  const int st = SlotTable::stride(E);
+  int32_t* b_blk = slots + SlotTable::kHeader + 3 * st;
+  int32_t* g_exp = b_blk + st;
+  if (ctid < ns) {
+    g_exp[ctid] = s_exp[ctid];
+    g_exp[st + ctid] = s_exp[kMaxSmallSlots + ctid];
+    g_exp[2 * st + ctid] = s_exp[2 * kMaxSmallSlots + ctid];
+  }
+  if (ctid == 0) {
+    offsets[E] = R;
+    b_blk[0] = 0;
+    slots[SlotTable::kNumBig] = 0;
+    slots[SlotTable::kBigBlocks] = 0;
+    slots[SlotTable::kRows] = R;
+    slots[SlotTable::kSharedRows] = shared_rows;
+    slots[SlotTable::kNumSmall] = ns;
+    status[kStSkipped] = skipped;
+    status[kStErrorFlags] = 0;
+    status[kStErrorSite] = 0;
+    status[kStRows] = R;
+    status[kStSharedRows] = shared_rows;
+    status[kStSlots] = ns;
+  }
+  for (int b = ctid; b <= G; b += kConsumers) {
+    ranges[b] = small_item_start(td + TD_WP, ns, p.I / (BN / 2), G, b);
+    ranges[kMaxCtas + 1 + b] = small_item_start(td + TD_WP, ns, p.h / BN, G, b);
+  }
+  if (ctid < bs) {
+    int nvalid = 0;
+    for (int k = 0; k < K; ++k) nvalid += td[TD_PE + ctid * K + k] >= 0;
+    ws_ptr<int32_t>(p, p.L.tok_ticket)[ctid] = 0;
+    ws_ptr<int32_t>(p, p.L.tok_expect)[ctid] = nvalid * p.h;
+  }
+}
+
+// The consumers' part of the one-launch prologue after the local dispatch:
+// CTA 0 publishes it, every CTA clears its share of the row-block tickets,
+// CTA (1 + t) mod G quantises token t (and writes the zero rows of tokens
+// that nothing combines into); then the grid barrier, and the `ready`
+// barrier tells this CTA's producer that it may read what other CTAs wrote.
+// false (for every consumer) if the grid barrier gave up.
+__device__ bool publish_and_quant(const FwdParams& p, char* smem) {
+  const int ctid = threadIdx.x;
+  const int G = p.num_ctas, b = blockIdx.x;
+  int32_t* status = ws_ptr<int32_t>(p, p.L.status);
+  float* s_red = reinterpret_cast<float*>(smem + OFF_MISC) + 2;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC);
+  uint64_t* ready = reinterpret_cast<uint64_t*>(smem + OFF_BAR) + 2 * STAGES + 2;
+  if (b == 0) publish_dispatch(p, reinterpret_cast<const int32_t*>(smem + OFF_T));
+  int32_t* blk_ticket = ws_ptr<int32_t>(p, p.L.blk_ticket);
+  const int nt = static_cast<int>(p.L.sizes[kRegBlkTicket] / 4), per = (nt + G - 1) / G;
+  const int i_end = min(nt, (b + 1) * per);
+  for (int i = b * per + ctid; i < i_end; i += kConsumers) blk_ticket[i] = 0;
+  for (int t = 0; t < p.bs; ++t)
+    if ((1 + t) % G == b) quant_token(p, t, s_red, 0);
+  consumer_sync();
+  bool ok = true;
+  if (ctid == 0) {
+    ok = grid_barrier(status + kStBarArrive, status + kStBarRelease, G, status, kKGemm1Small * 16 + 7);
+    if (!ok) *abort_flag = 1;
+    mbar_arrive(ready);
+  }
+  return !consumer_sync_or(!ok);
+}
+
 }  // namespace small_path
 
 constexpr int SMEM_BYTES = small_path::SMEM_BYTES;
@@ -513,10 +825,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_small_kernel(FwdParams p
   grid_launch_dependents();
   constexpr bool G1 = (MODE == kGemm1SwiGLU || MODE == kGemm1Raw);
   small_path::init_rings(smem);
-  small_path::cache_slots<G1>(p, smem);
+  const small_path::SmallRange rg = small_path::global_range<G1>(p);
+  small_path::cache_slots_global<G1>(p, smem, rg);
   __syncthreads();
   small_path::SmallState ss;
-  small_path::run<MODE>(p, raw, smem, ss, false);
+  small_path::run<MODE>(p, raw, smem, ss, false, rg, nullptr);
   if ((threadIdx.x >> 5) == kConsumerWarps)
     small_path::drain_copies(smem, ss, ws_ptr<int32_t>(p, p.L.status), (G1 ? kKGemm1Small : kKGemm2Small) * 16 + 14);
 }
@@ -532,14 +845,41 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_small_streamed_kernel(Fw
   grid_dependency_wait();
   grid_launch_dependents();
   small_path::init_rings(smem);
-  small_path::cache_slots<true>(p, smem);
-  small_path::cache_slots<false>(p, smem);
+  const small_path::SmallRange rg1 = small_path::global_range<true>(p);
+  const small_path::SmallRange rg2 = small_path::global_range<false>(p);
+  small_path::cache_slots_global<true>(p, smem, rg1);
+  small_path::cache_slots_global<false>(p, smem, rg2);
   __syncthreads();
   small_path::SmallState ss;
-  small_path::run<kGemm1SwiGLU>(p, nullptr, smem, ss, false);
-  small_path::run<kGemm2Bf16>(p, nullptr, smem, ss, true);
+  small_path::run<kGemm1SwiGLU>(p, nullptr, smem, ss, false, rg1, nullptr);
+  small_path::run<kGemm2Bf16>(p, nullptr, smem, ss, true, rg2, nullptr);
   if ((threadIdx.x >> 5) == kConsumerWarps)
     small_path::drain_copies(smem, ss, ws_ptr<int32_t>(p, p.L.status), kKGemm1Small * 16 + 14);
+}
+
+// The whole forward of a batch of at most kSmallRows tokens in one launch
+// (num_ctas CTAs, one per SM, all resident): dispatch and quant as above,
+// then GEMM1 -> GEMM2 -> combine streamed as in the streamed kernel.
+__global__ void __launch_bounds__(kThreads, 1) moe_decode_one_launch_kernel(FwdParams p) {
+  extern __shared__ __align__(128) char smem[];
+  // the previous forward may still read the workspace and write the outputs
+  grid_dependency_wait();
+  grid_launch_dependents();
+  small_path::init_rings(smem);
+  __syncthreads();
+  const bool consumer = (threadIdx.x >> 5) < kConsumerWarps;
+  if (consumer) small_path::local_dispatch(p, smem);
+  __syncthreads();
+  const int32_t* rng = reinterpret_cast<const int32_t*>(smem + small_path::OFF_MISC) + small_path::MISC_RANGE;
+  const small_path::SmallRange rg1{rng[0], rng[1], false}, rg2{rng[2], rng[3], false};
+  uint64_t* ready = reinterpret_cast<uint64_t*>(smem + small_path::OFF_BAR) + 2 * small_path::STAGES + 2;
+  const bool go = consumer ? small_path::publish_and_quant(p, smem) : true;
+  small_path::SmallState ss;
+  if (go) {
+    small_path::run<kGemm1SwiGLU>(p, nullptr, smem, ss, false, rg1, ready);
+    small_path::run<kGemm2Bf16>(p, nullptr, smem, ss, true, rg2, ready);
+  }
+  if (!consumer) small_path::drain_copies(smem, ss, ws_ptr<int32_t>(p, p.L.status), kKGemm1Small * 16 + 14);
 }
 
 }  // namespace
@@ -549,7 +889,8 @@ cudaError_t moe_gemm_small_prepare_attributes() {
                        reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm2Bf16>),
                        reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm1Raw>),
                        reinterpret_cast<const void*>(moe_gemm_small_kernel<kGemm2Raw>),
-                       reinterpret_cast<const void*>(moe_gemm_small_streamed_kernel)};
+                       reinterpret_cast<const void*>(moe_gemm_small_streamed_kernel),
+                       reinterpret_cast<const void*>(moe_decode_one_launch_kernel)};
   for (const void* f : fns) {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -575,6 +916,13 @@ cudaError_t launch_moe_gemm_small_streamed(const FwdParams& p, int num_ctas, cud
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(num_ctas), dim3(kThreads), SMEM_BYTES, s, attr);
   return cudaLaunchKernelEx(&cfg, moe_gemm_small_streamed_kernel, p);
+}
+
+cudaError_t launch_moe_decode_one_launch(const FwdParams& p, cudaStream_t s) {
+  if (p.bs == 0) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas), dim3(kThreads), SMEM_BYTES, s, attr);
+  return cudaLaunchKernelEx(&cfg, moe_decode_one_launch_kernel, p);
 }
 
 }  // namespace moe

@@ -16,6 +16,10 @@ enum StatusWord : int {
   kStRows = 3,
   kStSharedRows = 4,
   kStSlots = 5,
+  // grid barrier of the one-launch decode kernel: arrivals of the CTAs other
+  // than CTA 0 (zero between barriers), and the barrier's generation
+  kStBarArrive = 32,
+  kStBarRelease = 33,
 };
 constexpr int kErrWaitTimeout = 1;
 
@@ -188,6 +192,9 @@ cudaError_t launch_combine(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_moe_gemm_small(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);
 // GEMM1 then GEMM2 of the small experts in one launch (GEMM2 streamed behind GEMM1)
 cudaError_t launch_moe_gemm_small_streamed(const FwdParams& p, int num_ctas, cudaStream_t s);
+// the whole forward of a batch of at most small_rows tokens (small_only, token
+// quant) in one launch of num_ctas CTAs: dispatch, quant, GEMM1, GEMM2, combine
+cudaError_t launch_moe_decode_one_launch(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_moe_gemm_big(const FwdParams& p, const TcMaps& maps, int mode, int32_t* raw_acc, int num_ctas,
                                 cudaStream_t s);
 cudaError_t moe_gemm_small_prepare_attributes();

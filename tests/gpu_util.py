@@ -68,8 +68,8 @@ def make_block(wl, dev, bs_max=None, unfused=False, fold_routing=False):
                       expert_smooth=wl.smooth_per_expert)
 
 
-def region(blk, name, dtype, shape=None):
-    t = blk.region(name).view(dtype)
+def region(blk, name, dtype, shape=None, workspace=None):
+    t = blk.region(name, workspace=workspace).view(dtype)
     if shape is not None:
         n = int(np.prod(shape))
         t = t[:n].view(*shape)
