@@ -90,7 +90,7 @@ def kernel_sha(kernel: str) -> str:
     valid for another that differs only in comments."""
     csrc = os.path.join(ROOT, "moe_expert_ffn_dispatch_gb300", "csrc")
     hsh = hashlib.sha256()
-    for name in (KERNEL_SOURCES[kernel], "device_prims.cuh", "epilogue_ops.cuh", "moe_internal.h"):
+    for name in (KERNEL_SOURCES[kernel], "device_prims.cuh", "epilogue_ops.cuh", "moe_internal.h", "quant_ops.cuh"):
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             hsh.update(_code_only(f.read()).encode())
     return hsh.hexdigest()[:16]
@@ -381,6 +381,12 @@ def run_ours(args, wl, ws, rank, local):
     # the small experts' GEMM2 streams behind their GEMM1 in one launch: that
     # launch carries both GEMMs' algorithmic bytes and ops
     streamed_small = ktimes["gemm1_small"][1] > 0 and ktimes["gemm2_small"][1] == 0
+    # a batch of at most 8 tokens: the gemm1_small launch is the whole forward
+    # (dispatch and quant included; its bytes and ops are the forward's)
+    one_launch = streamed_small and ktimes["dispatch_quant"][1] == 0
+    if one_launch:
+        # x in, ids and routing weights in, expert_token_nums out
+        alg["gemm1_small"] += wl.bs * wl.hidden * 2 + wl.bs * wl.topk * 8 + wl.num_experts * 4
     if streamed_small:
         alg["gemm1_small"] += alg["gemm2_small"]
         alg["ops"]["gemm1_small"] += alg["ops"]["gemm2_small"]
@@ -494,7 +500,7 @@ def run_ours(args, wl, ws, rank, local):
         "config": {**workload_config(wl, alg, ws), **({"unfused": True} if getattr(args, "unfused", False) else {}),
                    **({"fold_routing": True} if getattr(args, "fold_routing", False) else {})},
         "roofline": {**roof, "traffic": traffic, "kernel": dom, "peak_kind": peak_kind,
-                     "streamed_small_gemm2": streamed_small,
+                     "streamed_small_gemm2": streamed_small, "one_launch_forward": one_launch,
                      "alg_bytes_per_launch": alg[dom], "int_ops_per_launch": alg["ops"][dom],
                      "avg_launch_us": d_avg_s * 1e6,
                      "timing": "CUDA events around each launch, second pass of the same %d forwards "

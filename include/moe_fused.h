@@ -175,6 +175,14 @@ int moe_fused_workspace_size(const moe_fused_config_t* cfg, size_t* workspace_by
 /* Enqueue one forward of the block on `stream`.  `workspace` must hold at least
  * the reported bytes; its contents need no initialisation and are overwritten.
  * Two forwards that share a workspace must be ordered on the GPU.
+ * A batch of at most 8 tokens (without MOE_FLAG_EXPERT_SMOOTH smooth scales,
+ * and unless MOE_FLAG_UNFUSED is set) runs as one launch whose CTAs meet at
+ * one grid barrier; its arrival count lives in the workspace (status word 32,
+ * word 33 its generation).  The handle zeroes that count, with one enqueued
+ * 4-byte memset, the first time it runs such a forward on a workspace (and
+ * again after moe_fused_get_status reported a wait that gave up); the kernel
+ * leaves it at zero.  So the caller must not write a workspace's first 256
+ * bytes (the status words) between forwards; the rest may be reused freely.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE (bs > bs_max), WORKSPACE_TOO_SMALL,
  * ALIGNMENT, CUDA (launch failure). */
 int moe_fused_forward(moe_fused_handle_t* handle, const moe_fused_args_t* args, void* workspace,
