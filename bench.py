@@ -378,6 +378,11 @@ def run_ours(args, wl, ws, rank, local):
     torch.cuda.synchronize()
     ms_instrumented = e2.elapsed_time(e3)
     ktimes = blk.get_timing()
+    # how the last forward split the CTAs between the two GEMM engines
+    hdr = blk.region("slots")[:32].view(torch.int32).cpu().tolist()
+    n_ctas = min(torch.cuda.get_device_properties(dev).multi_processor_count, 1023)
+    engines = {"side_by_side": bool(hdr[6]), "small_phase_ctas": hdr[5],
+               "tensor_core_ctas": (n_ctas - hdr[5]) if hdr[6] else n_ctas}
     # the small experts' GEMM2 streams behind their GEMM1 in one launch: that
     # launch carries both GEMMs' algorithmic bytes and ops
     streamed_small = ktimes["gemm1_small"][1] > 0 and ktimes["gemm2_small"][1] == 0
@@ -510,6 +515,7 @@ def run_ours(args, wl, ws, rank, local):
         "per_forward_us": {**per_fwd, "timing": "CUDA events around each forward, third pass of the same %d "
                                                "forwards" % args.steps},
         "kernels_us": {k: (v[0] / max(v[1], 1) * 1e3) for k, v in ktimes.items()},
+        "engines": engines,
         "gpu_launches": launches,
         "e2e": {"value": whole_job_tokens_per_s(wl.bs, ws, e2e_steps, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d,

@@ -39,9 +39,15 @@ struct moe_fused_handle {
   moe::TcMaps maps;          // tensor maps of the last forward's operands
   const void* map_key[5];    // pointers they were built for
   bool maps_valid;
-  // workspaces whose grid-barrier arrival count (one-launch decode kernel)
-  // this handle has zeroed; the kernel leaves it at zero after every barrier
+  // workspaces whose cross-launch counters (the one-launch kernel's grid
+  // barrier, the arrival counters of side-by-side engines: status words
+  // 32..47) this handle has zeroed; the kernels leave them at zero
   std::vector<const void*> barrier_ready;
+  // engines side by side: the tensor-core chain's stream, and the events of
+  // the fork (after expand), of the tensor-core GEMM1's launch completion
+  // (every CTA begun) and of the join (before the combine)
+  cudaStream_t side;
+  cudaEvent_t ev_fork, ev_started, ev_join;
 };
 
 namespace {
@@ -328,13 +334,19 @@ int moe_fused_create(const moe_fused_config_t* cfg, moe_fused_handle_t** out_han
   hd->cfg = *cfg;
   hd->timing = false;
   hd->maps_valid = false;
+  hd->side = nullptr;
+  hd->ev_fork = hd->ev_started = hd->ev_join = nullptr;
   cudaError_t e = cudaGetDevice(&hd->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&hd->num_sms, cudaDevAttrMultiProcessorCount, hd->device);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hd->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hd->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hd->ev_started, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hd->ev_join, cudaEventDisableTiming);
   if (e == cudaSuccess) e = moe::moe_gemm_small_prepare_attributes();
   if (e == cudaSuccess) e = moe::moe_gemm_big_prepare_attributes();
   if (e == cudaSuccess) e = moe::dispatch_prepare_attributes(1024);
   if (e != cudaSuccess) {
-    delete hd;
+    moe_fused_destroy(hd);
     return cuda_fail(e);
   }
   hd->L = plan(*cfg);
@@ -373,18 +385,26 @@ int moe_fused_debug_forward_range(moe_fused_handle_t* hd, const moe_fused_args_t
   // be zero before the workspace's first such forward; the kernel leaves it
   // at zero.  After a wait that gave up it may not be: get_status, which
   // reports that, makes the next forward zero it again.
-  if (p.small_only && !p.xq_per_row && first_kernel == moe::kKDispatchQuant && last_kernel >= moe::kKGemm2Small) {
+  const bool one_launch =
+      p.small_only && !p.xq_per_row && first_kernel == moe::kKDispatchQuant && last_kernel >= moe::kKGemm2Small;
+  // A whole forward of a larger batch on the fused path runs the dp4a launch
+  // and the tensor-core chain side by side (below); the dispatch splits the
+  // CTAs between them.
+  p.split_engines = p.small_rows > 0 && !p.small_only && first_kernel == moe::kKDispatchQuant &&
+                    last_kernel == moe::kKCombine;
+  if (one_launch || p.split_engines) {
     auto& known = hd->barrier_ready;
     bool seen = false;
     for (const void* w : known) seen = seen || (w == workspace);
     if (!seen) {
-      e = cudaMemsetAsync(p.ws + p.L.status + sizeof(int32_t) * moe::kStBarArrive, 0, sizeof(int32_t), s);
+      e = cudaMemsetAsync(p.ws + p.L.status + sizeof(int32_t) * moe::kStBarArrive, 0, 16 * sizeof(int32_t), s);
       if (e != cudaSuccess) return cuda_fail(e);
       if (known.size() >= 64) known.erase(known.begin());
       known.push_back(workspace);
     }
-    return cuda_fail(timed(hd, moe::kKGemm1Small, s, [&] { return moe::launch_moe_decode_one_launch(p, s); }));
   }
+  if (one_launch)
+    return cuda_fail(timed(hd, moe::kKGemm1Small, s, [&] { return moe::launch_moe_decode_one_launch(p, s); }));
   rc = prepare_maps(hd, p);
   if (rc) return rc;
   const int sms = p.num_ctas;
@@ -409,6 +429,45 @@ int moe_fused_debug_forward_range(moe_fused_handle_t* hd, const moe_fused_args_t
       default: return moe::launch_combine(p, s);
     }
   };
+  if (p.split_engines) {
+    // Stream s: dispatch (+ finish) and expand.  Side stream: the tensor-core
+    // GEMM1, the requant, GEMM2.  Stream s again, once every CTA of the
+    // tensor-core GEMM1 has begun (so that its CTAs hold their SMs before the
+    // dp4a launch fills the rest): the dp4a launch; then, after the side
+    // stream, the combine.  Neither the tensor-core GEMM1 nor the requant
+    // starts early behind its predecessor: CTAs waiting for a predecessor
+    // would hold SMs that the other engine's CTAs need.
+    e = cudaSuccess;
+    for (int k = moe::kKDispatchQuant; k <= moe::kKExpand && e == cudaSuccess; ++k) {
+      if (k == moe::kKDispatchFinish && p.disp_chunks <= 1) continue;
+      e = timed(hd, k, s, [&] { return run(k); });
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(hd->ev_fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hd->side, hd->ev_fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    moe::LaunchOpts first_big;
+    first_big.pdl = false;
+    first_big.started = hd->ev_started;
+    moe::LaunchOpts no_pdl;
+    no_pdl.pdl = false;
+    e = timed(hd, moe::kKGemm1Big, hd->side, [&] {
+      return moe::launch_moe_gemm_big(p, maps, moe::kGemm1SwiGLU, nullptr, sms, hd->side, first_big);
+    });
+    if (e == cudaSuccess)
+      e = timed(hd, moe::kKRequantBig, hd->side, [&] { return moe::launch_requant_big(p, hd->side, no_pdl); });
+    if (e == cudaSuccess)
+      e = timed(hd, moe::kKGemm2Big, hd->side,
+                [&] { return moe::launch_moe_gemm_big(p, maps, moe::kGemm2Bf16, nullptr, sms, hd->side); });
+    // the side stream always rejoins s (a capture must not be left forked)
+    const cudaError_t ej = cudaEventRecord(hd->ev_join, hd->side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hd->ev_started, 0);
+    if (e == cudaSuccess)
+      e = timed(hd, moe::kKGemm1Small, s, [&] { return moe::launch_moe_gemm_small_streamed(p, sms, s, no_pdl); });
+    const cudaError_t ew = ej == cudaSuccess ? cudaStreamWaitEvent(s, hd->ev_join, 0) : ej;
+    if (e == cudaSuccess) e = ew;
+    if (e == cudaSuccess) e = timed(hd, moe::kKCombine, s, [&] { return run(moe::kKCombine); });
+    return cuda_fail(e);
+  }
   e = cudaSuccess;
   for (int k = first_kernel; k <= last_kernel && e == cudaSuccess; ++k) {
     if (k == moe::kKDispatchFinish && p.disp_chunks <= 1) continue;  // one-CTA dispatch: nothing to launch
@@ -460,6 +519,9 @@ int moe_fused_destroy(moe_fused_handle_t* hd) {
     cudaEventDestroy(r.stop);
   }
   for (auto e : hd->pool) cudaEventDestroy(e);
+  for (cudaEvent_t e : {hd->ev_fork, hd->ev_started, hd->ev_join})
+    if (e) cudaEventDestroy(e);
+  if (hd->side) cudaStreamDestroy(hd->side);
   delete hd;
   return MOE_OK;
 }

@@ -263,6 +263,21 @@ __device__ __forceinline__ bool grid_barrier(int32_t* arrive, int32_t* release, 
   return true;
 }
 
+// Logical index of this CTA in a launch whose CTAs take their work in
+// arrival order: the i-th CTA to get here gets i.  *counter is zero before
+// the launch; the last CTA to arrive (every CTA of the grid calls this once)
+// puts it back to zero.  Called by every thread of the CTA after the
+// launch's grid-dependency wait; s_lid: one int of shared memory.
+__device__ __forceinline__ int arrival_index(int32_t* counter, int* s_lid) {
+  if (threadIdx.x == 0) {
+    const int i = atomicAdd(counter, 1);
+    if (i == static_cast<int>(gridDim.x) - 1) atomicExch(counter, 0);
+    *s_lid = i;
+  }
+  __syncthreads();
+  return *s_lid;
+}
+
 // true in exactly one lane of the (converged) warp: lets a warp run a loop
 // with warp-uniform values while a single lane issues TMA / tcgen05 work
 __device__ __forceinline__ bool elect_one() {

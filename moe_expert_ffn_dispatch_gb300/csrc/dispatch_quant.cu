@@ -139,6 +139,41 @@ __device__ void rank_range(const FwdParams& p, int32_t* running, int32_t* wcnt, 
   __syncthreads();
 }
 
+// Engines side by side: how many of the num_ctas CTAs the small phase (the
+// dp4a launch) gets when the tensor-core chain (GEMM1, requant, GEMM2 of the
+// big blocks) runs at the same time on the others.  Each side's time is its
+// weight bytes over its CTAs' streaming rate, plus a fixed cost on the
+// tensor-core side (the requant between its GEMMs, launch gaps); the split
+// minimises the larger of the two.  Rates per CTA, measured with the engines
+// side by side on the decode workloads: dp4a 43 GB/s, the tensor-core chain
+// 29 GB/s, fixed cost 15 us.  Every small slot and every big token block
+// streams one expert's weights (3 h I bytes).  With ts, tb the two sides'
+// CTA-us and F the fixed cost, the sides meet where ts / g = F + tb / (G - g),
+// the smaller root of F g^2 - (F G + ts + tb) g + ts G = 0; the better of
+// the two integers around it is taken.  0 when there is no small work,
+// num_ctas when there is no big work.
+__device__ int small_phase_ctas(const FwdParams& p, int n_small, int big_blocks) {
+  const int G = p.num_ctas;
+  if (n_small == 0) return 0;
+  if (big_blocks == 0 || G < 2) return G;
+  constexpr float kRateSmall = 43e3f, kRateBig = 29e3f;  // bytes per us per CTA
+  constexpr float kFixedBig = 15.0f;                      // us
+  const float wb = 3.0f * static_cast<float>(p.h) * static_cast<float>(p.I);
+  const float ts = static_cast<float>(n_small) * wb / kRateSmall;
+  const float tb = static_cast<float>(big_blocks) * wb / kRateBig;
+  const float g = static_cast<float>(G);
+  const float b = kFixedBig * g + ts + tb;
+  const float disc = fmaxf(b * b - 4.0f * kFixedBig * ts * g, 0.0f);
+  const float root = (b - sqrtf(disc)) / (2.0f * kFixedBig);
+  int lo = static_cast<int>(floorf(root));
+  lo = lo < 1 ? 1 : lo > G - 1 ? G - 1 : lo;
+  const int hi = lo + 1 < G ? lo + 1 : lo;
+  auto t_of = [&](int gs) {
+    return fmaxf(ts / static_cast<float>(gs), kFixedBig + tb / static_cast<float>(G - gs));
+  };
+  return t_of(hi) < t_of(lo) ? hi : lo;
+}
+
 // Everything after the rows are placed, by one CTA: counts, offsets and
 // expert_token_nums; the active-token list and shared rows; the slot tables;
 // the status words; the small-phase item ranges and the per-forward ticket
@@ -242,6 +277,8 @@ __device__ void dispatch_tail(const FwdParams& p, int32_t* dsm, int c, int off, 
     slots[SlotTable::kRows] = R;
     slots[SlotTable::kSharedRows] = shared_rows;
     slots[SlotTable::kNumSmall] = n_small;
+    slots[SlotTable::kSmallCtas] = p.split_engines ? small_phase_ctas(p, n_small, big_blk) : p.num_ctas;
+    slots[SlotTable::kSplit] = p.split_engines ? 1 : 0;
     status[kStSkipped] = s_skipped;
     status[kStErrorFlags] = 0;
     status[kStErrorSite] = 0;
@@ -269,7 +306,7 @@ __device__ void dispatch_tail(const FwdParams& p, int32_t* dsm, int c, int off, 
       carry += tot;
     }
     __syncthreads();
-    const int G = p.num_ctas;
+    const int G = slots[SlotTable::kSmallCtas];  // written by thread 0 above
     int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges);
     for (int g = 0; g < 2; ++g) {
       const int J = g == 0 ? p.I / 16 : p.h / 32;   // items per small slot, GEMM1 / GEMM2
@@ -480,14 +517,14 @@ cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s) {
   const int nd = p.disp_chunks > 1 ? p.disp_chunks : 1;
   const int qblocks = (p.bs + kQuantGroups - 1) / kQuantGroups;
   const int blocks = nd + (qblocks < 2 * p.num_ctas ? qblocks : 2 * p.num_ctas);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pdl_config(dim3(blocks), dim3(kDispatchThreads), dispatch_smem_bytes(p.E), s, attr);
   return cudaLaunchKernelEx(&cfg, dispatch_quant_kernel, p);
 }
 
 cudaError_t launch_dispatch_finish(const FwdParams& p, cudaStream_t s) {
   if (p.bs == 0 || p.disp_chunks <= 1) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg =
       pdl_config(dim3(p.disp_chunks), dim3(kDispatchThreads), dispatch_smem_bytes(p.E), s, attr);
   return cudaLaunchKernelEx(&cfg, dispatch_finish_kernel, p);

@@ -62,9 +62,10 @@ constexpr int kNumBars = 2 * STAGES + 3;                        // full, empty [
 constexpr int OFF_BAR = OFF_Y + 2 * BN * MT * 4;
 constexpr int OFF_INFO = OFF_BAR + kNumBars * 8;                // kInfoSlots x {scale, row, token}[MT]
 constexpr int OFF_SLOT = OFF_INFO + kInfoSlots * 3 * MT * 4;    // 2 x kSlotCache x {e, row0, rows}: GEMM1, GEMM2
-constexpr int OFF_MISC = OFF_SLOT + 2 * kSlotCache * 3 * 4;     // abort, flag, red[8], tok[MT], range[4]
+constexpr int OFF_MISC = OFF_SLOT + 2 * kSlotCache * 3 * 4;     // abort, flag, red[8], tok[MT], range[4], lid
 constexpr int MISC_RANGE = 2 + kConsumerWarps + MT;             // item range {begin, end} of GEMM1, GEMM2
-constexpr int SMEM_BYTES = OFF_MISC + (MISC_RANGE + 4) * 4;
+constexpr int MISC_LID = MISC_RANGE + 4;                        // this CTA's index in arrival order
+constexpr int SMEM_BYTES = OFF_MISC + (MISC_LID + 1) * 4;
 static_assert(kRowsPerWarp * MT == 32, "one reduced value per lane");
 static_assert(kInfoSlots > STAGES, "info ring must outlive the stage ring");
 
@@ -182,12 +183,26 @@ struct SmallRange {
   bool has_big;
 };
 
-// The range as the dispatch kernel left it in the workspace.
+// The range of CTA `cta` as the dispatch kernel left it in the workspace.
 template <bool G1>
-__device__ __forceinline__ SmallRange global_range(const FwdParams& p) {
+__device__ __forceinline__ SmallRange global_range(const FwdParams& p, int cta) {
   const int32_t* ranges = ws_ptr<int32_t>(p, p.L.ranges) + (G1 ? 0 : kMaxCtas + 1);
   const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
-  return SmallRange{ranges[blockIdx.x], ranges[blockIdx.x + 1], slots[SlotTable::kBigBlocks] > 0};
+  return SmallRange{ranges[cta], ranges[cta + 1], slots[SlotTable::kBigBlocks] > 0};
+}
+
+// This CTA's index among the small phase's CTAs, or -1 if the phase has no
+// work for it: blockIdx.x, or, with the engines side by side (the tensor-core
+// chain holding some SMs), the CTA's place in arrival order, so that the
+// CTAs that work are the ones that got an SM first (the streamed GEMM2 waits
+// on other CTAs' GEMM1 work).  Called by every thread.
+__device__ __forceinline__ int small_cta(const FwdParams& p, char* smem) {
+  const int32_t* slots = ws_ptr<int32_t>(p, p.L.slots);
+  int lid = blockIdx.x;
+  if (slots[SlotTable::kSplit])
+    lid = arrival_index(ws_ptr<int32_t>(p, p.L.status) + kStCtaCounter,
+                        reinterpret_cast<int*>(smem + OFF_MISC) + MISC_LID);
+  return lid < slots[SlotTable::kSmallCtas] ? lid : -1;
 }
 
 __device__ __forceinline__ void init_rings(char* smem) {
@@ -763,6 +778,8 @@ __device__ void publish_dispatch(const FwdParams& p, const int32_t* td) {
     slots[SlotTable::kRows] = R;
     slots[SlotTable::kSharedRows] = shared_rows;
     slots[SlotTable::kNumSmall] = ns;
+    slots[SlotTable::kSmallCtas] = G;
+    slots[SlotTable::kSplit] = 0;
     status[kStSkipped] = skipped;
     status[kStErrorFlags] = 0;
     status[kStErrorSite] = 0;
@@ -824,8 +841,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_small_kernel(FwdParams p
   grid_dependency_wait();
   grid_launch_dependents();
   constexpr bool G1 = (MODE == kGemm1SwiGLU || MODE == kGemm1Raw);
+  const int cta = small_path::small_cta(p, smem);
+  if (cta < 0) return;
   small_path::init_rings(smem);
-  const small_path::SmallRange rg = small_path::global_range<G1>(p);
+  const small_path::SmallRange rg = small_path::global_range<G1>(p, cta);
   small_path::cache_slots_global<G1>(p, smem, rg);
   __syncthreads();
   small_path::SmallState ss;
@@ -844,9 +863,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_gemm_small_streamed_kernel(Fw
   extern __shared__ __align__(128) char smem[];
   grid_dependency_wait();
   grid_launch_dependents();
+  const int cta = small_path::small_cta(p, smem);
+  if (cta < 0) return;
   small_path::init_rings(smem);
-  const small_path::SmallRange rg1 = small_path::global_range<true>(p);
-  const small_path::SmallRange rg2 = small_path::global_range<false>(p);
+  const small_path::SmallRange rg1 = small_path::global_range<true>(p, cta);
+  const small_path::SmallRange rg2 = small_path::global_range<false>(p, cta);
   small_path::cache_slots_global<true>(p, smem, rg1);
   small_path::cache_slots_global<false>(p, smem, rg2);
   __syncthreads();
@@ -900,7 +921,7 @@ cudaError_t moe_gemm_small_prepare_attributes() {
 
 cudaError_t launch_moe_gemm_small(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pdl_config(dim3(num_ctas), dim3(kThreads), SMEM_BYTES, s, attr);
   switch (mode) {
     case kGemm1SwiGLU: return cudaLaunchKernelEx(&cfg, moe_gemm_small_kernel<kGemm1SwiGLU>, p, raw_acc);
@@ -911,16 +932,16 @@ cudaError_t launch_moe_gemm_small(const FwdParams& p, int mode, int32_t* raw_acc
   }
 }
 
-cudaError_t launch_moe_gemm_small_streamed(const FwdParams& p, int num_ctas, cudaStream_t s) {
+cudaError_t launch_moe_gemm_small_streamed(const FwdParams& p, int num_ctas, cudaStream_t s, const LaunchOpts& o) {
   if (p.bs == 0) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(num_ctas), dim3(kThreads), SMEM_BYTES, s, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_config(dim3(num_ctas), dim3(kThreads), SMEM_BYTES, s, attr, o);
   return cudaLaunchKernelEx(&cfg, moe_gemm_small_streamed_kernel, p);
 }
 
 cudaError_t launch_moe_decode_one_launch(const FwdParams& p, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas), dim3(kThreads), SMEM_BYTES, s, attr);
   return cudaLaunchKernelEx(&cfg, moe_decode_one_launch_kernel, p);
 }

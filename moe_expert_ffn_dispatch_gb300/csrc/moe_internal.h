@@ -20,6 +20,10 @@ enum StatusWord : int {
   // than CTA 0 (zero between barriers), and the barrier's generation
   kStBarArrive = 32,
   kStBarRelease = 33,
+  // arrival counters of the GEMM launches whose CTAs take their work in
+  // arrival order (engines side by side): small, big GEMM1, big GEMM2; zero
+  // between launches
+  kStCtaCounter = 40,
 };
 constexpr int kErrWaitTimeout = 1;
 
@@ -76,7 +80,10 @@ constexpr int kMaxCtas = 1023;  // persistent grid size limit (one CTA per SM)
 // it more rows takes several small slots of at most kSmallRows rows (see
 // FwdParams::small_only).  Stored as int32 words at layout.slots:
 //   header: [0] n_big  [1] token blocks over big slots  [2] R  [3] S
-//           [4] n_small  [5..7] reserved
+//           [4] n_small  [5] CTAs of the small phase (the item ranges are
+//           split over these)  [6] engines side by side (the GEMM launches'
+//           CTAs take their work in arrival order; the big launches use the
+//           num_ctas - [5] CTAs the small phase leaves)  [7] reserved
 //   then seven arrays of stride (E + 2 + kSplitSlots):
 //     big:   expert id, first row, row count, exclusive prefix of blocks
 //     small: expert id, first row, row count
@@ -88,6 +95,7 @@ constexpr int kSplitSlots = kMaxTopk;
 struct SlotTable {
   static constexpr int kHeader = 8;
   static constexpr int kNumBig = 0, kBigBlocks = 1, kRows = 2, kSharedRows = 3, kNumSmall = 4;
+  static constexpr int kSmallCtas = 5, kSplit = 6;
   static __host__ __device__ int stride(int E) { return E + 2 + kSplitSlots; }
   static __host__ __device__ int words(int E) { return kHeader + 7 * stride(E); }
 };
@@ -109,6 +117,8 @@ struct FwdParams {
                           // more rows, from repeated ids, in slots of at most small_rows rows), so
                           // no big block exists and the tensor-core launches are skipped
   int32_t num_ctas;       // grid of the GEMM launches (<= kMaxCtas)
+  int32_t split_engines;  // the dp4a launch and the tensor-core chain run side by side on disjoint CTA
+                          // sets, split by the dispatch (slot table words 5 and 6)
   int32_t act_fp16;       // x, y2 and the outputs are fp16 (else bf16)
   int32_t scale_dtype;    // routed weight scales: 0 fp32, 1 bf16, 2 fp16
   int32_t xq_per_row;     // per-expert smooth: routed x_q / x_scale are indexed by row, not token
@@ -167,19 +177,42 @@ struct alignas(64) TcMaps {
 // GEMM modes
 enum GemmMode : int { kGemm1SwiGLU = 0, kGemm2Bf16 = 1, kGemm1Raw = 2, kGemm2Raw = 3 };
 
-// Launch attributes shared by the forward's kernels: programmatic stream
-// serialisation (each kernel waits on its predecessor in-kernel).
-inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr) {
+// How a launch joins its stream: programmatic stream serialisation (the
+// kernel may start while its predecessor drains and waits for it in-kernel;
+// the default), and optionally an event recorded once every CTA of the launch
+// has begun (launch completion).
+struct LaunchOpts {
+  bool pdl = true;
+  cudaEvent_t started = nullptr;
+};
+
+inline cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr,
+                                        const LaunchOpts& o) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  unsigned n = 0;
+  if (o.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (o.started) {
+    attr[n].id = cudaLaunchAttributeLaunchCompletionEvent;
+    attr[n].val.launchCompletionEvent.event = o.started;
+    attr[n].val.launchCompletionEvent.flags = 0;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   return cfg;
+}
+
+// The default: programmatic stream serialisation only.  attr: 2 entries.
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr) {
+  return launch_config(grid, block, smem, s, attr, LaunchOpts());
 }
 
 // ---------------------------------------------------------------- launches
@@ -187,16 +220,17 @@ size_t dispatch_smem_bytes(int E);
 cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_expand(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_dispatch_finish(const FwdParams& p, cudaStream_t s);
-cudaError_t launch_requant_big(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_requant_big(const FwdParams& p, cudaStream_t s, const LaunchOpts& o = LaunchOpts());
 cudaError_t launch_combine(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_moe_gemm_small(const FwdParams& p, int mode, int32_t* raw_acc, int num_ctas, cudaStream_t s);
 // GEMM1 then GEMM2 of the small experts in one launch (GEMM2 streamed behind GEMM1)
-cudaError_t launch_moe_gemm_small_streamed(const FwdParams& p, int num_ctas, cudaStream_t s);
+cudaError_t launch_moe_gemm_small_streamed(const FwdParams& p, int num_ctas, cudaStream_t s,
+                                           const LaunchOpts& o = LaunchOpts());
 // the whole forward of a batch of at most small_rows tokens (small_only, token
 // quant) in one launch of num_ctas CTAs: dispatch, quant, GEMM1, GEMM2, combine
 cudaError_t launch_moe_decode_one_launch(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_moe_gemm_big(const FwdParams& p, const TcMaps& maps, int mode, int32_t* raw_acc, int num_ctas,
-                                cudaStream_t s);
+                                cudaStream_t s, const LaunchOpts& o = LaunchOpts());
 cudaError_t moe_gemm_small_prepare_attributes();
 cudaError_t moe_gemm_big_prepare_attributes();
 cudaError_t dispatch_prepare_attributes(int E);

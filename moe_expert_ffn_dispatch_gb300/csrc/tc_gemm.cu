@@ -94,7 +94,7 @@ constexpr int OFF_BAR = OFF_A8 + S8 * A8_BYTES;
 constexpr int NBAR = 2 * S8 + 2 * SA + 2 * SB + 4 + 2 * SI + 1;
 constexpr int OFF_INFO = OFF_BAR + NBAR * 8;         // tok_scale, tok_row, tok_tok [TB]
 constexpr int OFF_ITEM = OFF_INFO + 3 * TB * 4;      // SI decoded items, 8 ints each
-constexpr int OFF_MISC = OFF_ITEM + SI * 8 * 4;      // tmem slot, abort flag
+constexpr int OFF_MISC = OFF_ITEM + SI * 8 * 4;      // tmem slot, abort flag, arrival index
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 constexpr int kItemReaders = 4;                      // weight TMA, token TMA, MMA, epilogue
 static_assert(KB == 128 && KA == 64, "the MMA loop issues two atoms of four K16 steps per stage");
@@ -243,7 +243,16 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   const int site = (G1 ? kKGemm1Big : kKGemm2Big) * 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (total <= blockIdx.x) return;  // uniform: no item for this CTA (before any barrier or allocation)
+  // This CTA's first item and the item stride: blockIdx.x and gridDim.x, or,
+  // with the engines side by side (the dp4a launch holding the other SMs),
+  // the CTA's place in arrival order among the num_ctas - (small-phase CTAs)
+  // that work, so that those are the ones that got an SM.
+  long cta0 = blockIdx.x, ncta = gridDim.x;
+  if (slots[SlotTable::kSplit]) {
+    cta0 = arrival_index(status + kStCtaCounter + (G1 ? 1 : 2), reinterpret_cast<int*>(smem + OFF_MISC) + 2);
+    ncta = p.num_ctas - slots[SlotTable::kSmallCtas];
+  }
+  if (total <= cta0 || cta0 >= ncta) return;  // uniform: no item for this CTA (before any barrier or allocation)
 
   if (threadIdx.x == 0) {
     if ((smem_u32(smem) & 1023u) != 0) report_timeout(status, site + 15);  // swizzle alignment broken
@@ -280,14 +289,14 @@ __global__ void __launch_bounds__(kBigThreads, 1)
   // The single-issuer roles (the two TMA producers and the MMA issuer) run
   // their loops on the whole warp, so every address and descriptor is
   // warp-uniform; one elected lane issues the copies and tensor-core work.
-  // Every role walks the same item sequence (blockIdx.x, + gridDim.x, ...)
+  // Every role walks the same item sequence (cta0, + ncta, ...)
   // and takes each item's decoded form from the scheduler's ring.
   int si = 0;
   uint32_t pi = 0;
   if (aligned && warp == kWarpSched) {
     // ------------------------------------------------------- item scheduler
     bool wrapped = false;
-    for (long it = blockIdx.x; it < total; it += gridDim.x) {
+    for (long it = cta0; it < total; it += ncta) {
       const BigItem x = decode_item(it, J, slots, p.E);
       if (wrapped &&
           !__all_sync(0xffffffffu, mbar_wait_bounded(&it_empty[si], pi ^ 1u, abort_flag, status, site + 9, false)))
@@ -304,7 +313,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     bool wrapped = false;
-    for (long it = blockIdx.x; it < total; it += gridDim.x) {
+    for (long it = cta0; it < total; it += ncta) {
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(&it_full[si], pi, abort_flag, status, site + 10))) goto done_a;
       const BigItem x = get_item(items + 8 * si);
       __syncwarp();
@@ -343,7 +352,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     bool wrapped = false;
-    for (long it = blockIdx.x; it < total; it += gridDim.x) {
+    for (long it = cta0; it < total; it += ncta) {
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(&it_full[si], pi, abort_flag, status, site + 10))) goto done_b;
       const BigItem x = get_item(items + 8 * si);
       __syncwarp();
@@ -409,7 +418,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     for (int o = 16; o > 0; o >>= 1) rows_sum += __shfl_xor_sync(0xffffffffu, rows_sum, o);
     const bool pipelined = rows_sum <= 64 * slots[SlotTable::kBigBlocks];
     if (pipelined) {
-      const long n_items = (total - blockIdx.x + gridDim.x - 1) / gridDim.x;
+      const long n_items = (total - cta0 + ncta - 1) / ncta;
       const long n_stages = n_items * n_kb;
       int s8 = 0, sa = 0;
       uint32_t p8 = 0, pa = 0;
@@ -457,7 +466,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       uint32_t p8 = 0, pa = 0;
       bool wrapped = false;
       bool ok = true;
-      for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      for (long it = cta0; it < total && ok; it += ncta) {
         for (int kb = 0; kb < n_kb; ++kb) {
           ok = __all_sync(0xffffffffu, mbar_wait_bounded(&a8_full[s8], p8, abort_flag, status, site + 3));
           if (ok && wrapped)
@@ -514,7 +523,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
       uint32_t pa = 0, pb = 0;
       long acc_n = 0;
       bool ok = true;
-      for (long it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      for (long it = cta0; it < total && ok; it += ncta) {
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&it_full[si], pi, abort_flag, status, site + 10))) break;
         const int mblk = items[8 * si + 6];
         __syncwarp();
@@ -594,7 +603,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
     int32_t* amax2 = ws_ptr<int32_t>(p, p.L.amax2);
     uint16_t* y2 = ws_ptr<uint16_t>(p, p.L.y2);
     long acc_n = 0;
-    for (long it = blockIdx.x; it < total && aligned; it += gridDim.x) {
+    for (long it = cta0; it < total && aligned; it += ncta) {
       const bool got = mbar_wait_bounded(&it_full[si], pi, abort_flag, status, site + 10);
       const BigItem x = get_item(items + 8 * si);
       // the previous item's epilogue is done with the token info, and every
@@ -1010,17 +1019,17 @@ __global__ void __launch_bounds__(256, 4) combine_kernel(FwdParams p) {
 
 }  // namespace
 
-cudaError_t launch_requant_big(const FwdParams& p, cudaStream_t s) {
+cudaError_t launch_requant_big(const FwdParams& p, cudaStream_t s, const LaunchOpts& o) {
   if (p.bs == 0) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   const size_t smem = big_slots_smem_bytes(p.E);
-  cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 4), dim3(kRqWarps * 32), smem, s, attr);
+  cudaLaunchConfig_t cfg = launch_config(dim3(p.num_ctas * 4), dim3(kRqWarps * 32), smem, s, attr, o);
   return cudaLaunchKernelEx(&cfg, requant_big_kernel, p);
 }
 
 cudaError_t launch_combine(const FwdParams& p, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 4), dim3(256), 0, s, attr);
   return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
@@ -1040,16 +1049,16 @@ cudaError_t moe_gemm_big_prepare_attributes() {
 
 cudaError_t launch_expand(const FwdParams& p, cudaStream_t s) {
   if (p.bs == 0) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pdl_config(dim3(p.num_ctas * 4), dim3(256), big_slots_smem_bytes(p.E), s, attr);
   return cudaLaunchKernelEx(&cfg, expand_kernel, p);
 }
 
 cudaError_t launch_moe_gemm_big(const FwdParams& p, const TcMaps& maps, int mode, int32_t* raw_acc, int num_ctas,
-                                cudaStream_t s) {
+                                cudaStream_t s, const LaunchOpts& o) {
   if (p.bs == 0) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(num_ctas), dim3(kBigThreads), SMEM_BYTES, s, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_config(dim3(num_ctas), dim3(kBigThreads), SMEM_BYTES, s, attr, o);
   switch (mode) {
     case kGemm1SwiGLU: return cudaLaunchKernelEx(&cfg, moe_gemm_big_kernel<kGemm1SwiGLU>, maps, p, raw_acc);
     case kGemm2Bf16: return cudaLaunchKernelEx(&cfg, moe_gemm_big_kernel<kGemm2Bf16>, maps, p, raw_acc);
