@@ -480,8 +480,14 @@ def run_ours(args, wl, ws, rank, local):
     e2e_s = max_over_ranks(t1 - t0, dev)
 
     peaks, peak_kind = measured_peaks()
-    # dominant kernel: the GEMM kernel with the most time in the timed region
-    dom = max(KERNEL_SOURCES, key=lambda k: ktimes[k][0])
+    # dominant kernel: the GEMM kernel with the most work, i.e. the largest
+    # roofline time max(bytes / HBM rate, ops / tensor rate) (with the engines
+    # side by side, launch durations overlap and no longer rank the kernels)
+    def ideal_s(k):
+        return max(alg[k] / (peaks["hbm_gbs"] * 1e9), alg["ops"][k] / (peaks["bf16_tflops"] * 1e12))
+
+    launched = [k for k in KERNEL_SOURCES if ktimes[k][1] > 0] or list(KERNEL_SOURCES)
+    dom = max(launched, key=ideal_s)
     d_ms, d_n = ktimes[dom]
     d_avg_s = d_ms / max(d_n, 1) / 1e3
     roof = roofline_of(alg[dom], alg["ops"][dom], d_avg_s, peaks)
