@@ -423,14 +423,15 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_kernel(FwdParams
   dispatch_block(p, dsm);
 }
 
-constexpr int kQuantGroups = kDispatchThreads / kQuantThreads;  // tokens per quant CTA
+constexpr int kQuantGroups = kDispatchThreads / kQuantThreads;  // tokens per quant CTA in flight, 256-thread groups
+constexpr int kQuantWarps = kDispatchThreads / 32;               // tokens per quant CTA in flight, one warp each
+constexpr int kGroupQuantMaxBs = 1216;  // the batch one pass of 304 quant CTAs covers with 256-thread groups
 
 // The first CTA (or the first disp_chunks CTAs, for large batches) dispatch;
-// the others quantise tokens, one per 256-thread group at a time.  The two
-// halves are independent: nothing the quant writes depends on the dispatch.
+// the others quantise tokens.  The two halves are independent: nothing the
+// quant writes depends on the dispatch.
 __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(FwdParams p) {
   extern __shared__ int32_t dsm[];
-  __shared__ float s_red[kQuantGroups][8];
   // the previous forward's GEMM2 may still read the workspace and write outputs
   grid_dependency_wait();
   grid_launch_dependents();
@@ -440,12 +441,22 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(Fwd
     else dispatch_chunk(p, dsm, blockIdx.x);
     return;
   }
-  // quant CTAs loop over tokens (at most two CTAs per SM), one token per
-  // 256-thread group at a time
-  const int group = threadIdx.x / kQuantThreads;
-  const int stride = (gridDim.x - nd) * kQuantGroups;
-  for (int t = (blockIdx.x - nd) * kQuantGroups + group; t < p.bs; t += stride)
-    quant_token(p, t, s_red[group], group);
+  // quant CTAs loop over tokens (at most two CTAs per SM).  Up to
+  // kGroupQuantMaxBs tokens, one token per 256-thread group at a time (4 a
+  // CTA in flight, one pass over the grid, and eight warps' loads in flight
+  // per token); above it, one token per warp (32 a CTA in flight): a prefill
+  // batch then takes one pass over the grid instead of several.
+  if (p.bs <= kGroupQuantMaxBs) {
+    __shared__ float s_red[kQuantGroups][8];
+    const int group = threadIdx.x / kQuantThreads;
+    const int stride = (gridDim.x - nd) * kQuantGroups;
+    for (int t = (blockIdx.x - nd) * kQuantGroups + group; t < p.bs; t += stride)
+      quant_token(p, t, s_red[group], group);
+  } else {
+    const int warp = threadIdx.x >> 5;
+    const int stride = (gridDim.x - nd) * kQuantWarps;
+    for (int t = (blockIdx.x - nd) * kQuantWarps + warp; t < p.bs; t += stride) quant_token_warp(p, t);
+  }
 }
 
 // Multi-CTA dispatch, second phase, one CTA per chunk: CTA g places the
@@ -515,7 +526,8 @@ size_t dispatch_smem_bytes(int E) {
 
 cudaError_t launch_dispatch_quant(const FwdParams& p, cudaStream_t s) {
   const int nd = p.disp_chunks > 1 ? p.disp_chunks : 1;
-  const int qblocks = (p.bs + kQuantGroups - 1) / kQuantGroups;
+  const int per_cta = p.bs <= kGroupQuantMaxBs ? kQuantGroups : kQuantWarps;
+  const int qblocks = (p.bs + per_cta - 1) / per_cta;
   const int blocks = nd + (qblocks < 2 * p.num_ctas ? qblocks : 2 * p.num_ctas);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pdl_config(dim3(blocks), dim3(kDispatchThreads), dispatch_smem_bytes(p.E), s, attr);

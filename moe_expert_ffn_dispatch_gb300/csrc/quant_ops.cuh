@@ -106,6 +106,75 @@ __device__ void quant_token(const FwdParams& p, int t, float* s_red, int group) 
   }
 }
 
+// The same quant of one row by one warp (no block barrier): each lane takes
+// every 32nd group of 8 values; the row maximum is a warp reduction, so the
+// codes and the scale are the ones quant_row computes.
+__device__ void quant_row_warp(const uint16_t* __restrict__ x, bool fp16, const float* __restrict__ smooth, int h,
+                               int8_t* __restrict__ q, float* __restrict__ scale_out) {
+  const int lane = threadIdx.x & 31;
+  const int n8 = h >> 3;
+  float amax = 0.0f;
+  for (int i = lane; i < n8; i += 32) {
+    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float f = act_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu), fp16);
+      if (smooth) f = __fmul_rn(f, smooth[i * 8 + j]);
+      amax = fmaxf(amax, fabsf(f));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (amax < kAmaxEps) amax = kAmaxEps;
+  const float m = __fdiv_rn(127.0f, amax);
+  for (int i = lane; i < n8; i += 32) {
+    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float f = act_bits_to_f32(static_cast<uint16_t>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu), fp16);
+      if (smooth) f = __fmul_rn(f, smooth[i * 8 + j]);
+      const uint32_t b = static_cast<uint8_t>(f32_to_q(__fmul_rn(f, m)));
+      packed[j >> 2] |= b << ((j & 3) * 8);
+    }
+    reinterpret_cast<uint2*>(q)[i] = make_uint2(packed[0], packed[1]);
+  }
+  if (lane == 0) *scale_out = __fdiv_rn(1.0f, m);
+}
+
+// quant_token by one warp.
+__device__ void quant_token_warp(const FwdParams& p, int t) {
+  const int lane = threadIdx.x & 31;
+  const bool act = (p.mask == nullptr) || (p.mask[t] != 0);
+  int nvalid = 0;
+  if (act)
+    for (int k = 0; k < p.topk; ++k) {
+      const int id = p.ids[t * p.topk + k];
+      nvalid += (id >= 0 && id < p.E);
+    }
+  const int n8 = p.h >> 3;
+  if (nvalid == 0) {
+    uint4* out = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * p.h);
+    for (int i = lane; i < n8; i += 32) out[i] = make_uint4(0, 0, 0, 0);
+  }
+  if (!act) {
+    if (p.has_shared) {
+      uint4* so = reinterpret_cast<uint4*>(p.sout + static_cast<size_t>(t) * p.h);
+      for (int i = lane; i < n8; i += 32) so[i] = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  const uint16_t* xr = p.x + static_cast<size_t>(t) * p.h;
+  if (!p.xq_per_row)
+    quant_row_warp(xr, p.act_fp16, p.smooth, p.h, ws_ptr<int8_t>(p, p.L.x_q) + static_cast<size_t>(t) * p.h,
+                   ws_ptr<float>(p, p.L.x_scale) + t);
+  if (p.has_shared && !p.share_uses_xq)
+    quant_row_warp(xr, p.act_fp16, p.ssmooth, p.h, ws_ptr<int8_t>(p, p.L.xs_q) + static_cast<size_t>(t) * p.h,
+                   ws_ptr<float>(p, p.L.xs_scale) + t);
+}
+
 // First item of CTA b (of G) in the small phase of one GEMM.  The small slots'
 // items are split by cost: an item of an expert with m rows streams the same
 // weight bytes as any other but does m dot products per weight, so it counts
