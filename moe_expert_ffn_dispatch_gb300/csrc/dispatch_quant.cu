@@ -459,10 +459,10 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_quant_kernel(Fwd
   }
 }
 
-// Multi-CTA dispatch, second phase, one CTA per chunk: CTA g places the
-// routed pairs of chunk g -- expert e's rows of chunk g start at
-// offsets[e] + (rows of e in the chunks before g) -- and CTA 0 then runs the
-// tail (counts, offsets, active list, slot tables, status, tickets).
+// Multi-CTA dispatch, second phase: CTA g < G places the routed pairs of
+// chunk g -- expert e's rows of chunk g start at offsets[e] + (rows of e in
+// the chunks before g) -- while CTA G runs the tail (counts, offsets, active
+// list, slot tables, status, tickets), which reads none of the placement.
 __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_finish_kernel(FwdParams p) {
   extern __shared__ int32_t dsm[];
   __shared__ int s_warp1[32];
@@ -470,6 +470,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_finish_kernel(Fw
   grid_launch_dependents();
   const int E = p.E, K = p.topk, nf = p.bs * K, G = p.disp_chunks;
   const int tid = threadIdx.x, g = blockIdx.x;
+  const bool tail = g == G;
   const int32_t* dcnt = ws_ptr<int32_t>(p, p.L.dcnt);
   int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of);
   int32_t* tk_of_row = ws_ptr<int32_t>(p, p.L.tk_of_row);
@@ -484,6 +485,14 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_finish_kernel(Fw
   }
   int R = 0;
   const int off = block_exclusive_scan(tot, &R, s_warp1);
+  if (tail) {
+    // skipped ids of all chunks (G < 1024: one per thread), then the tail
+    const int sk = tid < G ? dcnt[static_cast<size_t>(G) * E + tid] : 0;
+    int skipped = 0;
+    block_exclusive_scan(sk, &skipped, s_warp1);
+    dispatch_tail(p, dsm, tot, off, R, skipped);
+    return;
+  }
   if (tid < E) dsm[tid] = off + pre;
   __syncthreads();
   const int f_lo = g * kDispChunk, f_hi = min(nf, f_lo + kDispChunk);
@@ -505,13 +514,6 @@ __global__ void __launch_bounds__(kDispatchThreads, 1) dispatch_finish_kernel(Fw
         row_token[r] = f / K;
       }
     }
-  }
-  if (g == 0) {
-    int skipped = 0;
-    if (tid == 0)
-      for (int j = 0; j < G; ++j) skipped += dcnt[static_cast<size_t>(G) * E + j];
-    __syncthreads();  // every placement of chunk 0 has read dsm
-    dispatch_tail(p, dsm, tot, off, R, skipped);
   }
 }
 
@@ -538,7 +540,7 @@ cudaError_t launch_dispatch_finish(const FwdParams& p, cudaStream_t s) {
   if (p.bs == 0 || p.disp_chunks <= 1) return cudaSuccess;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg =
-      pdl_config(dim3(p.disp_chunks), dim3(kDispatchThreads), dispatch_smem_bytes(p.E), s, attr);
+      pdl_config(dim3(p.disp_chunks + 1), dim3(kDispatchThreads), dispatch_smem_bytes(p.E), s, attr);
   return cudaLaunchKernelEx(&cfg, dispatch_finish_kernel, p);
 }
 
