@@ -165,7 +165,10 @@ typedef struct moe_fused_handle moe_fused_handle_t;
 /* Validate `cfg`, allocate the host handle and report the workspace size in
  * bytes (device memory the caller allocates, 256-byte aligned, and passes to
  * every forward).  The device current at this call is the device the handle
- * launches on.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, CUDA. */
+ * launches on.  The handle also creates one non-blocking stream and three
+ * events of its own (the second engine's stream, see moe_fused_forward);
+ * moe_fused_destroy releases them.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
+ * CUDA. */
 int moe_fused_create(const moe_fused_config_t* cfg, moe_fused_handle_t** out_handle,
                      size_t* workspace_bytes);
 
@@ -177,14 +180,19 @@ int moe_fused_workspace_size(const moe_fused_config_t* cfg, size_t* workspace_by
  * Two forwards that share a workspace must be ordered on the GPU.
  * A batch of at most 8 tokens (without MOE_FLAG_EXPERT_SMOOTH smooth scales,
  * and unless MOE_FLAG_UNFUSED is set) runs as one launch whose CTAs meet at
- * one grid barrier; its arrival count lives in the workspace (status word 32,
- * word 33 its generation).  The handle zeroes that count, with one enqueued
- * 4-byte memset, the first time it runs such a forward on a workspace (and
- * again after moe_fused_get_status reported a wait that gave up); the kernel
- * leaves it at zero.  So the caller must not write a workspace's first 256
- * bytes (the status words) between forwards; the rest may be reused freely.
- * Errors: INVALID_ARG, UNSUPPORTED_SHAPE (bs > bs_max), WORKSPACE_TOO_SMALL,
- * ALIGNMENT, CUDA (launch failure). */
+ * one grid barrier (status word 32 its arrival count, word 33 its
+ * generation).  A larger batch on the fused path runs the dp4a launch on
+ * `stream` beside the tensor-core GEMMs on the handle's own stream, forked
+ * from `stream` after the dispatch and joined back before the combine (so a
+ * CUDA graph captured from `stream` holds both); launches whose CTAs take
+ * their work in arrival order count arrivals in status words 40..42.  These
+ * counters are zero between launches: the handle zeroes words 32..47, with
+ * one enqueued memset, the first time it runs such a forward on a workspace
+ * (and again after moe_fused_get_status reported a wait that gave up), and
+ * the kernels leave them at zero.  So the caller must not write a
+ * workspace's first 256 bytes (the status words) between forwards; the rest
+ * may be reused freely.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE
+ * (bs > bs_max), WORKSPACE_TOO_SMALL, ALIGNMENT, CUDA (launch failure). */
 int moe_fused_forward(moe_fused_handle_t* handle, const moe_fused_args_t* args, void* workspace,
                       size_t workspace_bytes, void* stream);
 
@@ -194,7 +202,8 @@ int moe_fused_forward(moe_fused_handle_t* handle, const moe_fused_args_t* args, 
 int moe_fused_get_status(moe_fused_handle_t* handle, const void* workspace, void* stream,
                          moe_fused_status_t* out);
 
-/* Free the handle (no device memory is owned).  NULL is accepted. */
+/* Free the handle, its stream and events (no device memory is owned).  NULL
+ * is accepted. */
 int moe_fused_destroy(moe_fused_handle_t* handle);
 
 /* Static string for an error code. */
