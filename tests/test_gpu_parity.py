@@ -309,13 +309,20 @@ def test_graphed_step_matches_eager_forward():
         host["expert_ids"].copy_(torch.roll(host["expert_ids"], 1, dims=0))
 
 
-def test_pipelined_steps_match_eager_forward():
+@pytest.mark.parametrize("which", ["engines_side_by_side", "one_launch"])
+def test_pipelined_steps_match_eager_forward(which):
     """The pipelined serving loop (two buffer sets; the copies on their own
     streams overlap the neighbouring steps' forwards) gives every step the
     eager forward's outputs bit for bit, with new inputs written for each step
-    and two steps in flight at a time."""
+    and two steps in flight at a time.  Its CUDA graphs hold either the two
+    engines side by side (a forked and joined second stream) or, for a batch
+    of 8 tokens, the one-launch forward with its grid barrier."""
     import moe_expert_ffn_dispatch_gb300 as m
-    wl = CASES[3]  # zipf_skew: small and tensor-core experts, masked tokens, the shared expert
+    if which == "one_launch":
+        wl = synth.custom("pipelined_bs8", bs=8, hidden=512, num_experts=32, topk=4, inter=256, has_shared=True,
+                          routing="zipf", masked_fraction=0.25, seed=96)
+    else:
+        wl = CASES[3]  # zipf_skew: small and tensor-core experts, masked tokens, the shared expert
     inp = synth.make_inputs(wl)
     blk = make_block(wl, DEV)
     di, dw = device_inputs(inp, DEV), device_weights(inp, DEV)
