@@ -160,6 +160,10 @@ typedef struct {
   int32_t reserved[2];
 } moe_fused_status_t;
 
+/* A handle holds host-side state between calls (tensor maps, the workspaces
+ * whose counters it has zeroed, timing records, its own stream): one host
+ * thread at a time may call into a given handle.  Distinct handles are
+ * independent. */
 typedef struct moe_fused_handle moe_fused_handle_t;
 
 /* Validate `cfg`, allocate the host handle and report the workspace size in
