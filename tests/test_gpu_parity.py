@@ -247,6 +247,11 @@ VARIANT_CASES = [
                  smooth_per_expert=True, seed=53),
     synth.custom("expert_smooth_big_blocks", bs=300, hidden=256, num_experts=4, topk=2, inter=128,
                  has_shared=True, smooth=True, smooth_per_expert=True, seed=54),
+    # more than 1216 tokens: the token quant runs one warp per token (fp16 x,
+    # smooth and share-smooth scales, masked tokens' zero rows)
+    synth.custom("warp_quant_fp16_smooth", bs=1300, hidden=256, num_experts=16, topk=2, inter=128,
+                 has_shared=True, masked_fraction=0.3, smooth=True, share_smooth=True, act_dtype="fp16",
+                 routing="zipf", seed=53),
 ]
 
 
