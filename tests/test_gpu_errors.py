@@ -87,3 +87,30 @@ def test_bounded_wait_runs_out_and_reports(which):
     torch.cuda.synchronize()
     st = blk.status()
     assert st["rc"] == m.MOE_OK and st["error_flags"] == 0
+
+
+def test_barrier_count_rezeroed_after_a_reported_timeout():
+    """A grid barrier that gave up can leave arrivals counted (status word 32).
+    Once get_status has reported a timeout on a workspace, the handle zeroes
+    that count again before the workspace's next one-launch forward, which
+    must then give the same outputs as before.  The leftover count is planted
+    here after a bounded debug wait ran out (no kernel is made to fail)."""
+    blk, a, keep, out = _setup()
+    ws = blk.workspace()
+    stream = torch.cuda.current_stream()
+    assert _fwd(blk, a) == m.MOE_OK
+    torch.cuda.synchronize()
+    ref = out.clone()
+    assert m.moe_fused_debug_wait_timeout(blk.handle, ws.data_ptr(), ws.numel(), 0, stream.cuda_stream) == m.MOE_OK
+    torch.cuda.synchronize()
+    status = blk.region("status", workspace=ws).view(torch.int32)
+    status[32] = 5  # arrivals a barrier that gave up could leave behind
+    torch.cuda.synchronize()
+    assert blk.status()["rc"] == m.MOE_ERR_DEVICE_TIMEOUT
+    out.fill_(7.0)
+    assert _fwd(blk, a) == m.MOE_OK
+    torch.cuda.synchronize()
+    st = blk.status()
+    assert st["rc"] == m.MOE_OK and st["error_flags"] == 0, st
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert int(blk.region("status", workspace=ws).view(torch.int32)[32]) == 0
