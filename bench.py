@@ -533,6 +533,8 @@ def run_ours(args, wl, ws, rank, local):
         res["active_tokens_per_s"] = whole_job_tokens_per_s(n_active, ws, args.steps, ms_total / 1e3)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+        if args.cpu_full:
+            res["cpu_baseline"]["full_forward"] = cpu_full_forward(wl)
     if ws > 1:
         torch.distributed.destroy_process_group()
     return res if rank == 0 else None
@@ -583,6 +585,20 @@ def cpu_baseline(wl, budget_s=15.0):
                   "every token, GEMMs and combine of the sampled tokens' %d routed rows and shared row), "
                   "weights pre-drawn on the host" % (n, wl.name, bs, chunk, n_tok, wl.topk))
     return {"value": n_tok / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
+
+
+def cpu_full_forward(wl):
+    """One whole forward of the workload by the oracle on the host cores
+    (every token, every row; weights drawn on the host before the clock starts)."""
+    oracle, inp, cache = _oracle_setup(wl)
+    threads = os.cpu_count() or 1
+    n_act = wl.bs if inp.mask is None else int(inp.mask.bool().sum())
+    t0 = time.perf_counter()
+    oracle.forward(inp, threads=threads, intermediates=False, expert_weights=lambda e: cache[e])
+    dt = time.perf_counter() - t0
+    return {"seconds": dt, "value": n_act / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "one full forward of %s (bs %d): every token and row, weights pre-drawn on the host"
+                      % (wl.name, wl.bs)}
 
 
 def run_reference(args, wl, ws, rank):
@@ -643,6 +659,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="also time one whole forward of the workload by the oracle (minutes at prefill)")
     ap.add_argument("--unfused", action="store_true",
                     help="MOE_FLAG_UNFUSED: the unfused chain (tensor-core GEMMs, separate requant and combine) "
                          "as an A/B baseline")
