@@ -162,8 +162,15 @@ typedef struct {
 
 /* A handle holds host-side state between calls (tensor maps, the workspaces
  * whose counters it has zeroed, timing records, its own stream): one host
- * thread at a time may call into a given handle.  Distinct handles are
- * independent. */
+ * thread at a time may call into a given handle.  Distinct handles share no
+ * host state.  On the GPU, forwards must not overlap one another: the
+ * one-launch forward (a grid barrier) and the small experts' streamed launch
+ * (GEMM2 work that waits on other CTAs' GEMM1 work) count on every CTA of
+ * the launch getting an SM, one CTA per SM.  Forwards issued in sequence
+ * (one stream, or streams ordered by events) meet that.  Two forwards in
+ * flight at once on one GPU (one handle or several, on unordered streams)
+ * can each hold SMs the other's waiting CTAs need; their bounded waits then
+ * give up after 2 s and get_status reports MOE_ERR_DEVICE_TIMEOUT. */
 typedef struct moe_fused_handle moe_fused_handle_t;
 
 /* Validate `cfg`, allocate the host handle and report the workspace size in
