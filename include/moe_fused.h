@@ -160,9 +160,8 @@ typedef struct {
   int32_t reserved[2];
 } moe_fused_status_t;
 
-/* A handle holds host-side state between calls (tensor maps, the workspaces
- * whose counters it has zeroed, timing records, its own stream): one host
- * thread at a time may call into a given handle.  Distinct handles share no
+/* A handle holds host-side state between calls (tensor maps, timing records,
+ * its own stream): one host thread at a time may call into a given handle.  Distinct handles share no
  * host state.  On the GPU, forwards must not overlap one another: the
  * one-launch forward (a grid barrier) and the small experts' streamed launch
  * (GEMM2 work that waits on other CTAs' GEMM1 work) count on every CTA of
@@ -191,19 +190,19 @@ int moe_fused_workspace_size(const moe_fused_config_t* cfg, size_t* workspace_by
  * Two forwards that share a workspace must be ordered on the GPU.
  * A batch of at most 8 tokens (without MOE_FLAG_EXPERT_SMOOTH smooth scales,
  * and unless MOE_FLAG_UNFUSED is set) runs as one launch whose CTAs meet at
- * one grid barrier (status word 32 its arrival count, word 33 its
- * generation).  A larger batch on the fused path runs the dp4a launch on
- * `stream` beside the tensor-core GEMMs on the handle's own stream, forked
- * from `stream` after the dispatch and joined back before the combine (so a
- * CUDA graph captured from `stream` holds both); launches whose CTAs take
- * their work in arrival order count arrivals in status words 40..42.  These
- * counters are zero between launches: the handle zeroes words 32..47, with
- * one enqueued memset, the first time it runs such a forward on a workspace
- * (and again after moe_fused_get_status reported a wait that gave up), and
- * the kernels leave them at zero.  So the caller must not write a
- * workspace's first 256 bytes (the status words) between forwards; the rest
- * may be reused freely.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE
- * (bs > bs_max), WORKSPACE_TOO_SMALL, ALIGNMENT, CUDA (launch failure). */
+ * one grid barrier; its words (a workspace region of their own) need no
+ * initial value: each CTA's arrival tag carries the barrier's generation
+ * mixed with a random constant of the handle.  A larger batch on the fused
+ * path runs the dp4a launch on `stream` beside the tensor-core GEMMs on the
+ * handle's own stream, forked from `stream` after the dispatch and joined
+ * back before the combine (so a CUDA graph captured from `stream` holds
+ * both); launches whose CTAs take their work in arrival order count arrivals
+ * in status words 40..42, which the forward's dispatch zeroes first.  So no
+ * state carries from one forward to the next: between forwards the caller
+ * may overwrite any part of the workspace (moe_fused_get_status reads the
+ * status words the last forward left).  Errors: INVALID_ARG,
+ * UNSUPPORTED_SHAPE (bs > bs_max), WORKSPACE_TOO_SMALL, ALIGNMENT, CUDA
+ * (launch failure). */
 int moe_fused_forward(moe_fused_handle_t* handle, const moe_fused_args_t* args, void* workspace,
                       size_t workspace_bytes, void* stream);
 

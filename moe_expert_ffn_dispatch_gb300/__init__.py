@@ -50,7 +50,7 @@ KERNEL_ID = {n: i for i, n in enumerate(KERNEL_NAMES)}
 REGIONS = {"status": 0, "counts": 1, "offsets": 2, "row_of": 3, "tk_of_row": 4, "active": 5, "x_q": 6,
            "x_scale": 7, "xs_q": 8, "xs_scale": 9, "h": 10, "x2": 11, "s2": 12, "y2": 13, "slots": 14,
            "row_token": 15, "shared_row": 16, "blk_ticket": 17, "tok_ticket": 18, "tok_expect": 19,
-           "ranges": 20, "x1h": 21, "x2h": 22, "dcnt": 23, "amax2": 24}
+           "ranges": 20, "x1h": 21, "x2h": 22, "dcnt": 23, "amax2": 24, "bar_tags": 25}
 
 EXPORTS = ["moe_fused_create", "moe_fused_workspace_size", "moe_fused_forward", "moe_fused_get_status",
            "moe_fused_destroy", "moe_fused_strerror", "moe_fused_set_timing", "moe_fused_get_timing",

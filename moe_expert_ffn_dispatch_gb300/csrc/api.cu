@@ -14,7 +14,9 @@
 // (moe_decode_one_launch_kernel).
 #include <cstdio>
 #include <cstring>
+#include <chrono>
 #include <new>
+#include <random>
 #include <vector>
 
 #include <cuda.h>
@@ -39,10 +41,8 @@ struct moe_fused_handle {
   moe::TcMaps maps;          // tensor maps of the last forward's operands
   const void* map_key[5];    // pointers they were built for
   bool maps_valid;
-  // workspaces whose cross-launch counters (the one-launch kernel's grid
-  // barrier, the arrival counters of side-by-side engines: status words
-  // 32..47) this handle has zeroed; the kernels leave them at zero
-  std::vector<const void*> barrier_ready;
+  // random constant mixed into the one-launch grid barrier's arrival tags
+  uint64_t bar_salt;
   // engines side by side: the tensor-core chain's stream, and the events of
   // the fork (after expand), of the tensor-core GEMM1's launch completion
   // (every CTA begun) and of the join (before the combine)
@@ -117,6 +117,7 @@ moe::WsLayout plan(const moe_fused_config_t& c) {
   const size_t chunks = routed > 4 * moe::kDispChunk ? (routed + moe::kDispChunk - 1) / moe::kDispChunk : 1;
   take(L.dcnt, chunks > 1 ? (chunks * E + chunks) * 4 : 0, moe::kRegDcnt);
   take(L.amax2, rows * 4, moe::kRegAmax2);
+  take(L.bar_tags, moe::kMaxCtas * sizeof(uint64_t), moe::kRegBarTags);
   L.total = off;
   return L;
 }
@@ -193,6 +194,7 @@ int build_params(moe_fused_handle* hd, const moe_fused_args_t* a, void* ws, size
   p->token_nums = a->expert_token_nums;
   p->ws = static_cast<char*>(ws);
   p->L = hd->L;
+  p->bar_salt = hd->bar_salt;
   return MOE_OK;
 }
 
@@ -336,6 +338,12 @@ int moe_fused_create(const moe_fused_config_t* cfg, moe_fused_handle_t** out_han
   hd->maps_valid = false;
   hd->side = nullptr;
   hd->ev_fork = hd->ev_started = hd->ev_join = nullptr;
+  {
+    std::random_device rd;
+    const uint64_t t = static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count());
+    hd->bar_salt = ((static_cast<uint64_t>(rd()) << 32) ^ rd()) ^ (t * 0x9E3779B97F4A7C15ull) ^
+                   static_cast<uint64_t>(reinterpret_cast<uintptr_t>(hd));
+  }
   cudaError_t e = cudaGetDevice(&hd->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&hd->num_sms, cudaDevAttrMultiProcessorCount, hd->device);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hd->side, cudaStreamNonBlocking);
@@ -381,28 +389,14 @@ int moe_fused_debug_forward_range(moe_fused_handle_t* hd, const moe_fused_args_t
   }
   // A batch of at most small_rows tokens with per-token quant: the whole
   // forward is one launch (dispatch and quant repeated per CTA, then the
-  // streamed GEMMs behind a grid barrier).  The barrier's arrival count must
-  // be zero before the workspace's first such forward; the kernel leaves it
-  // at zero.  After a wait that gave up it may not be: get_status, which
-  // reports that, makes the next forward zero it again.
+  // streamed GEMMs behind a grid barrier that needs no initial state).
   const bool one_launch =
       p.small_only && !p.xq_per_row && first_kernel == moe::kKDispatchQuant && last_kernel >= moe::kKGemm2Small;
   // A whole forward of a larger batch on the fused path runs the dp4a launch
   // and the tensor-core chain side by side (below); the dispatch splits the
-  // CTAs between them.
+  // CTAs between them and zeroes the launches' arrival counters.
   p.split_engines = p.small_rows > 0 && !p.small_only && first_kernel == moe::kKDispatchQuant &&
                     last_kernel == moe::kKCombine;
-  if (one_launch || p.split_engines) {
-    auto& known = hd->barrier_ready;
-    bool seen = false;
-    for (const void* w : known) seen = seen || (w == workspace);
-    if (!seen) {
-      e = cudaMemsetAsync(p.ws + p.L.status + sizeof(int32_t) * moe::kStBarArrive, 0, 16 * sizeof(int32_t), s);
-      if (e != cudaSuccess) return cuda_fail(e);
-      if (known.size() >= 64) known.erase(known.begin());
-      known.push_back(workspace);
-    }
-  }
   if (one_launch)
     return cuda_fail(timed(hd, moe::kKGemm1Small, s, [&] { return moe::launch_moe_decode_one_launch(p, s); }));
   rc = prepare_maps(hd, p);
@@ -498,17 +492,7 @@ int moe_fused_get_status(moe_fused_handle_t* hd, const void* workspace, void* st
   out->shared_rows = w[moe::kStSharedRows];
   out->active_slots = w[moe::kStSlots];
   out->reserved[0] = out->reserved[1] = 0;
-  if (out->error_flags & moe::kErrWaitTimeout) {
-    // a grid barrier that gave up can leave arrivals counted: zero the count
-    // again before this workspace's next one-launch forward
-    auto& known = hd->barrier_ready;
-    for (size_t i = 0; i < known.size(); ++i)
-      if (known[i] == workspace) {
-        known.erase(known.begin() + static_cast<long>(i));
-        break;
-      }
-    return MOE_ERR_DEVICE_TIMEOUT;
-  }
+  if (out->error_flags & moe::kErrWaitTimeout) return MOE_ERR_DEVICE_TIMEOUT;
   return MOE_OK;
 }
 
@@ -588,7 +572,7 @@ int moe_fused_debug_region(moe_fused_handle_t* hd, int region, size_t* offset, s
   const size_t offs[moe::kNumRegions] = {L.status, L.counts, L.offsets, L.row_of, L.tk_of_row, L.active, L.x_q,
                                          L.x_scale, L.xs_q, L.xs_scale, L.hbuf, L.x2, L.s2, L.y2, L.slots,
                                          L.row_token, L.shared_row, L.blk_ticket, L.tok_ticket, L.tok_expect,
-                                         L.ranges, L.x1h, L.x2h, L.dcnt, L.amax2};
+                                         L.ranges, L.x1h, L.x2h, L.dcnt, L.amax2, L.bar_tags};
   if (region < 0 || region >= moe::kNumRegions) return MOE_ERR_INVALID_ARG;
   *offset = offs[region];
   *bytes = L.sizes[region];

@@ -227,40 +227,88 @@ __device__ __forceinline__ bool spin_until_ge(const int32_t* flag, int want, vol
   }
 }
 
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Grid-wide barrier of a launch whose CTAs are all resident (one per SM),
-// called by one thread of each CTA.  *arrive counts the CTAs other than CTA 0
-// that have arrived and is zero between barriers; *release is the barrier's
-// generation.  A CTA reads the generation before it arrives and waits for it
-// to change; CTA 0 waits for the G - 1 arrivals, puts the count back to zero
-// and then advances the generation.  What a CTA wrote before the call (its
-// other threads' writes ordered by a CTA barrier first) is visible to every
-// CTA after it: a fence before each arrival, acquire loads on the way out.
-// Bounded: false once the wait budget runs out (reported in the status).
-__device__ __forceinline__ bool grid_barrier(int32_t* arrive, int32_t* release, int G, int32_t* status, int site) {
-  __threadfence();
+// called by one full warp of each CTA after a CTA barrier that orders the
+// CTA's other writes before it.  It needs no initial state: tags[0] (the
+// generation) and tags[1 .. G-1] may hold anything when the launch starts.
+// Every CTA reads the generation g; CTA b > 0 then writes its arrival tag
+// (g + 1) ^ salt to tags[b] and waits for the generation to change; CTA 0
+// waits until every tag reads (g + 1) ^ salt and then sets the generation to
+// g + 1.  The generation changes only after every CTA has arrived, so all
+// read the same g; the salt (a random constant of the caller) keeps any
+// earlier content of the words from passing for an arrival, and tags of an
+// earlier barrier carry an older generation.  Ordering: the tag and the new
+// generation are release stores (after the CTA barrier, and after CTA 0's
+// warp barrier), the generation is polled with acquire loads, and CTA 0's
+// lanes fence after the relaxed loads that saw the tags.  Bounded: a CTA
+// whose wait runs out reports it in the status and adds 2 to the
+// generation, so that the waiting CTAs stop (they see neither g nor g + 1)
+// and no tag written here matches a later barrier.  Returns false (on every
+// lane) if this CTA's barrier failed.
+__device__ __forceinline__ bool grid_barrier_tagged(uint64_t* tags, uint64_t salt, int G, int32_t* status,
+                                                    int site) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  const uint64_t g = __shfl_sync(0xffffffffu, lane == 0 ? ld_relaxed_gpu_u64(tags) : 0ull, 0);
+  const uint64_t want = (g + 1) ^ salt;
   const uint64_t t0 = global_timer_ns();
   uint32_t n = 0;
+  bool ok = true;
   if (blockIdx.x == 0) {
-    while (ld_acquire_gpu(arrive) != G - 1) {
-      if ((++n & 255u) == 0 && global_timer_ns() - t0 > kWaitBudgetNs) {
-        report_timeout(status, site);
-        return false;
+    while (true) {
+      // every tag of a pass loaded before any is compared: one round trip a pass
+      bool all = true;
+      for (int base = 1; base < G; base += 8 * 32) {
+        uint64_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int b = base + lane + 32 * j;
+          v[j] = b < G ? ld_relaxed_gpu_u64(tags + b) : want;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) all &= v[j] == want;
+      }
+      if (__all_sync(0xffffffffu, all)) break;
+      if ((++n & 63u) == 0 && __shfl_sync(0xffffffffu, global_timer_ns() - t0 > kWaitBudgetNs, 0)) {
+        ok = false;
+        break;
       }
     }
-    *reinterpret_cast<volatile int32_t*>(arrive) = 0;
-    __threadfence();
-    atomicAdd(release, 1);
-    return true;
-  }
-  const int gen = ld_acquire_gpu(release);
-  atomicAdd(arrive, 1);
-  while (ld_acquire_gpu(release) == gen) {
-    if ((++n & 255u) == 0 && global_timer_ns() - t0 > kWaitBudgetNs) {
-      report_timeout(status, site);
-      return false;
+    fence_acq_rel_gpu();  // acquire: what the CTAs wrote before their tags
+    __syncwarp();
+    if (ok && lane == 0) st_release_gpu_u64(tags, g + 1);
+  } else {
+    uint64_t v = g;
+    if (lane == 0) {
+      st_release_gpu_u64(tags + blockIdx.x, want);
+      while ((v = ld_acquire_gpu_u64(tags)) == g) {
+        if ((++n & 255u) == 0 && global_timer_ns() - t0 > kWaitBudgetNs) break;
+      }
     }
+    v = __shfl_sync(0xffffffffu, v, 0);
+    __syncwarp();
+    ok = v == g + 1;
   }
-  return true;
+  if (!ok && lane == 0) {
+    atomicAdd(reinterpret_cast<unsigned long long*>(tags), 2ull);
+    report_timeout(status, site);
+  }
+  return ok;
 }
 
 // Logical index of this CTA in a launch whose CTAs take their work in

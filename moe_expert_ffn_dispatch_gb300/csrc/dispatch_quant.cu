@@ -279,6 +279,8 @@ __device__ void dispatch_tail(const FwdParams& p, int32_t* dsm, int c, int off, 
     slots[SlotTable::kNumSmall] = n_small;
     slots[SlotTable::kSmallCtas] = p.split_engines ? small_phase_ctas(p, n_small, big_blk) : p.num_ctas;
     slots[SlotTable::kSplit] = p.split_engines ? 1 : 0;
+    // the arrival counters of the launches that follow (engines side by side)
+    for (int i = 0; i < 3; ++i) status[kStCtaCounter + i] = 0;
     status[kStSkipped] = s_skipped;
     status[kStErrorFlags] = 0;
     status[kStErrorSite] = 0;

@@ -802,8 +802,9 @@ __device__ void publish_dispatch(const FwdParams& p, const int32_t* td) {
 // The consumers' part of the one-launch prologue after the local dispatch:
 // CTA 0 publishes it, every CTA clears its share of the row-block tickets,
 // CTA (1 + t) mod G quantises token t (and writes the zero rows of tokens
-// that nothing combines into); then the grid barrier, and the `ready`
-// barrier tells this CTA's producer that it may read what other CTAs wrote.
+// that nothing combines into); then the grid barrier (run by the first
+// consumer warp), and the `ready` barrier tells this CTA's producer that it
+// may read what other CTAs wrote.
 // false (for every consumer) if the grid barrier gave up.
 __device__ bool publish_and_quant(const FwdParams& p, char* smem) {
   const int ctid = threadIdx.x;
@@ -821,10 +822,12 @@ __device__ bool publish_and_quant(const FwdParams& p, char* smem) {
     if ((1 + t) % G == b) quant_token(p, t, s_red, 0);
   consumer_sync();
   bool ok = true;
-  if (ctid == 0) {
-    ok = grid_barrier(status + kStBarArrive, status + kStBarRelease, G, status, kKGemm1Small * 16 + 7);
-    if (!ok) *abort_flag = 1;
-    mbar_arrive(ready);
+  if (ctid < 32) {  // the first consumer warp
+    ok = grid_barrier_tagged(ws_ptr<uint64_t>(p, p.L.bar_tags), p.bar_salt, G, status, kKGemm1Small * 16 + 7);
+    if (ctid == 0) {
+      if (!ok) *abort_flag = 1;
+      mbar_arrive(ready);
+    }
   }
   return !consumer_sync_or(!ok);
 }

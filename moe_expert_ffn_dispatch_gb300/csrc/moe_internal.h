@@ -16,13 +16,9 @@ enum StatusWord : int {
   kStRows = 3,
   kStSharedRows = 4,
   kStSlots = 5,
-  // grid barrier of the one-launch decode kernel: arrivals of the CTAs other
-  // than CTA 0 (zero between barriers), and the barrier's generation
-  kStBarArrive = 32,
-  kStBarRelease = 33,
   // arrival counters of the GEMM launches whose CTAs take their work in
-  // arrival order (engines side by side): small, big GEMM1, big GEMM2; zero
-  // between launches
+  // arrival order (engines side by side): small, big GEMM1, big GEMM2; the
+  // dispatch zeroes them every forward, before those launches start
   kStCtaCounter = 40,
 };
 constexpr int kErrWaitTimeout = 1;
@@ -58,6 +54,8 @@ struct WsLayout {
   size_t x2h;        // [rows, I] f16: GEMM2 token operand of the rows in big blocks
   size_t dcnt;       // multi-CTA dispatch: [chunks][E] rows per (chunk, expert), then [chunks] skipped ids
   size_t amax2;      // [rows] f32 bits: max |h| of each tensor-core row (atomic max from the GEMM1 epilogue)
+  size_t bar_tags;   // [kMaxCtas] u64: the one-launch kernel's grid barrier (word 0 its generation, word b
+                     // the arrival tag of CTA b); any initial content works
   size_t total;
   size_t sizes[32];  // bytes per region id (debug_region)
 };
@@ -66,7 +64,8 @@ struct WsLayout {
 enum Region : int {
   kRegStatus = 0, kRegCounts, kRegOffsets, kRegRowOf, kRegTkOfRow, kRegActive, kRegXq, kRegXScale,
   kRegXsq, kRegXsScale, kRegH, kRegX2, kRegS2, kRegY2, kRegSlots, kRegRowToken, kRegSharedRow,
-  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kRegRanges, kRegX1h, kRegX2h, kRegDcnt, kRegAmax2, kNumRegions
+  kRegBlkTicket, kRegTokTicket, kRegTokExpect, kRegRanges, kRegX1h, kRegX2h, kRegDcnt, kRegAmax2, kRegBarTags,
+  kNumRegions
 };
 
 constexpr int kMaxCtas = 1023;  // persistent grid size limit (one CTA per SM)
@@ -122,6 +121,7 @@ struct FwdParams {
   int32_t act_fp16;       // x, y2 and the outputs are fp16 (else bf16)
   int32_t scale_dtype;    // routed weight scales: 0 fp32, 1 bf16, 2 fp16
   int32_t xq_per_row;     // per-expert smooth: routed x_q / x_scale are indexed by row, not token
+  uint64_t bar_salt;      // the handle's random constant mixed into the grid barrier's arrival tags
   const uint16_t* x;
   const int32_t* ids;
   const float* scales;
