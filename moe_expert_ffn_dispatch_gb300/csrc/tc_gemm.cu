@@ -920,7 +920,8 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
     if (p.xq_per_row && tab.exp[sl] >= 0) continue;  // quantised and copied above
     const int r = tab.row0[sl] + (g - tab.rpre[sl]);
     // lane l converts codes 8 c .. 8 c + 7 for c = l, l + 32, ...: every warp
-    // store covers 512 contiguous bytes of the f16 row
+    // store covers 512 contiguous bytes of the f16 row; streaming (evict-first)
+    // stores, since GEMM1 reads these rows once, after the whole pass
     const uint2* src = reinterpret_cast<const uint2*>((tab.exp[sl] >= 0 ? xq : xsq) +
                                                       static_cast<size_t>(row_token[r]) * p.h);
     uint4* dst = reinterpret_cast<uint4*>(x1h + static_cast<size_t>(r) * p.h);
@@ -936,7 +937,7 @@ __global__ void __launch_bounds__(256) expand_kernel(FwdParams p) {
         if (c < n8) {
           uint4 lo16, hi16;
           int8x16_to_f16(make_uint4(v[u].x, v[u].y, 0u, 0u), lo16, hi16);
-          dst[c] = lo16;
+          __stcs(dst + c, lo16);
         }
       }
     }
@@ -953,8 +954,11 @@ __device__ __forceinline__ void quant_store4(float4 v, float inv, int c, __half2
   int8_t q[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) q[j] = f32_to_q(__fmul_rn(__fmul_rn(f[j], 127.0f), inv));
-  h2[2 * c] = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
-  h2[2 * c + 1] = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
+  const __half2 a = __halves2half2(__int2half_rn(q[0]), __int2half_rn(q[1]));
+  const __half2 b = __halves2half2(__int2half_rn(q[2]), __int2half_rn(q[3]));
+  // one streaming 8-byte store of the four codes (GEMM2 reads them once)
+  __stcs(reinterpret_cast<uint2*>(h2) + c,
+         make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b)));
 }
 
 constexpr int kRqWarps = 8;          // rows in flight per CTA (one per warp)
