@@ -78,10 +78,10 @@ __device__ void requant_rows(const FwdParams& p, int r0, int n, float* s_red, in
   }
 }
 
-// Combine of token t, by the consumer threads (y2 through L2): each thread
-// owns 8 output columns at a time, issues the loads of up to 8 expert rows
-// before using any, and adds the terms in ascending k (fp32, each product and
-// each sum rounded once, from 0.0f).
+// Combine of token t, by the consumer threads (y2 through L2, evict-first:
+// each row is read once): each thread owns 8 output columns at a time, issues
+// the loads of up to 8 expert rows before using any, and adds the terms in
+// ascending k (fp32, each product and each sum rounded once, from 0.0f).
 __device__ void combine_token(const FwdParams& p, int t, int ctid) {
   const int h = p.h, K = p.topk, n8 = h >> 3;
   const int32_t* row_of = ws_ptr<int32_t>(p, p.L.row_of) + static_cast<size_t>(t) * K;
@@ -98,7 +98,7 @@ __device__ void combine_token(const FwdParams& p, int t, int ctid) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         r[u] = (k0 + u < K) ? row_of[k0 + u] : -1;
-        if (r[u] >= 0) v[u] = __ldcg(reinterpret_cast<const uint4*>(y2 + static_cast<size_t>(r[u]) * h) + i);
+        if (r[u] >= 0) v[u] = __ldcs(reinterpret_cast<const uint4*>(y2 + static_cast<size_t>(r[u]) * h) + i);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
