@@ -1,5 +1,6 @@
-"""Host-side helpers of bench.py that decide whether a committed ncu summary
-still describes the current kernel code (no GPU)."""
+"""Host-side helpers of bench.py (no GPU): whether a committed ncu summary
+still describes the current kernel code, per-forward percentiles, the clock
+sampler, the algorithmic-byte accounting and the whole-forward CPU baseline."""
 import os
 
 import bench
@@ -93,3 +94,18 @@ def test_algorithmic_bytes_follow_the_kernel_that_runs_each_expert():
     w = 2 * I * h + h * I + 4 * (2 * I + h)
     assert a["step"] == 4 * w + 8 * h * 2 + 8 * 4 * 8 + 8 * h * 2 + 4 * 4
     assert b["step"] == 4 * w + 16 * h * 2 + 16 * 2 * 8 + 16 * h * 2 + 4 * 4
+
+
+def test_cpu_full_forward_counts_active_tokens_of_one_whole_forward():
+    """bench --cpu-full: one whole oracle forward of the workload, timed on the
+    host cores, its rate over the active tokens only."""
+    import synth
+    wl = synth.custom("cpu_full", bs=16, hidden=128, num_experts=8, topk=2, inter=64, has_shared=True,
+                      masked_fraction=0.25, seed=5)
+    inp = synth.make_inputs(wl, with_weights=False)
+    n_act = int(inp.mask.bool().sum())
+    assert 0 < n_act < wl.bs
+    r = bench.cpu_full_forward(wl)
+    assert r["kind"] == "oracle" and r["unit"] == "tokens/s" and r["cores"] >= 1
+    assert r["seconds"] > 0 and abs(r["value"] * r["seconds"] - n_act) < 1e-6 * n_act
+    assert "one full forward of cpu_full (bs 16)" in r["sample"]
