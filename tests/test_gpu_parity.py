@@ -384,3 +384,25 @@ def test_random_shapes_staged_parity(wl):
     inp = synth.make_inputs(wl)
     blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True)
     check_raw_accumulators(blk, inp, ref, di, dw, DEV)
+
+
+HALF_TILE_ROWS = [1, 8, 9, 16, 17, 32, 33, 48, 63, 64, 65, 80, 96, 128]
+
+
+def test_block_row_counts_at_every_half_tile_boundary():
+    """Experts with exactly 1, 8, 9, 16, 17, 32, 33, 48, 63, 64, 65, 80, 96
+    and 128 rows (top-1), and a 660-row shared expert whose last block has 20:
+    the tensor-core epilogues' half tiles of every size class (SwiGLU over 8
+    or 16 slots a lane for halves of at most 16 / 32 rows, the 32-slot form
+    above; GEMM2's chunked loop below 64 rows, its single loop at 64) staged
+    against the oracle, GEMM2 and the combine bit-exact on planted codes, and
+    the raw accumulators of both GEMMs."""
+    bs = sum(HALF_TILE_ROWS)
+    wl = synth.custom("half_tile_sizes", bs=bs, hidden=256, num_experts=len(HALF_TILE_ROWS), topk=1, inter=128,
+                      has_shared=True, seed=95)
+    inp = synth.make_inputs(wl)
+    flat = torch.cat([torch.full((r,), e, dtype=torch.int32) for e, r in enumerate(HALF_TILE_ROWS)])
+    inp.expert_ids = flat[synth.permutation(95, 1, bs)].view(bs, 1).contiguous()
+    blk, ref, (di, dw) = run_and_check(inp, DEV, staged=True)
+    assert ref["expert_token_nums"].tolist() == HALF_TILE_ROWS
+    check_raw_accumulators(blk, inp, ref, di, dw, DEV)
