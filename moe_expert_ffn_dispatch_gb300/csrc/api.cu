@@ -339,10 +339,18 @@ int moe_fused_create(const moe_fused_config_t* cfg, moe_fused_handle_t** out_han
   hd->side = nullptr;
   hd->ev_fork = hd->ev_started = hd->ev_join = nullptr;
   {
-    std::random_device rd;
+    // the grid barrier's salt: random where the platform has an entropy
+    // source, else the clock and the handle's address alone (no exception
+    // leaves this C entry point)
     const uint64_t t = static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count());
-    hd->bar_salt = ((static_cast<uint64_t>(rd()) << 32) ^ rd()) ^ (t * 0x9E3779B97F4A7C15ull) ^
-                   static_cast<uint64_t>(reinterpret_cast<uintptr_t>(hd));
+    uint64_t r = 0;
+    try {
+      std::random_device rd;
+      r = (static_cast<uint64_t>(rd()) << 32) ^ rd();
+    } catch (...) {
+      r = 0;
+    }
+    hd->bar_salt = r ^ (t * 0x9E3779B97F4A7C15ull) ^ static_cast<uint64_t>(reinterpret_cast<uintptr_t>(hd));
   }
   cudaError_t e = cudaGetDevice(&hd->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&hd->num_sms, cudaDevAttrMultiProcessorCount, hd->device);
