@@ -221,7 +221,13 @@ cudaError_t timed(moe_fused_handle* hd, int kernel, cudaStream_t s, F fn) {
   if (e != cudaSuccess) return e;
   e = cudaEventRecord(r.stop, s);
   if (e != cudaSuccess) return e;
-  hd->records.push_back(r);
+  try {
+    hd->records.push_back(r);
+  } catch (...) {  // no exception leaves a C entry point
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+    return cudaErrorMemoryAllocation;
+  }
   return cudaSuccess;
 }
 
@@ -554,8 +560,16 @@ int moe_fused_get_timing(moe_fused_handle_t* hd, float* ms, int32_t* launches, i
       ms[r.kernel] += t;
       launches[r.kernel] += 1;
     }
-    hd->pool.push_back(r.start);
-    hd->pool.push_back(r.stop);
+    try {
+      hd->pool.push_back(r.start);
+    } catch (...) {
+      cudaEventDestroy(r.start);
+    }
+    try {
+      hd->pool.push_back(r.stop);
+    } catch (...) {
+      cudaEventDestroy(r.stop);
+    }
   }
   hd->records.clear();
   if (err != cudaSuccess) return cuda_fail(err);

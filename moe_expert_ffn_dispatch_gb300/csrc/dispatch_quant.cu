@@ -632,8 +632,8 @@ bool current_context_id(unsigned long long* id) {
 
 // Device address of the static scratch in the current context; the first
 // call in a context looks it up (and sets the dispatch kernel's attribute).
-char* noalloc_scratch() {
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+// Called under g_noalloc_mu.
+char* noalloc_scratch_locked() {
   unsigned long long id = 0;
   if (!current_context_id(&id)) return nullptr;
   if (id == 0) {
@@ -657,6 +657,17 @@ char* noalloc_scratch() {
   }
   g_noalloc_ctx[slot] = NoallocCtx{id, static_cast<char*>(ptr)};
   return static_cast<char*>(ptr);
+}
+
+// noalloc_scratch_locked under the lock; nullptr also if taking the lock
+// fails (no exception leaves the C entry point that calls this)
+char* noalloc_scratch() {
+  try {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    return noalloc_scratch_locked();
+  } catch (...) {
+    return nullptr;
+  }
 }
 
 // Scratch layout inside the static array for (bs, topk, E).
