@@ -22,7 +22,12 @@
 // full tiles a stage takes about 1050 cycles against 512 cycles of tensor
 // work (an isolated M128 N128 K16 MMA takes 64 cycles, random operands or
 // not), and taking out the token copies, the conversion arithmetic, the
-// tensor-memory stores or half of the MMAs each gains only 1-4 %.  For
+// tensor-memory stores or half of the MMAs each gains only 1-4 %.  With all
+// of them taken out the bare handshake ring (the same waits, arrivals and
+// commits) still costs about 470 cycles a stage under this kernel's load,
+// and each kind of work adds to it instead of hiding under it; 256-K stages,
+// one accumulator with six weight slots, converting ahead of the free slot
+// and sleeping pollers were each no faster.  For
 // GEMM1 the 128 rows are 64 gate rows and the 64 matching up rows, laid out
 // so that each 32-lane quadrant of tensor memory holds 16 gate rows in its
 // lanes 0..15 and the 16 matching up rows in lanes 16..31 (every warp
